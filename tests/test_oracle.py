@@ -1,0 +1,450 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: scipy's
+Hadamard construction, the Sylvester recursion, closed forms and identities
+the pages state, hand-derived worked examples under tests/golden/, brute-force
+loops, and the error bounds the pages publish.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+from oracle import kvint4_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+HEADS = [2, 4, 6, 64, 96, 128, 192, 256]
+
+
+def _bf16_values(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+    return x.to(torch.float64).numpy()
+
+
+def _signs(d, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randint(0, 2, (d,), generator=g) * 2 - 1).numpy().astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Hadamard / rotation (PR #56198 page; PR #62881 page, Details / Root cause)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 32, 64, 128, 256])
+def test_hadamard_matches_scipy_sylvester(b):
+    assert np.array_equal(O.hadamard(b), scipy.linalg.hadamard(b).astype(np.float64))
+
+
+def test_hadamard_textbook_h2_and_recursion():
+    assert np.array_equal(O.hadamard(2), np.array([[1.0, 1.0], [1.0, -1.0]]))
+    for b in [1, 2, 4, 8, 16, 32, 64, 128]:
+        h = O.hadamard(b)
+        h2 = np.block([[h, h], [h, -h]])
+        assert np.array_equal(O.hadamard(2 * b), h2)
+
+
+@pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 32, 64, 128, 256])
+def test_hadamard_orthogonal_up_to_b(b):
+    h = O.hadamard(b)
+    assert np.array_equal(h @ h.T, b * np.eye(b))
+
+
+@pytest.mark.parametrize("d,b,n", [(96, 32, 3), (192, 64, 3), (128, 128, 1), (64, 64, 1),
+                                   (256, 256, 1), (80, 16, 5), (6, 2, 3), (2, 2, 1)])
+def test_largest_pow2_divisor_and_block_layout(d, b, n):
+    assert O.largest_pow2_divisor(d) == b
+    hb = O.block_hadamard(d)
+    expect = np.kron(np.eye(n), scipy.linalg.hadamard(b))
+    assert np.array_equal(hb, expect)
+    assert np.array_equal(hb @ hb.T, b * np.eye(d))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_power_of_two_heads_take_unblocked_path(d):
+    x = _bf16_values((5, d), 1)
+    s = _signs(d, 2)
+    y = O.rht_forward(x, s)
+    ref = (x * s) @ scipy.linalg.hadamard(d).T
+    assert np.array_equal(y, ref)
+
+
+def test_signs_are_an_involution():
+    from int4_token_head_gb300 import synthetic
+    for name in ["tiny", "phi3", "mixed"]:
+        w = synthetic.make_workload(name)
+        s = w.signs.numpy().astype(np.float64)
+        assert set(np.unique(s)) <= {-1.0, 1.0}
+        dmat = np.diag(s)
+        assert np.array_equal(dmat @ dmat, np.eye(len(s)))
+
+
+@pytest.mark.parametrize("d", HEADS)
+def test_rotated_inner_product_preserved(d):
+    """q'.K_s / b = q.k before quantisation (fp64)."""
+    b = O.largest_pow2_divisor(d)
+    rng = np.random.default_rng(d)
+    q = rng.standard_normal((7, d))
+    k = rng.standard_normal((11, d))
+    s = _signs(d, d + 1)
+    lhs = O.rht_forward(q, s) @ O.rht_forward(k, s).T / b
+    rhs = q @ k.T
+    assert np.max(np.abs(lhs - rhs)) <= 1e-12 * np.max(np.abs(rhs)) * d
+
+
+@pytest.mark.parametrize("d", HEADS)
+def test_inverse_rotation_round_trip_exact(d):
+    x = _bf16_values((9, d), d)
+    s = _signs(d, 3 * d)
+    back = O.rht_inverse(O.rht_forward(x, s), s)
+    assert np.array_equal(back, x)
+
+
+def test_rotation_order_is_D_then_H():
+    # H.D.x differs from D.H.x; the golden fixtures fix the order, this pins
+    # that the two are really distinguishable on the fixture's input.
+    x = np.array([4.75, 2.25])
+    s = np.array([1.0, -1.0])
+    h = scipy.linalg.hadamard(2)
+    assert np.array_equal(O.rht_forward(x, s), h @ (s * x))
+    assert not np.array_equal(O.rht_forward(x, s), s * (h @ x))
+
+
+# --------------------------------------------------------------------------
+# bf16 rounding (PR #62881 page, Details / Fix: "rounding through bf16")
+# --------------------------------------------------------------------------
+
+def test_round_bf16_agrees_with_torch_on_fp32_inputs():
+    g = torch.Generator().manual_seed(5)
+    x32 = torch.randn(200000, generator=g) * torch.exp(torch.randn(200000, generator=g) * 8)
+    ref = x32.to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_bf16(x32.to(torch.float64).numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_round_bf16_is_nearest_with_ties_to_even_brute_force():
+    rng = np.random.default_rng(11)
+    xs = rng.standard_normal(3000) * np.exp2(rng.integers(-20, 20, 3000))
+    grid_cache = {}
+    for x in xs:
+        r = O.round_bf16(np.array([x]))[0]
+        m, e = math.frexp(abs(x))
+        q = 2.0 ** (e - 8)
+        lo = math.floor(abs(x) / q) * q
+        cands = [lo, lo + q]
+        dist = [abs(abs(x) - c) for c in cands]
+        if dist[0] < dist[1]:
+            want = cands[0]
+        elif dist[1] < dist[0]:
+            want = cands[1]
+        else:  # tie: even significand
+            want = cands[0] if int(round(cands[0] / q)) % 2 == 0 else cands[1]
+        assert r == math.copysign(want, x)
+    # explicit ties
+    assert O.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert O.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2 * 2.0 ** -7
+    assert O.round_bf16(np.array([2.5078125]))[0] == 2.5
+
+
+def test_round_bf16_specials():
+    assert O.round_bf16(np.array([0.0]))[0] == 0.0
+    assert np.isinf(O.round_bf16(np.array([3.5e38]))[0])
+    assert np.isnan(O.round_bf16(np.array([np.nan]))[0])
+    # subnormal spacing 2^-133
+    assert O.round_bf16(np.array([3 * 2.0 ** -134]))[0] == 2 * 2.0 ** -133
+
+
+def test_rht_bf16_error_within_pages_bounds():
+    """Relative error of the bf16-rounded rotation vs fp64 stays under the
+    figures the PR #56198 page reports (3.56e-3 at d=128, 3.99e-3 at 96,
+    3.52e-3 at 192)."""
+    for d, bound in [(128, 3.56e-3), (96, 3.99e-3), (192, 3.52e-3)]:
+        x = _bf16_values((2048, d), d)
+        s = _signs(d, d)
+        exact = O.rht_forward(x, s)
+        rounded = O.rotate_for_cache(x, s)
+        rel = np.linalg.norm(rounded - exact) / np.linalg.norm(exact)
+        assert rel <= bound
+        assert rel > 1e-4  # it really was rounded
+
+
+# --------------------------------------------------------------------------
+# Quantiser and packing
+# --------------------------------------------------------------------------
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _load("write_examples.json")["cases"], ids=lambda c: c["name"])
+def test_golden_write_examples(case):
+    x = np.array(case["x"], dtype=np.float64)
+    s = np.array(case["signs"], dtype=np.float64)
+    y = O.rotate_for_cache(x[None], s)
+    assert np.array_equal(y[0], np.array(case["y_bf16"]))
+    codes, scale = O.quantize(y)
+    assert codes[0].tolist() == case["codes"]
+    assert float(scale[0]) == case["scale"]
+    assert O.pack_codes(codes)[0].tolist() == case["bytes"]
+    # through the cache writer, one token in slot 3 of a 1-block cache
+    d = len(x)
+    kc = np.full((1, 16, 1, d // 2), 0xA5, np.uint8)
+    vc = kc.copy()
+    ks = np.full((1, 16, 1), np.nan, np.float32)
+    vs = ks.copy()
+    O.write_cache(x[None, None], x[None, None], [3], kc, vc, ks, vs, 16, s)
+    assert kc[0, 3, 0].tolist() == case["bytes"]
+    assert float(ks[0, 3, 0]) == case["scale"]
+    untouched = np.delete(np.arange(16), 3)
+    assert (kc[0, untouched] == 0xA5).all() and np.isnan(ks[0, untouched]).all()
+
+
+def test_pack_unpack_round_trip_and_nibble_order():
+    codes = np.array([[1, -1, 7, -8, 0, 3, -4, 5]], dtype=np.int8)
+    p = O.pack_codes(codes)
+    assert p.tolist() == [[0xF1, 0x87, 0x30, 0x5C]]
+    all_codes = np.array(np.meshgrid(np.arange(-8, 8), np.arange(-8, 8))).reshape(2, -1).T
+    assert np.array_equal(O.unpack_codes(O.pack_codes(all_codes)), all_codes)
+
+
+@pytest.mark.parametrize("d", [64, 96, 128, 192, 256])
+def test_quantizer_invariants(d):
+    y = O.rotate_for_cache(_bf16_values((4096, d), d, scale=3.0), _signs(d, 1))
+    c, s = O.quantize(y)
+    assert np.abs(c).max() <= 7
+    # the element reaching absmax maps to +-7
+    i = np.argmax(np.abs(y), axis=1)
+    top = c[np.arange(len(c)), i]
+    assert np.array_equal(np.abs(top), np.full(len(c), 7))
+    # |y - c s| <= s/2 (plus the fp32 reciprocal's relative error)
+    err = np.abs(y - c * s.astype(np.float64)[:, None])
+    assert (err <= s.astype(np.float64)[:, None] * (0.5 + 1e-6)).all()
+    # the stored scale is the fp32-rounded absmax/7
+    a = np.abs(y).max(axis=1)
+    assert (np.abs(s.astype(np.float64) - a / 7) <= a / 7 * 2.0 ** -24).all()
+    # the clamp is a guard only: never active
+    raw = np.rint(y * (np.float32(1) / s).astype(np.float64)[:, None])
+    assert np.abs(raw).max() <= 7
+
+
+def test_quantizer_degenerate_vectors():
+    c, s = O.quantize(np.zeros((1, 8)))
+    assert (c == 0).all() and s[0] == 0
+    tiny = np.array([[2.0 ** -121, -(2.0 ** -122), 0, 0]])
+    c, s = O.quantize(tiny)
+    assert (c == 0).all() and s[0] == 0
+    just = np.array([[2.0 ** -120, 0, 0, 0]])
+    c, s = O.quantize(just)
+    assert c[0].tolist() == [7, 0, 0, 0] and s[0] > 0   # the flush bound is exclusive
+    exact = np.array([[7 * 2.0 ** -120, -3.5 * 2.0 ** -120, 0, 0]])
+    c, s = O.quantize(exact)
+    assert c[0].tolist() == [7, -4, 0, 0] and s[0] == 2.0 ** -120  # -3.5 ties to -4
+
+
+def test_dequant_round_trip_within_pages_tolerance():
+    """Inverse-rotated dequantised values match the input at the INT4
+    round-trip tolerance deq_atol = deq_rtol = 0.5 used in the pages' tests
+    (PR #40835 review thread)."""
+    for d in [96, 128, 192]:
+        # a test-sized tensor (block 16 x 4 heads, as in the pages' test ids)
+        x = _bf16_values((64, d), d)
+        s = _signs(d, d)
+        c, sc = O.quantize(O.rotate_for_cache(x, s))
+        back = O.dequantize_original(c, sc, s)
+        assert np.all(np.abs(back - x) <= 0.5 + 0.5 * np.abs(x))
+        # a large tensor: the error is the rotated-domain rounding error
+        # (uniform, rms s/sqrt(12)) spread by the orthogonal-up-to-b inverse
+        # rotation, i.e. rms s / sqrt(12 b) per original-domain element.
+        x = _bf16_values((4000, d), d + 7)
+        c, sc = O.quantize(O.rotate_for_cache(x, s))
+        back = O.dequantize_original(c, sc, s)
+        b = O.largest_pow2_divisor(d)
+        pred = math.sqrt(np.mean(sc.astype(np.float64) ** 2) / (12 * b))
+        rms = math.sqrt(np.mean((back - x) ** 2))
+        assert abs(rms / pred - 1) < 0.05
+        assert np.mean(np.abs(back - x) <= 0.5 + 0.5 * np.abs(x)) > 0.9999
+
+
+def test_write_scatter_slots_and_padding():
+    d, hkv, bs, nb = 8, 2, 4, 3
+    x = _bf16_values((5, hkv, d), 3)
+    s = _signs(d, 4)
+    kc = np.full((nb, bs, hkv, d // 2), 0xA5, np.uint8)
+    vc = kc.copy()
+    ks = np.full((nb, bs, hkv), np.nan, np.float32)
+    vs = ks.copy()
+    slots = [5, -1, 0, 11, 12]  # 12 is out of range, -1 is padding
+    bad = O.write_cache(x, -x, slots, kc, vc, ks, vs, bs, s)
+    assert bad == [12]
+    written = {5: 0, 0: 2, 11: 3}
+    for slot in range(nb * bs):
+        blk, off = divmod(slot, bs)
+        if slot in written:
+            t = written[slot]
+            c, sc = O.quantize(O.rotate_for_cache(x[t], s))
+            assert np.array_equal(kc[blk, off], O.pack_codes(c))
+            assert np.array_equal(ks[blk, off], sc)
+            cv, _ = O.quantize(O.rotate_for_cache(-x[t], s))
+            assert np.array_equal(vc[blk, off], O.pack_codes(cv))
+        else:
+            assert (kc[blk, off] == 0xA5).all() and np.isnan(ks[blk, off]).all()
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def _cache_from_codes(k_codes, v_codes, scale, hkv, d, bs=16, nb=1):
+    kc = np.zeros((nb, bs, hkv, d // 2), np.uint8)
+    vc = kc.copy()
+    ks = np.zeros((nb, bs, hkv), np.float32)
+    vs = ks.copy()
+    for t, (ck, cv) in enumerate(zip(k_codes, v_codes)):
+        kc[t // bs, t % bs, 0] = O.pack_codes(np.array(ck, np.int8))
+        vc[t // bs, t % bs, 0] = O.pack_codes(np.array(cv, np.int8))
+        ks[t // bs, t % bs, 0] = scale
+        vs[t // bs, t % bs, 0] = scale
+    return kc, vc, ks, vs
+
+
+@pytest.mark.parametrize("case", _load("attention_examples.json")["cases"], ids=lambda c: c["name"])
+def test_golden_attention_examples(case):
+    g = _load("attention_examples.json")
+    kc, vc, ks, vs = _cache_from_codes(g["k_codes"], g["v_codes"], g["scale"], 1, 2)
+    q = np.array(case["q"], dtype=np.float64)[:, None, :]
+    L = case["seq_len"]
+    out = O.attention(q, kc, vc, ks, vs, np.array([[0]]), [L], [0, len(q)], 1, 16,
+                      math.log(3.0) / g["softmax_scale_ln3_over"], True, np.ones(2))
+    assert np.allclose(out[:, 0, :], np.array(case["expected"]), atol=1e-12, rtol=0)
+
+
+def _random_cache(rng, nb, bs, hkv, d):
+    kc = rng.integers(0, 256, (nb, bs, hkv, d // 2), dtype=np.uint8)
+    vc = rng.integers(0, 256, (nb, bs, hkv, d // 2), dtype=np.uint8)
+    ks = rng.uniform(0.05, 2.0, (nb, bs, hkv)).astype(np.float32)
+    vs = rng.uniform(0.05, 2.0, (nb, bs, hkv)).astype(np.float32)
+    return kc, vc, ks, vs
+
+
+def test_attention_brute_force_loops_gqa_paged_causal():
+    """Literal per-element loops over a tiny paged, GQA, mixed batch."""
+    rng = np.random.default_rng(0)
+    d, bs, hkv, hq, nb = 6, 4, 2, 4, 6
+    kc, vc, ks, vs = _random_cache(rng, nb, bs, hkv, d)
+    signs = np.array([1, -1, -1, 1, 1, -1], np.float64)
+    seqs = [(3, 7), (1, 5), (2, 2)]
+    table = np.array([[4, 1], [0, 5], [3, 2]])
+    qsl = [0, 3, 4, 6]
+    q = _bf16_values((6, hq, d), 9)
+    scale = 0.37
+    out = O.attention(q, kc, vc, ks, vs, table, [kv for _, kv in seqs], qsl, hkv, bs, scale, True, signs)
+    H = scipy.linalg.hadamard(2)  # b = 2, n = 3
+    for s, (ql, L) in enumerate(seqs):
+        ctx = L - ql
+        for j in range(ql):
+            tok = qsl[s] + j
+            for h in range(hq):
+                kvh = h // (hq // hkv)
+                keys, vals = [], []
+                for t in range(L):
+                    blk, off = table[s][t // bs], t % bs
+                    def deq(cache, sc):
+                        vec = []
+                        for i in range(d // 2):
+                            byte = int(cache[blk, off, kvh, i])
+                            for nib in (byte & 15, byte >> 4):
+                                vec.append((nib - 16 if nib >= 8 else nib) * float(sc[blk, off, kvh]))
+                        orig = []
+                        for i in range(d):
+                            blk0 = (i // 2) * 2
+                            acc = sum(H[i - blk0][jj] * vec[blk0 + jj] for jj in range(2))
+                            orig.append(signs[i] * acc / 2)
+                        return orig
+                    keys.append(deq(kc, ks))
+                    vals.append(deq(vc, vs))
+                sc = [scale * sum(q[tok, h, i] * keys[t][i] for i in range(d)) if t <= ctx + j else -math.inf
+                      for t in range(L)]
+                m = max(sc)
+                w = [math.exp(x - m) for x in sc]
+                z = sum(w)
+                for i in range(d):
+                    ref = sum(w[t] * vals[t][i] for t in range(L)) / z
+                    assert abs(out[tok, h, i] - ref) < 1e-12
+
+
+def test_attention_rotated_domain_matches_original_domain():
+    """The read path's formula (q'.(c s) * softmax_scale / b) gives the same
+    scores as softmax_scale * q . k_hat in the original domain."""
+    for d in [96, 128, 192]:
+        rng = np.random.default_rng(d)
+        codes = rng.integers(-8, 8, (50, d))
+        scales = rng.uniform(0.1, 1.0, 50)
+        s = _signs(d, d)
+        q = _bf16_values((3, d), d)
+        k_hat = O.dequantize_original(codes, scales, s)
+        ref = 0.1 * q @ k_hat.T
+        got = O.rotated_domain_scores(q, codes, scales, s, 0.1)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_single_key_returns_value():
+    rng = np.random.default_rng(3)
+    d = 128
+    kc, vc, ks, vs = _random_cache(rng, 1, 16, 1, d)
+    s = _signs(d, 1)
+    q = _bf16_values((1, 1, d), 2)
+    out = O.attention(q, kc, vc, ks, vs, np.array([[0]]), [1], [0, 1], 1, 16, 0.1, True, s)
+    codes = O.unpack_codes(vc[0, 0, 0])
+    v_hat = O.dequantize_original(codes[None], np.array([vs[0, 0, 0]]), s)[0]
+    assert np.allclose(out[0, 0], v_hat, atol=1e-12)
+
+
+def test_attention_noncausal_sees_all_keys():
+    rng = np.random.default_rng(4)
+    d = 64
+    kc, vc, ks, vs = _random_cache(rng, 2, 16, 1, d)
+    s = _signs(d, 4)
+    q = _bf16_values((2, 1, d), 5)
+    c = O.attention(q, kc, vc, ks, vs, np.array([[1, 0]]), [20], [0, 2], 1, 16, 0.2, True, s)
+    n = O.attention(q, kc, vc, ks, vs, np.array([[1, 0]]), [20], [0, 2], 1, 16, 0.2, False, s)
+    assert np.allclose(c[1], n[1], atol=1e-12)      # last query sees everything anyway
+    assert not np.allclose(c[0], n[0], atol=1e-6)   # first query is masked when causal
+
+
+def test_end_to_end_attention_close_to_unquantised():
+    """Quantise real-valued K/V through the oracle's write, attend, and compare
+    with plain attention on the unquantised values: INT4 is lossy, so only a
+    loose agreement is expected (the pages' e2e checks are accuracy runs)."""
+    from int4_token_head_gb300 import synthetic
+    w = synthetic.make_workload("tiny")
+    d, hkv, bs = w.head_size, w.num_kv_heads, w.block_size
+    kc, vc, ks, vs = [t.numpy() for t in w.empty_cache()]
+    khist, vhist = w.history_kv()
+    O.write_cache(khist.float().numpy(), vhist.float().numpy(), w.history_slot_mapping().numpy(),
+                  kc, vc, ks, vs, bs, w.signs.numpy())
+    kst, vst = w.step_kv()
+    O.write_cache(kst.float().numpy(), vst.float().numpy(), w.step_slot_mapping().numpy(),
+                  kc, vc, ks, vs, bs, w.signs.numpy())
+    q = w.queries().float().numpy()
+    scale = 1 / math.sqrt(d)
+    out = O.attention(q, kc, vc, ks, vs, w.block_table.numpy(), w.seq_lens.numpy(),
+                      w.query_start_loc.numpy(), hkv, bs, scale, True, w.signs.numpy())
+    assert np.isfinite(out).all()
+    # unquantised reference
+    q0 = 0
+    for s, (ql, L) in enumerate(w.seqs):
+        k, v = w.seq_kv(s)
+        k = k.double().numpy()
+        v = v.double().numpy()
+        for h in range(w.num_q_heads):
+            ref = O.attention_head(q[q0:q0 + ql, h], k[:, h // w.group], v[:, h // w.group],
+                                   L - ql, scale, True)
+            corr = np.corrcoef(out[q0:q0 + ql, h].ravel(), ref.ravel())[0, 1]
+            assert corr > 0.95
+        q0 += ql
