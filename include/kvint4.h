@@ -1,0 +1,185 @@
+/*
+ * kvint4.h -- C ABI of the GB300 (sm_103a) INT4 per-token-head KV cache with a
+ * randomized Hadamard rotation, and of paged attention over that cache.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, unless it
+ *   says otherwise.  The library allocates no device memory, keeps no
+ *   per-call state and never synchronises the device; each call only enqueues
+ *   kernels on `stream` (a cudaStream_t passed as void*; NULL is the legacy
+ *   default stream) and returns.  Calls are thread-safe.
+ * - "bf16" arguments are arrays of IEEE bfloat16 (2 bytes per element).
+ * - A head vector has `head_size` = d elements; b = d & -d is the largest
+ *   power-of-two divisor of d and n = d / b.  Supported head sizes: 64, 96,
+ *   128, 192, 256.  Supported block size: 16.
+ * - The cache layout (vLLM PR #40835, "[Feature] Triton INT4 per-token-head KV
+ *   cache quantization", review thread on reshape_and_cache_per_token_head_quant):
+ *     k_cache, v_cache:             uint8 [num_blocks][block_size][num_kv_heads][d/2]
+ *     k_scale_cache, v_scale_cache: float [num_blocks][block_size][num_kv_heads]
+ *   Slot s is (block s / block_size, offset s % block_size).  Element 2j of a
+ *   head vector is the low nibble of byte j, element 2j+1 the high nibble,
+ *   both signed 4-bit two's complement.
+ * - Return value: KV_INT4_OK (0) or a KV_INT4_ERR_* code from host-side
+ *   validation, done before anything is enqueued (on error nothing runs and
+ *   no memory is touched), or KV_INT4_ERR_CUDA if a launch failed.
+ * - `dev_status` (nullable) is a caller-owned device int32 that kernels OR
+ *   KV_INT4_DEV_* bits into when they meet bad device-side data (an index
+ *   out of range, inconsistent lengths).  The offending work is skipped; the
+ *   kernels never trap or assert.  The caller clears and reads it when it
+ *   chooses.
+ */
+#ifndef KVINT4_H
+#define KVINT4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVINT4_API __attribute__((visibility("default")))
+#else
+#define KVINT4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host-side status codes */
+#define KV_INT4_OK 0
+#define KV_INT4_ERR_NULL 1          /* a required pointer is NULL */
+#define KV_INT4_ERR_HEAD_SIZE 2     /* head_size not in {64, 96, 128, 192, 256} */
+#define KV_INT4_ERR_HEADS 3         /* num_q_heads % num_kv_heads != 0, or a head count <= 0 */
+#define KV_INT4_ERR_BLOCK_SIZE 4    /* block_size != 16 */
+#define KV_INT4_ERR_ALIGN 5         /* a pointer or stride breaks the 16-byte alignment rule */
+#define KV_INT4_ERR_WORKSPACE 6     /* workspace NULL or smaller than kv_int4_attention_workspace_size() */
+#define KV_INT4_ERR_SIZE 7          /* a negative count, or a size that overflows the index types */
+#define KV_INT4_ERR_CUDA 8          /* a CUDA call or kernel launch failed */
+
+/* device-side status bits (ORed into *dev_status) */
+#define KV_INT4_DEV_BAD_SLOT 1      /* slot_mapping entry >= num_blocks * block_size */
+#define KV_INT4_DEV_BAD_BLOCK 2     /* block_table entry outside [0, num_blocks) */
+#define KV_INT4_DEV_BAD_SEQ 4       /* q_len < 0, q_len > seq_len, seq_len > max_blocks_per_seq * block_size,
+                                       or query_start_loc outside [0, num_q_tokens] */
+#define KV_INT4_DEV_BAD_SIGNS 8     /* a sign entry other than +1 / -1 */
+
+/*
+ * kv_int4_write -- reshape_and_cache_int4: quantise new K/V head vectors into
+ * the paged INT4 cache.
+ *
+ * Defined by: "Rotate KV into RHT domain in the INT4 unified attn test" (vLLM
+ * PR #62881), Details / Root cause (K_s = H.D.k) and Details / Fix (rounding
+ * through bf16); "vLLM -- Attention Kernels & KV Cache Quantization" (PR
+ * #56198), the block-diagonal H_b for non-power-of-two d.
+ *
+ * For each token t < num_tokens and kv head h, with x = k[t][h][:] (and then
+ * v[t][h][:]):
+ *   y  = bf16_round( (I_n (x) H_b) . D . x )   H_b Sylvester Walsh-Hadamard,
+ *                                              D = diag(signs), fp32 arithmetic
+ *   s  = fp32(max_i |y_i| / 7)                 (0 when max|y| < 2^-120)
+ *   c_i = round_half_even(y_i * fp32(1/s))     in [-7, 7] (0 when s == 0)
+ * then codes go to k_cache[slot], the scale to k_scale_cache[slot] with
+ * slot = slot_mapping[t].  slot < 0 marks a padding token (skipped); slot >=
+ * num_blocks*block_size is skipped and sets KV_INT4_DEV_BAD_SLOT.
+ *
+ * k, v: bf16, element (t, h, i) at k[t*k_token_stride + h*head_size + i];
+ *   heads and elements contiguous.  Strides are in elements and must be
+ *   multiples of 8; k, v must be 16-byte aligned.
+ * slot_mapping: int64 [num_tokens].  signs: int8 [head_size], each +1 or -1
+ *   (the random diagonal D, shared by K, V, Q and all heads).
+ * Caches: as above, 16-byte aligned.  num_tokens == 0 is a no-op.
+ */
+KVINT4_API int kv_int4_write(const void* k, int64_t k_token_stride,
+                  const void* v, int64_t v_token_stride,
+                  const int64_t* slot_mapping, int num_tokens,
+                  uint8_t* k_cache, uint8_t* v_cache,
+                  float* k_scale_cache, float* v_scale_cache,
+                  int num_blocks, int block_size, int num_kv_heads, int head_size,
+                  const int8_t* signs, int32_t* dev_status, void* stream);
+
+/*
+ * kv_int4_write_prerotated -- the write path from step "s = ..." on: k and v
+ * already hold the bf16 rotated values y (the rotation and the bf16 rounding
+ * are skipped).  Same layout, slots and errors as kv_int4_write; no signs.
+ * It exists so that codes can be compared bit for bit against an independent
+ * implementation fed the same rotated values.
+ */
+KVINT4_API int kv_int4_write_prerotated(const void* k, int64_t k_token_stride,
+                             const void* v, int64_t v_token_stride,
+                             const int64_t* slot_mapping, int num_tokens,
+                             uint8_t* k_cache, uint8_t* v_cache,
+                             float* k_scale_cache, float* v_scale_cache,
+                             int num_blocks, int block_size, int num_kv_heads, int head_size,
+                             int32_t* dev_status, void* stream);
+
+/*
+ * kv_int4_attention_workspace_size -- bytes of device workspace that
+ * kv_int4_attention needs for these sizes (a pure host computation).  The
+ * workspace holds the device-built schedule, the rotated queries and the
+ * split-KV partial results; its contents need no initialisation.
+ * Returns 0 for invalid arguments.
+ */
+KVINT4_API size_t kv_int4_attention_workspace_size(int num_seqs, int num_q_tokens,
+                                        int num_q_heads, int num_kv_heads, int head_size);
+
+/*
+ * kv_int4_attention -- unified_attention_int4: varlen prefill + decode
+ * attention with GQA over the paged INT4 cache.
+ *
+ * Defined by: "Rotate KV into RHT domain in the INT4 unified attn test" (vLLM
+ * PR #62881), Details / Root cause: q' = H.D.q, scores scaled by
+ * softmax_scale/b so that q'.K_s/b = q.k, and D.H(.)/b applied to the output
+ * to undo V's rotation; with b in place of d for block-diagonal H_b ("vLLM --
+ * Attention Kernels & KV Cache Quantization", PR #56198).  Mixed batches of
+ * prefills and decodes in any order ([Feature] Triton INT4 per-token-head KV
+ * cache quantization, PR #40835 review thread: everything goes through
+ * unified attention).
+ *
+ * Sequence i has query tokens [query_start_loc[i], query_start_loc[i+1]) and
+ * kv length seq_lens[i] (including those tokens, whose K/V must already be in
+ * the cache).  Its queries are its last q_len positions: query j sits at
+ * position seq_lens[i] - q_len + j and, when `causal` != 0, sees keys
+ * 0 .. that position; otherwise all seq_lens[i] keys.  Key position p of
+ * sequence i is in block block_table[i*max_blocks_per_seq + p/block_size],
+ * offset p % block_size.  q head hq uses kv head hq / (num_q_heads/num_kv_heads).
+ *
+ * out[t][hq][:] = sum_p softmax_p(softmax_scale * q[t][hq] . k_hat_p) v_hat_p
+ * with k_hat_p = D.(I_n (x) H_b).(c_p * s_p)/b the dequantised, inverse-rotated
+ * key (likewise v_hat), computed in the rotated domain.
+ *
+ * q: bf16, element (t, hq, i) at q[t*q_token_stride + hq*head_size + i]
+ *   (stride a multiple of 8 elements, 16-byte aligned).
+ * out: bf16, same layout with out_token_stride.
+ * block_table: int32 [num_seqs][max_blocks_per_seq].  seq_lens: int32
+ *   [num_seqs].  query_start_loc: int32 [num_seqs+1], non-decreasing from 0
+ *   to num_q_tokens.  max_query_len / max_seq_len: upper bounds of the
+ *   per-sequence values (used only to size launches).
+ * signs: int8 [head_size], the same D that the cache was written with.
+ * workspace: >= kv_int4_attention_workspace_size(...) bytes, 256-byte aligned.
+ * Sequences whose metadata is invalid are skipped (their output rows are not
+ * written) and set KV_INT4_DEV_BAD_SEQ; blocks outside [0, num_blocks) are
+ * treated as masked and set KV_INT4_DEV_BAD_BLOCK.
+ */
+KVINT4_API int kv_int4_attention(const void* q, int64_t q_token_stride,
+                      const uint8_t* k_cache, const uint8_t* v_cache,
+                      const float* k_scale_cache, const float* v_scale_cache,
+                      const int32_t* block_table, int max_blocks_per_seq,
+                      const int32_t* seq_lens, const int32_t* query_start_loc,
+                      int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len,
+                      int num_q_heads, int num_kv_heads, int head_size,
+                      int block_size, int num_blocks, float softmax_scale, int causal,
+                      const int8_t* signs, void* out, int64_t out_token_stride,
+                      void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream);
+
+/* kv_int4_status_string -- a static, human-readable name for a KV_INT4_* code. */
+KVINT4_API const char* kv_int4_status_string(int status);
+
+/* kv_int4_version -- the library's ABI version (currently 1). */
+KVINT4_API int kv_int4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVINT4_H */

@@ -1,0 +1,167 @@
+"""ctypes binding of libkvint4.so: argument marshalling only.
+
+Every function takes torch tensors, checks dtypes/shapes/layouts, and passes
+raw device pointers and sizes to the C ABI declared in include/kvint4.h.  All
+computation happens in the library's CUDA kernels; if the library cannot be
+built or loaded, these functions raise instead of computing anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+c_int, c_int64, c_void_p, c_size_t, c_float = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+
+_SIGNATURES = {
+    "kv_int4_write": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p, c_void_p,
+                              c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "kv_int4_write_prerotated": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
+                                         c_void_p]),
+    "kv_int4_attention_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "kv_int4_attention": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                  c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                  c_int, c_float, c_int, c_void_p, c_void_p, c_int64, c_void_p, c_size_t,
+                                  c_void_p, c_void_p]),
+    "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
+    "kv_int4_version": (c_int, []),
+}
+
+OK = 0
+DEV_BAD_SLOT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SIGNS = 1, 2, 4, 8
+
+
+class KvInt4Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+def load(path: Optional[str] = None):
+    """Load (building first if needed) libkvint4.so and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.build()
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def status_string(code: int) -> str:
+    return load().kv_int4_status_string(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _token_major(x: torch.Tensor, name: str, heads: int, d: int):
+    _check(x.dim() == 3 and x.shape[1] == heads and x.shape[2] == d,
+           f"{name} must be [tokens, {heads}, {d}], got {tuple(x.shape)}")
+    _check(x.dtype == torch.bfloat16, f"{name} must be bfloat16")
+    _check(x.stride(2) == 1 and (x.shape[1] <= 1 or x.stride(1) == d),
+           f"{name} must have contiguous heads and head dims")
+    return x.stride(0) if x.shape[0] > 0 else heads * d
+
+
+def _cache_dims(k_cache, v_cache, k_scale, v_scale):
+    _check(k_cache.dtype == torch.uint8 and v_cache.dtype == torch.uint8, "caches must be uint8")
+    _check(k_cache.dim() == 4 and k_cache.shape == v_cache.shape, "caches must be [blocks, block_size, heads, d/2]")
+    _check(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
+    nb, bs, hkv, half = k_cache.shape
+    for s in (k_scale, v_scale):
+        _check(s.dtype == torch.float32 and tuple(s.shape) == (nb, bs, hkv) and s.is_contiguous(),
+               "scale caches must be contiguous float32 [blocks, block_size, heads]")
+    return nb, bs, hkv, 2 * half
+
+
+def _raise(code, where):
+    if code != OK:
+        raise KvInt4Error(code, where)
+
+
+def write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, signs,
+          dev_status: Optional[torch.Tensor] = None, stream=None, prerotated: bool = False):
+    """reshape_and_cache_int4 through kv_int4_write (or kv_int4_write_prerotated)."""
+    nb, bs, hkv, d = _cache_dims(k_cache, v_cache, k_scale, v_scale)
+    ks = _token_major(k, "k", hkv, d)
+    vs = _token_major(v, "v", hkv, d)
+    _check(k.shape[0] == v.shape[0] == slot_mapping.shape[0], "k, v and slot_mapping disagree on tokens")
+    _check(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), "slot_mapping must be contiguous int64")
+    lib = load()
+    if prerotated:
+        code = lib.kv_int4_write_prerotated(_ptr(k), ks, _ptr(v), vs, _ptr(slot_mapping), int(k.shape[0]),
+                                            _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                            nb, bs, hkv, d, _ptr(dev_status), _stream(stream))
+        _raise(code, "kv_int4_write_prerotated")
+    else:
+        _check(signs.dtype == torch.int8 and signs.numel() == d and signs.is_contiguous(), "signs must be int8 [d]")
+        code = lib.kv_int4_write(_ptr(k), ks, _ptr(v), vs, _ptr(slot_mapping), int(k.shape[0]),
+                                 _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                 nb, bs, hkv, d, _ptr(signs), _ptr(dev_status), _stream(stream))
+        _raise(code, "kv_int4_write")
+
+
+def attention_workspace_size(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_size) -> int:
+    return int(load().kv_int4_attention_workspace_size(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_size))
+
+
+def attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, query_start_loc,
+              max_query_len, max_seq_len, softmax_scale, causal, signs, out, workspace,
+              dev_status: Optional[torch.Tensor] = None, stream=None):
+    """unified_attention_int4 through kv_int4_attention; writes ``out`` in place."""
+    nb, bs, hkv, d = _cache_dims(k_cache, v_cache, k_scale, v_scale)
+    _check(q.dim() == 3 and q.shape[2] == d, "q must be [tokens, q_heads, d]")
+    hq = q.shape[1]
+    qs = _token_major(q, "q", hq, d)
+    os_ = _token_major(out, "out", hq, d)
+    _check(out.shape[0] == q.shape[0], "out must match q")
+    _check(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous(),
+           "block_table must be contiguous int32 [seqs, max_blocks]")
+    _check(seq_lens.dtype == torch.int32 and query_start_loc.dtype == torch.int32, "seq_lens/query_start_loc int32")
+    num_seqs = seq_lens.shape[0]
+    _check(query_start_loc.shape[0] == num_seqs + 1 and block_table.shape[0] == num_seqs, "metadata shapes")
+    _check(signs.dtype == torch.int8 and signs.numel() == d, "signs must be int8 [d]")
+    _check(workspace.dtype == torch.uint8 and workspace.is_contiguous(), "workspace must be contiguous uint8")
+    lib = load()
+    code = lib.kv_int4_attention(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                 _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+                                 _ptr(query_start_loc), int(num_seqs), int(q.shape[0]), int(max_query_len),
+                                 int(max_seq_len), int(hq), int(hkv), int(d), int(bs), int(nb),
+                                 float(softmax_scale), int(bool(causal)), _ptr(signs), _ptr(out), os_,
+                                 _ptr(workspace), int(workspace.numel()), _ptr(dev_status), _stream(stream))
+    _raise(code, "kv_int4_attention")

@@ -1,0 +1,175 @@
+// C ABI entry points: host-side validation, then one or a few kernel launches
+// on the caller's stream.  Nothing here allocates device memory or
+// synchronises the device.
+
+#include <cuda_runtime.h>
+
+#include "../../include/kvint4.h"
+#include "internal.h"
+
+namespace kvint4 {
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+int sm_count(int dev) {
+  static int cache[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool workspace_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
+                      int head_size, WorkspaceLayout* L) {
+  if (num_seqs < 0 || num_q_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0) return false;
+  if (num_q_heads % num_kv_heads) return false;
+  const int64_t group = num_q_heads / num_kv_heads;
+  int64_t tile_tokens = kPrefillRows / group;
+  if (tile_tokens < 1) tile_tokens = 1;
+  const int64_t S = num_seqs, T = num_q_tokens, Hq = num_q_heads, Hkv = num_kv_heads, D = head_size;
+  size_t off = 0;
+  L->plan = off;
+  off = align256(off + 64 * sizeof(int32_t));
+  L->dseq = off;
+  off = align256(off + (size_t)S * sizeof(int32_t));
+  L->dprefix = off;
+  off = align256(off + (size_t)(S + 1) * sizeof(int64_t));
+  L->max_prefill_items = (T / tile_tokens + S) * Hkv;
+  L->pitems = off;
+  off = align256(off + (size_t)L->max_prefill_items * 4 * sizeof(int32_t));
+  L->qrot = off;
+  off = align256(off + (size_t)T * Hq * D * 2);
+  L->direct_o = off;
+  off = align256(off + (size_t)S * Hkv * kDecodeCols * D * sizeof(float));
+  L->direct_ml = off;
+  off = align256(off + (size_t)S * Hkv * kDecodeCols * 2 * sizeof(float));
+  L->warp_o = off;
+  off = align256(off + (size_t)kMaxDecodeWarps * kDecodeCols * D * sizeof(float));
+  L->warp_ml = off;
+  off = align256(off + (size_t)kMaxDecodeWarps * kDecodeCols * 2 * sizeof(float));
+  L->total = off;
+  return true;
+}
+
+static bool head_size_ok(int d) { return d == 64 || d == 96 || d == 128 || d == 192 || d == 256; }
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace kvint4
+
+using namespace kvint4;
+
+extern "C" {
+
+int kv_int4_version(void) { return 1; }
+
+const char* kv_int4_status_string(int status) {
+  switch (status) {
+    case KV_INT4_OK: return "ok";
+    case KV_INT4_ERR_NULL: return "a required pointer is NULL";
+    case KV_INT4_ERR_HEAD_SIZE: return "unsupported head_size (expected 64, 96, 128, 192 or 256)";
+    case KV_INT4_ERR_HEADS: return "invalid head counts (num_q_heads must be a positive multiple of num_kv_heads)";
+    case KV_INT4_ERR_BLOCK_SIZE: return "unsupported block_size (expected 16)";
+    case KV_INT4_ERR_ALIGN: return "a pointer is not 16-byte aligned or a token stride is not a multiple of 8 elements";
+    case KV_INT4_ERR_WORKSPACE: return "workspace is NULL or smaller than kv_int4_attention_workspace_size()";
+    case KV_INT4_ERR_SIZE: return "a count is negative or a size overflows the index types";
+    case KV_INT4_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    default: return "unknown status";
+  }
+}
+
+static int validate_write(const void* k, int64_t ks, const void* v, int64_t vs, const int64_t* slots,
+                          int num_tokens, const uint8_t* kc, const uint8_t* vc, const float* ksc,
+                          const float* vsc, int num_blocks, int block_size, int hkv, int d,
+                          const int8_t* signs, bool need_signs) {
+  if (num_tokens < 0 || num_blocks < 0 || hkv <= 0) return num_tokens < 0 || num_blocks < 0 ? KV_INT4_ERR_SIZE : KV_INT4_ERR_HEADS;
+  if (!head_size_ok(d)) return KV_INT4_ERR_HEAD_SIZE;
+  if (block_size != 16) return KV_INT4_ERR_BLOCK_SIZE;
+  if (num_tokens == 0) return KV_INT4_OK;  // a no-op; empty tensors may carry NULL pointers
+  if (!k || !v || !slots || !kc || !vc || !ksc || !vsc || (need_signs && !signs)) return KV_INT4_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc) || (ks % 8) || (vs % 8) || ks < 0 || vs < 0)
+    return KV_INT4_ERR_ALIGN;
+  if ((int64_t)num_tokens * 2 * hkv >= (1ll << 31)) return KV_INT4_ERR_SIZE;
+  if ((int64_t)num_blocks * block_size * hkv * (d / 2) >= (1ll << 62)) return KV_INT4_ERR_SIZE;
+  return KV_INT4_OK;
+}
+
+static int do_write(const void* k, int64_t ks, const void* v, int64_t vs, const int64_t* slots, int num_tokens,
+                    uint8_t* kc, uint8_t* vc, float* ksc, float* vsc, int num_blocks, int block_size, int hkv,
+                    int d, const int8_t* signs, int32_t* status, void* stream, bool prerot) {
+  int e = validate_write(k, ks, v, vs, slots, num_tokens, kc, vc, ksc, vsc, num_blocks, block_size, hkv, d, signs,
+                         !prerot);
+  if (e != KV_INT4_OK) return e;
+  if (num_tokens == 0) return KV_INT4_OK;
+  if (current_device() < 0) return KV_INT4_ERR_CUDA;
+  WriteArgs a{k, ks, v, vs, slots, num_tokens, kc, vc, ksc, vsc, num_blocks, block_size, hkv, d, signs, status};
+  return launch_write(a, prerot, static_cast<cudaStream_t>(stream));
+}
+
+int kv_int4_write(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                  const int64_t* slot_mapping, int num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                  float* k_scale_cache, float* v_scale_cache, int num_blocks, int block_size, int num_kv_heads,
+                  int head_size, const int8_t* signs, int32_t* dev_status, void* stream) {
+  return do_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, k_cache, v_cache, k_scale_cache,
+                  v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, signs, dev_status, stream, false);
+}
+
+int kv_int4_write_prerotated(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                             const int64_t* slot_mapping, int num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                             float* k_scale_cache, float* v_scale_cache, int num_blocks, int block_size,
+                             int num_kv_heads, int head_size, int32_t* dev_status, void* stream) {
+  return do_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, k_cache, v_cache, k_scale_cache,
+                  v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, nullptr, dev_status, stream, true);
+}
+
+size_t kv_int4_attention_workspace_size(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
+                                        int head_size) {
+  if (!head_size_ok(head_size)) return 0;
+  WorkspaceLayout L;
+  if (!workspace_layout(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_size, &L)) return 0;
+  return L.total;
+}
+
+int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_cache, const uint8_t* v_cache,
+                      const float* k_scale_cache, const float* v_scale_cache, const int32_t* block_table,
+                      int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc,
+                      int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
+                      int num_kv_heads, int head_size, int block_size, int num_blocks, float softmax_scale,
+                      int causal, const int8_t* signs, void* out, int64_t out_token_stride, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (num_seqs < 0 || num_q_tokens < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0 ||
+      max_blocks_per_seq < 0)
+    return KV_INT4_ERR_SIZE;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return KV_INT4_ERR_HEADS;
+  if (!head_size_ok(head_size)) return KV_INT4_ERR_HEAD_SIZE;
+  if (block_size != 16) return KV_INT4_ERR_BLOCK_SIZE;
+  if (num_seqs == 0 || num_q_tokens == 0) return KV_INT4_OK;
+  if (!q || !k_cache || !v_cache || !k_scale_cache || !v_scale_cache || !block_table || !seq_lens ||
+      !query_start_loc || !signs || !out || !workspace)
+    return !workspace ? KV_INT4_ERR_WORKSPACE : KV_INT4_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || (q_token_stride % 8) ||
+      (out_token_stride % 8) || q_token_stride < 0 || out_token_stride < 0 || ((uintptr_t)workspace & 255u))
+    return KV_INT4_ERR_ALIGN;
+  if ((int64_t)max_blocks_per_seq * block_size >= (1ll << 31) || (int64_t)num_q_tokens * num_q_heads >= (1ll << 31))
+    return KV_INT4_ERR_SIZE;
+  WorkspaceLayout L;
+  if (!workspace_layout(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_size, &L)) return KV_INT4_ERR_SIZE;
+  if (workspace_bytes < L.total) return KV_INT4_ERR_WORKSPACE;
+  if (current_device() < 0) return KV_INT4_ERR_CUDA;
+  AttnArgs a{q, q_token_stride, k_cache, v_cache, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
+             seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len, max_seq_len, num_q_heads,
+             num_kv_heads, head_size, block_size, num_blocks, softmax_scale, causal, signs, out, out_token_stride,
+             workspace, workspace_bytes, dev_status};
+  return launch_attention(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,1025 @@
+// unified_attention_int4 for sm_103a: varlen prefill + decode with GQA over
+// the paged INT4 per-token-head cache, computed in the rotated domain.
+//
+// Method ("Rotate KV into RHT domain in the INT4 unified attn test", vLLM PR
+// #62881, Details / Root cause; b in place of d per "vLLM -- Attention
+// Kernels & KV Cache Quantization", PR #56198):
+//   q' = (I_n (x) H_b) D q,  score_t = softmax_scale/b * q' . (c_t s_t),
+//   o' = sum_t softmax_t * (c_t^v s_t^v),  out = D (I_n (x) H_b) o' / b.
+//
+// Launch sequence (all on the caller's stream):
+//  1. prep: CTA 0 builds the schedule from seq_lens / query_start_loc (decode
+//     sequence list with block prefix sums, prefill tile list); the other
+//     CTAs rotate every query once and pre-scale it by
+//     softmax_scale * log2(e) / b, stored as f16 (scores are then base-2).
+//  2. prefill (only if some sequence has q_len * G > 8 or G > 8): one CTA per
+//     64-row tile of (query token x q head of one kv group), FA2-style
+//     mma.sync with K/V dequantised once per block into f16 shared tiles.
+//  3. decode: stream-K over the flattened (decode sequence, kv head, block)
+//     space; every warp takes an equal contiguous range, so the split-KV
+//     load balance is exact.  Per block the warp computes S^T = K Q'^T with
+//     the 16 keys as the MMA M dimension (q_len*G <= 8 query columns as N),
+//     converting INT4 nibbles straight into f16 A fragments in registers
+//     (the in-register order of head dimensions is a permutation applied
+//     consistently to q', which leaves q'.K unchanged); P is transposed with
+//     movmatrix into the B operand of O'^T += V^T P^T.  Each segment piece
+//     writes (o', m, l) to the workspace.
+//  4. reduce: merges the pieces of every decode segment with the log-sum-exp
+//     rule, normalises, applies the inverse rotation and writes bf16.
+//
+// Device-side checks never trap: bad blocks are masked, bad sequences
+// skipped, and a KV_INT4_DEV_* bit is ORed into the caller's status word.
+
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvint4 {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct PlanView {
+  int32_t* plan;      // [0] n_dseq, [1] n_prefill_items, [2] prefill work counter
+  int32_t* dseq;
+  int64_t* dprefix;
+  int4* pitems;       // (seq, kv_head, tile, key blocks)
+  __half* qrot;
+  float* direct_o;
+  float* direct_ml;
+  float* warp_o;
+  float* warp_ml;
+};
+
+static PlanView plan_view(void* ws, const WorkspaceLayout& L) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  PlanView v;
+  v.plan = reinterpret_cast<int32_t*>(b + L.plan);
+  v.dseq = reinterpret_cast<int32_t*>(b + L.dseq);
+  v.dprefix = reinterpret_cast<int64_t*>(b + L.dprefix);
+  v.pitems = reinterpret_cast<int4*>(b + L.pitems);
+  v.qrot = reinterpret_cast<__half*>(b + L.qrot);
+  v.direct_o = reinterpret_cast<float*>(b + L.direct_o);
+  v.direct_ml = reinterpret_cast<float*>(b + L.direct_ml);
+  v.warp_o = reinterpret_cast<float*>(b + L.warp_o);
+  v.warp_ml = reinterpret_cast<float*>(b + L.warp_ml);
+  return v;
+}
+
+struct Common {
+  const uint16_t* q;
+  int64_t q_stride;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int num_seqs;
+  int num_q_tokens;
+  int hq;
+  int hkv;
+  int group;
+  int num_blocks;
+  int causal;
+  float qscale;  // softmax_scale * log2(e) / b
+  const int8_t* signs;
+  uint16_t* out;
+  int64_t out_stride;
+  int32_t* status;
+  int tile_tokens;  // prefill: query tokens per 64-row tile
+  long long max_items;  // capacity of the prefill item list
+};
+
+__device__ __forceinline__ bool is_decode_kind(int qlen, int group) {
+  return group <= kDecodeCols && qlen * group <= kDecodeCols;
+}
+
+// ---------------------------------------------------------------------------
+// 1. prep: schedule (CTA 0) + query rotation (CTAs 1..)
+// ---------------------------------------------------------------------------
+constexpr int kPrepThreads = 256;
+constexpr int kPrepRowsPerCta = 8;
+
+template <typename T>
+__device__ T block_exclusive_scan(T v, T* total, T* sbuf /*[kPrepThreads/32]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sbuf[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < kPrepThreads / 32 ? sbuf[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kPrepThreads / 32) sbuf[lane] = w;
+  }
+  __syncthreads();
+  T before = warp > 0 ? sbuf[warp - 1] : T(0);
+  *total = sbuf[kPrepThreads / 32 - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView pv) {
+  if (blockIdx.x == 0) {
+    __shared__ int32_t s_i32[kPrepThreads / 32];
+    __shared__ long long s_i64[kPrepThreads / 32];
+    int n_dseq = 0, n_items = 0;
+    long long dpre = 0;
+    for (int base = 0; base < c.num_seqs; base += kPrepThreads) {
+      const int s = base + threadIdx.x;
+      int kind = 0, nblk = 0, ntiles = 0, ql = 0, L = 0;
+      if (s < c.num_seqs) {
+        const int q0 = c.qsl[s], q1 = c.qsl[s + 1];
+        L = c.seq_lens[s];
+        ql = q1 - q0;
+        const bool bad = q0 < 0 || q1 > c.num_q_tokens || ql < 0 || L < ql ||
+                         (long long)L > (long long)c.max_blocks * 16;
+        if (bad) {
+          flag(c.status, KV_INT4_DEV_BAD_SEQ);
+        } else if (ql > 0) {
+          kind = is_decode_kind(ql, c.group) ? 1 : 2;
+          nblk = (L + 15) / 16;
+          if (kind == 2) ntiles = (ql + c.tile_tokens - 1) / c.tile_tokens;
+        }
+      }
+      int tot_a;
+      long long tot_b;
+      int tot_c;
+      const int ex_a = block_exclusive_scan<int>(kind == 1, &tot_a, s_i32);
+      const long long ex_b = block_exclusive_scan<long long>(kind == 1 ? nblk : 0, &tot_b, s_i64);
+      const int ex_c = block_exclusive_scan<int>(ntiles, &tot_c, s_i32);
+      if (kind == 1) {
+        pv.dseq[n_dseq + ex_a] = s;
+        pv.dprefix[n_dseq + ex_a] = dpre + ex_b;
+      } else if (kind == 2) {
+        const int ctx = L - ql;
+        for (int t = 0; t < ntiles; t++) {
+          int keys = L;
+          if (c.causal) {
+            const int last = min(ql, (t + 1) * c.tile_tokens) - 1;  // last query of the tile
+            keys = ctx + last + 1;
+          }
+          const int nkb = (keys + 15) / 16;
+          // tiles in descending order of work within a sequence
+          const long long slot = (long long)n_items + (long long)(ex_c + (ntiles - 1 - t)) * c.hkv;
+          if (slot + c.hkv > c.max_items) {  // only reachable with inconsistent query_start_loc
+            flag(c.status, KV_INT4_DEV_BAD_SEQ);
+            continue;
+          }
+          for (int h = 0; h < c.hkv; h++) pv.pitems[slot + h] = make_int4(s, h, t, nkb);
+        }
+      }
+      n_dseq += tot_a;
+      dpre += tot_b;
+      n_items += tot_c * c.hkv;
+    }
+    if (threadIdx.x == 0) {
+      pv.dprefix[n_dseq] = dpre;
+      pv.plan[0] = n_dseq;
+      // an overflowing list (inconsistent metadata, already flagged) is dropped whole
+      pv.plan[1] = (long long)n_items > c.max_items ? 0 : n_items;
+      pv.plan[2] = 0;
+    }
+    return;
+  }
+
+  // query rotation: one warp per (token, q head) row
+  __shared__ float srow[kPrepRowsPerCta][D];
+  constexpr int B = Head<D>::b;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)(blockIdx.x - 1) * kPrepRowsPerCta + warp;
+  if (row >= (long long)c.num_q_tokens * c.hq) return;
+  const long long t = row / c.hq;
+  const int h = (int)(row - t * c.hq);
+  const uint16_t* src = c.q + t * c.q_stride + (long long)h * D;
+  float* r = srow[warp];
+  for (int i = lane; i < D; i += 32) {
+    const float x = __uint_as_float((uint32_t)src[i] << 16);
+    r[i] = c.signs[i] < 0 ? -x : x;
+  }
+  __syncwarp();
+#pragma unroll 1
+  for (int hh = 1; hh < B; hh <<= 1) {
+    for (int p = lane; p < D / 2; p += 32) {
+      const int i = (p / hh) * 2 * hh + (p % hh);
+      const float a = r[i], b = r[i + hh];
+      r[i] = a + b;
+      r[i + hh] = a - b;
+    }
+    __syncwarp();
+  }
+  __half* dst = pv.qrot + row * D;
+  for (int i = lane; i < D; i += 32) dst[i] = __float2half_rn(r[i] * c.qscale);
+}
+
+// ---------------------------------------------------------------------------
+// 3. decode: stream-K, one warp per equal range of (segment, block) positions
+// ---------------------------------------------------------------------------
+template <int D>
+struct DecGeom {
+  static constexpr int WARPS = 8;
+  static constexpr int STAGES = 4;
+  static constexpr int TILE = 16 * D / 2;              // bytes of one 16-key code tile
+  static constexpr int STAGE = 2 * TILE + 2 * 16 * 4;  // K codes, V codes, K scales, V scales
+  static constexpr int WARP_SMEM = STAGES * STAGE + 16;
+  static constexpr int SMEM = WARPS * WARP_SMEM;
+  static constexpr int KW = D / 32;   // K words per row per thread (quarter row)
+  static constexpr int VB = D / 16;   // V bytes per row per thread (eighth row)
+  static constexpr int KSTEPS = D / 16;
+};
+
+struct DecWalk {
+  int i;      // index into the decode-sequence list
+  int h;      // kv head
+  int kb;     // block within the sequence
+  int nblk;   // blocks of the sequence
+  int seq;    // sequence id
+};
+
+__device__ __forceinline__ void walk_load(DecWalk& w, const Common& c, const PlanView& pv) {
+  w.seq = pv.dseq[w.i];
+  w.nblk = (c.seq_lens[w.seq] + 15) / 16;
+}
+__device__ __forceinline__ void walk_next(DecWalk& w, const Common& c, const PlanView& pv, bool reload) {
+  if (++w.kb == w.nblk) {
+    w.kb = 0;
+    if (++w.h == c.hkv) {
+      w.h = 0;
+      ++w.i;
+      if (reload) walk_load(w, c, pv);
+    }
+  }
+}
+
+template <int N, int BYTES>
+__device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint8_t* p) {
+  static_assert(N * 4 == BYTES, "word count");
+  if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+    for (int k = 0; k < N / 4; k++) {
+      uint4 v = reinterpret_cast<const uint4*>(p)[k];
+      w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+    }
+  } else if constexpr (BYTES % 8 == 0) {
+#pragma unroll
+    for (int k = 0; k < N / 2; k++) {
+      uint2 v = reinterpret_cast<const uint2*>(p)[k];
+      w[2 * k] = v.x; w[2 * k + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; k++) w[k] = reinterpret_cast<const uint32_t*>(p)[k];
+  }
+}
+
+// f16x2 (key a, key b) pairs for the thread's D/8 head dimensions
+template <int D>
+__device__ __forceinline__ void v_pairs(uint32_t (&P)[D / 8], const uint8_t* ra, const uint8_t* rb) {
+  constexpr int VB = D / 16;
+  if constexpr (VB % 4 == 0) {
+    uint32_t wa[VB / 4], wb[VB / 4];
+    lds_words<VB / 4, VB>(wa, ra);
+    lds_words<VB / 4, VB>(wb, rb);
+#pragma unroll
+    for (int k = 0; k < VB / 4; k++) {
+      const uint32_t xx = __byte_perm(wa[k], wb[k], 0x5410);
+      const uint32_t yy = __byte_perm(wa[k], wb[k], 0x7632);
+#pragma unroll
+      for (int t = 0; t < 4; t++) {
+        P[8 * k + t] = nib_to_f16x2(xx >> (4 * t));
+        P[8 * k + 4 + t] = nib_to_f16x2(yy >> (4 * t));
+      }
+    }
+  } else {
+    static_assert(VB % 2 == 0, "V bytes per thread must be even");
+#pragma unroll
+    for (int k = 0; k < VB / 2; k++) {
+      const uint32_t ha = reinterpret_cast<const uint16_t*>(ra)[k];
+      const uint32_t hb = reinterpret_cast<const uint16_t*>(rb)[k];
+      const uint32_t xx = __byte_perm(ha, hb, 0x5410);
+#pragma unroll
+      for (int t = 0; t < 4; t++) P[4 * k + t] = nib_to_f16x2(xx >> (4 * t));
+    }
+  }
+}
+
+struct DecParams {
+  Common c;
+  PlanView pv;
+  int total_warps;
+};
+
+template <int D>
+__global__ void __launch_bounds__(DecGeom<D>::WARPS * 32) decode_kernel(DecParams prm) {
+  using G = DecGeom<D>;
+  const Common& c = prm.c;
+  const PlanView& pv = prm.pv;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, cq = lane & 3;
+  uint8_t* wsm = smem + warp * G::WARP_SMEM;
+  int* sflag = reinterpret_cast<int*>(wsm + G::STAGES * G::STAGE);
+
+  const int n_dseq = pv.plan[0];
+  if (n_dseq == 0) return;
+  const long long per_head = pv.dprefix[n_dseq];
+  const long long Tb = per_head * c.hkv;
+  const int W = prm.total_warps;
+  const int wid = blockIdx.x * G::WARPS + warp;
+  const long long P0 = Tb * wid / W, P1 = Tb * (wid + 1) / W;
+  if (P0 >= P1) return;
+
+  // locate P0: largest i with dprefix[i] * hkv <= P0 (32-ary search)
+  int lo = 0, hi = n_dseq;  // invariant: key(lo) <= P0 < key(hi)
+  while (hi - lo > 1) {
+    const long long span = hi - lo;
+    const int probe = lo + (int)((span * lane) / 32);
+    const bool le = lane == 0 || pv.dprefix[probe] * c.hkv <= P0;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int last = 31 - __clz(m);
+    const int nlo = lo + (int)((span * last) / 32);
+    const int nhi = last == 31 ? hi : lo + (int)((span * (last + 1)) / 32);
+    lo = nlo;
+    hi = nhi > nlo ? nhi : nlo + 1;
+  }
+  DecWalk cw;
+  cw.i = lo;
+  walk_load(cw, c, pv);
+  {
+    const long long off = P0 - pv.dprefix[cw.i] * c.hkv;
+    cw.h = (int)(off / cw.nblk);
+    cw.kb = (int)(off - (long long)cw.h * cw.nblk);
+  }
+  DecWalk pw = cw;
+
+  auto issue = [&](const DecWalk& w, int stage) {
+    uint8_t* st = wsm + stage * G::STAGE;
+    const int blk = c.block_table[(long long)w.seq * c.max_blocks + w.kb];
+    const bool ok = blk >= 0 && blk < c.num_blocks;
+    if (!ok) {
+      if (lane == 0) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
+    } else {
+      const long long row0 = (long long)blk * 16;
+      for (int q = lane; q < D / 2; q += 32) {
+        const int r = q / (D / 32), col = q - r * (D / 32);
+        const long long goff = ((row0 + r) * c.hkv + w.h) * (D / 2) + col * 16;
+        cp_async16(st + r * (D / 2) + col * 16, c.k_cache + goff);
+        cp_async16(st + G::TILE + r * (D / 2) + col * 16, c.v_cache + goff);
+      }
+      const int r = lane & 15;
+      const long long soff = (row0 + r) * c.hkv + w.h;
+      if (lane < 16) cp_async4(st + 2 * G::TILE + r * 4, c.k_scale + soff);
+      else cp_async4(st + 2 * G::TILE + 64 + r * 4, c.v_scale + soff);
+    }
+    if (lane == 0) sflag[stage] = ok;
+  };
+
+  long long ppos = P0;
+#pragma unroll 1
+  for (int s = 0; s < G::STAGES - 1; s++) {
+    if (ppos < P1) {
+      issue(pw, s);
+      ppos++;
+      if (ppos < P1) walk_next(pw, c, pv, true);
+    }
+    cp_async_commit();
+  }
+
+  // per-segment state
+  uint32_t qb[G::KSTEPS][2];
+  float oacc[G::KSTEPS][4];
+  float m0, m1, l0, l1;
+  int lim0, lim1;  // keys visible to columns 2cq, 2cq+1
+  int L = 0;
+  bool first_piece = cw.kb == 0;
+
+  auto begin_segment = [&]() {
+    const int seq = cw.seq;
+    const int q0 = c.qsl[seq];
+    const int ql = c.qsl[seq + 1] - q0;
+    L = c.seq_lens[seq];
+    const int ctx = L - ql;
+    // B fragments of this lane's column n = g
+    const int n = g;
+    const bool colok = n < ql * c.group;
+    const int j = n / c.group, jj = n - j * c.group;
+    const __half* qrow = pv.qrot + ((long long)(q0 + (colok ? j : 0)) * c.hq + cw.h * c.group + (colok ? jj : 0)) * D;
+#pragma unroll
+    for (int w = 0; w < G::KW; w++) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (colok) v = *reinterpret_cast<const uint4*>(qrow + 8 * (cq * G::KW + w));
+      qb[2 * w][0] = __byte_perm(v.x, v.z, 0x5410);
+      qb[2 * w][1] = __byte_perm(v.x, v.z, 0x7632);
+      qb[2 * w + 1][0] = __byte_perm(v.y, v.w, 0x5410);
+      qb[2 * w + 1][1] = __byte_perm(v.y, v.w, 0x7632);
+    }
+    const int col0 = 2 * cq, col1 = 2 * cq + 1;
+    const int j0 = min(col0 / c.group, max(ql - 1, 0)), j1 = min(col1 / c.group, max(ql - 1, 0));
+    lim0 = c.causal ? min(L, ctx + j0 + 1) : L;
+    lim1 = c.causal ? min(L, ctx + j1 + 1) : L;
+#pragma unroll
+    for (int i = 0; i < G::KSTEPS; i++) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  };
+
+  auto flush = [&]() {
+    float a0 = l0, a1 = l1;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+      a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    }
+    float* dst_o;
+    float* dst_ml;
+    if (first_piece) {
+      const long long slot = (long long)cw.i * c.hkv + cw.h;
+      dst_o = pv.direct_o + slot * kDecodeCols * D;
+      dst_ml = pv.direct_ml + slot * kDecodeCols * 2;
+    } else {
+      dst_o = pv.warp_o + (long long)wid * kDecodeCols * D;
+      dst_ml = pv.warp_ml + (long long)wid * kDecodeCols * 2;
+    }
+    // thread holds d = g*D/8 + r (r = 2i + {0,1}) for columns 2cq, 2cq+1
+    float* o0 = dst_o + (2 * cq) * D + g * (D / 8);
+    float* o1 = dst_o + (2 * cq + 1) * D + g * (D / 8);
+#pragma unroll
+    for (int i = 0; i < G::KSTEPS; i += 2) {
+      *reinterpret_cast<float4*>(o0 + 2 * i) = make_float4(oacc[i][0], oacc[i][2], oacc[i + 1][0], oacc[i + 1][2]);
+      *reinterpret_cast<float4*>(o1 + 2 * i) = make_float4(oacc[i][1], oacc[i][3], oacc[i + 1][1], oacc[i + 1][3]);
+    }
+    if (g == 0) {
+      dst_ml[(2 * cq) * 2 + 0] = m0;
+      dst_ml[(2 * cq) * 2 + 1] = a0;
+      dst_ml[(2 * cq + 1) * 2 + 0] = m1;
+      dst_ml[(2 * cq + 1) * 2 + 1] = a1;
+    }
+  };
+
+  begin_segment();
+  int stage = 0;
+  const long long nblocks = P1 - P0;
+#pragma unroll 1
+  for (long long it = 0; it < nblocks; it++) {
+    if (ppos < P1) {
+      issue(pw, (stage + G::STAGES - 1) % G::STAGES);
+      ppos++;
+      if (ppos < P1) walk_next(pw, c, pv, true);
+    }
+    cp_async_commit();
+    cp_async_wait<G::STAGES - 1>();
+    __syncwarp();
+
+    const uint8_t* st = wsm + stage * G::STAGE;
+    const bool bok = sflag[stage] != 0;
+    const float* sks = reinterpret_cast<const float*>(st + 2 * G::TILE);
+    const float* svs = sks + 16;
+
+    // ---- S^T = K Q'^T ----
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      uint32_t xk[G::KW], yk[G::KW];
+      lds_words<G::KW, D / 8>(xk, st + g * (D / 2) + cq * (D / 8));
+      lds_words<G::KW, D / 8>(yk, st + (g + 8) * (D / 2) + cq * (D / 8));
+#pragma unroll
+      for (int w = 0; w < G::KW; w++) {
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          uint32_t a[4];
+          a[0] = nib_to_f16x2(xk[w] >> (8 * e));
+          a[1] = nib_to_f16x2(yk[w] >> (8 * e));
+          a[2] = nib_to_f16x2(xk[w] >> (8 * e + 4));
+          a[3] = nib_to_f16x2(yk[w] >> (8 * e + 4));
+          mma_16816(sacc, a, qb[2 * w + e][0], qb[2 * w + e][1]);
+        }
+      }
+    }
+    const int pos0 = cw.kb * 16 + g, pos1 = pos0 + 8;
+    const bool v00 = bok && pos0 < lim0, v01 = bok && pos0 < lim1;
+    const bool v10 = bok && pos1 < lim0, v11 = bok && pos1 < lim1;
+    const float ks0 = sks[g], ks1 = sks[g + 8];
+    const float s00 = v00 ? sacc[0] * ks0 : -INFINITY;
+    const float s01 = v01 ? sacc[1] * ks0 : -INFINITY;
+    const float s10 = v10 ? sacc[2] * ks1 : -INFINITY;
+    const float s11 = v11 ? sacc[3] * ks1 : -INFINITY;
+    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+    const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
+    const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
+    l0 = l0 * al0 + p00 + p10;
+    l1 = l1 * al1 + p01 + p11;
+    const float vs0 = svs[g], vs1 = svs[g + 8];
+    const uint32_t M0 = pack_f16x2(v00 ? p00 * vs0 : 0.f, v01 ? p01 * vs0 : 0.f);
+    const uint32_t M1 = pack_f16x2(v10 ? p10 * vs1 : 0.f, v11 ? p11 * vs1 : 0.f);
+    const uint32_t b0 = movmatrix_trans(M0), b1 = movmatrix_trans(M1);
+
+    // ---- O'^T += V^T P'^T ----
+    {
+      uint32_t P01[D / 8], P89[D / 8];
+      const uint8_t* sv = st + G::TILE + g * G::VB;
+      v_pairs<D>(P01, sv + (2 * cq) * (D / 2), sv + (2 * cq + 1) * (D / 2));
+      v_pairs<D>(P89, sv + (2 * cq + 8) * (D / 2), sv + (2 * cq + 9) * (D / 2));
+#pragma unroll
+      for (int i = 0; i < G::KSTEPS; i++) {
+        oacc[i][0] *= al0;
+        oacc[i][1] *= al1;
+        oacc[i][2] *= al0;
+        oacc[i][3] *= al1;
+        const uint32_t a[4] = {P01[2 * i], P01[2 * i + 1], P89[2 * i], P89[2 * i + 1]};
+        mma_16816(oacc[i], a, b0, b1);
+      }
+    }
+    __syncwarp();
+
+    const bool last_in_seg = cw.kb == cw.nblk - 1;
+    const bool last_in_range = it + 1 == nblocks;
+    if (last_in_seg || last_in_range) flush();
+    if (!last_in_range) {
+      walk_next(cw, c, pv, true);
+      if (last_in_seg) {
+        first_piece = true;
+        begin_segment();
+      }
+    }
+    stage = (stage + 1) % G::STAGES;
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+// 4. reduce: merge decode pieces, normalise, inverse-rotate, write bf16
+// ---------------------------------------------------------------------------
+struct RedParams {
+  Common c;
+  PlanView pv;
+  int total_warps;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm) {
+  const Common& c = prm.c;
+  const PlanView& pv = prm.pv;
+  constexpr int B = Head<D>::b;
+  __shared__ float srow[kDecodeCols][D];
+  const int seg = blockIdx.x;
+  const int n_dseq = pv.plan[0];
+  if (seg >= n_dseq * c.hkv) return;
+  const int i = seg / c.hkv, h = seg - i * c.hkv;
+  const int seq = pv.dseq[i];
+  const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+  const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (col >= ql * c.group) return;
+  const int nblk = (c.seq_lens[seq] + 15) / 16;
+  const long long Tb = pv.dprefix[n_dseq] * c.hkv;
+  const long long sbeg = pv.dprefix[i] * c.hkv + (long long)h * nblk, send = sbeg + nblk;
+  const int W = prm.total_warps;
+  auto wstart = [&](long long w) { return Tb * w / W; };
+
+  constexpr int PER = D / 32;
+  float acc[PER];
+  const float* od = pv.direct_o + ((long long)seg * kDecodeCols + col) * D;
+  float M = pv.direct_ml[((long long)seg * kDecodeCols + col) * 2];
+  float Lsum = pv.direct_ml[((long long)seg * kDecodeCols + col) * 2 + 1];
+#pragma unroll
+  for (int k = 0; k < PER; k++) acc[k] = od[lane + 32 * k];
+  // warps whose (non-empty) range starts strictly inside this segment
+  long long w = (sbeg * W) / Tb;
+  while (w < W && wstart(w) <= sbeg) w++;
+  for (; w < W && wstart(w) < send; w++) {
+    if (wstart(w + 1) <= wstart(w)) continue;
+    const float* ow = pv.warp_o + (w * kDecodeCols + col) * D;
+    const float mw = pv.warp_ml[(w * kDecodeCols + col) * 2];
+    const float lw = pv.warp_ml[(w * kDecodeCols + col) * 2 + 1];
+    const float Mn = fmaxf(M, mw);
+    const float Mu = Mn == -INFINITY ? 0.f : Mn;
+    const float a = fast_exp2(M - Mu), b = fast_exp2(mw - Mu);
+#pragma unroll
+    for (int k = 0; k < PER; k++) acc[k] = acc[k] * a + ow[lane + 32 * k] * b;
+    Lsum = Lsum * a + lw * b;
+    M = Mn;
+  }
+  float* r = srow[col];
+  const float inv = 1.f / (Lsum * (float)B);
+#pragma unroll
+  for (int k = 0; k < PER; k++) r[lane + 32 * k] = acc[k] * inv;
+  __syncwarp();
+#pragma unroll 1
+  for (int hh = 1; hh < B; hh <<= 1) {
+    for (int p = lane; p < D / 2; p += 32) {
+      const int ii = (p / hh) * 2 * hh + (p % hh);
+      const float a = r[ii], b = r[ii + hh];
+      r[ii] = a + b;
+      r[ii + hh] = a - b;
+    }
+    __syncwarp();
+  }
+  const int j = col / c.group, jj = col - j * c.group;
+  uint16_t* dst = c.out + (long long)(q0 + j) * c.out_stride + (long long)(h * c.group + jj) * D;
+  for (int p = lane; p < D / 2; p += 32) {
+    const float x0 = c.signs[2 * p] < 0 ? -r[2 * p] : r[2 * p];
+    const float x1 = c.signs[2 * p + 1] < 0 ? -r[2 * p + 1] : r[2 * p + 1];
+    reinterpret_cast<uint32_t*>(dst)[p] = pack_bf16x2_rn(x0, x1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. prefill: FA2-style, 64 query rows x 16 keys per step, mma.sync
+// ---------------------------------------------------------------------------
+template <int D>
+struct PreGeom {
+  static constexpr int WARPS = 4;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int ROWS = kPrefillRows;  // 16 per warp
+  static constexpr int STAGES = 3;
+  static constexpr int TILE = 16 * D / 2;
+  static constexpr int STAGE = 2 * TILE + 2 * 16 * 4;
+  static constexpr int HSTRIDE = D + 8;  // halves per row of the f16 tiles (odd multiple of 16 B)
+  static constexpr int SMEM = STAGES * STAGE + ROWS * HSTRIDE * 2 + 2 * 16 * HSTRIDE * 2 + D * 4 + 64;
+};
+
+struct PreParams {
+  Common c;
+  PlanView pv;
+};
+
+template <int D>
+__global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams prm) {
+  using G = PreGeom<D>;
+  constexpr int B = Head<D>::b;
+  constexpr int NT = D / 8;  // n-tiles of the output
+  const Common& c = prm.c;
+  const PlanView& pv = prm.pv;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* stages = smem;
+  __half* sQ = reinterpret_cast<__half*>(smem + G::STAGES * G::STAGE);
+  __half* sK = sQ + G::ROWS * G::HSTRIDE;
+  __half* sV = sK + 16 * G::HSTRIDE;
+  float* ssign = reinterpret_cast<float*>(sV + 16 * G::HSTRIDE);
+  int* sitem = reinterpret_cast<int*>(ssign + D);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, cq = lane & 3;
+  for (int i = tid; i < D; i += G::THREADS) ssign[i] = c.signs[i] < 0 ? -1.f : 1.f;
+  const int n_items = pv.plan[1];
+
+#pragma unroll 1
+  while (true) {
+    if (tid == 0) sitem[0] = atomicAdd(&pv.plan[2], 1);
+    __syncthreads();
+    const int itn = sitem[0];
+    __syncthreads();
+    if (itn >= n_items) break;
+    const int4 item = pv.pitems[itn];
+    const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
+    const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+    const int L = c.seq_lens[seq], ctx = L - ql;
+    const int tok0 = tile * c.tile_tokens;
+    const int ntok = min(c.tile_tokens, ql - tok0);
+    const int nrows = ntok * c.group;
+
+    // Q tile -> shared (rows beyond the tile are zero)
+    for (int idx = tid; idx < G::ROWS * (D / 8); idx += G::THREADS) {
+      const int r = idx / (D / 8), ch = idx - r * (D / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < nrows) {
+        const int j = r / c.group, jj = r - j * c.group;
+        v = *reinterpret_cast<const uint4*>(pv.qrot + ((long long)(q0 + tok0 + j) * c.hq + h * c.group + jj) * D + ch * 8);
+      }
+      *reinterpret_cast<uint4*>(sQ + r * G::HSTRIDE + ch * 8) = v;
+    }
+
+    auto issue = [&](int kb, int stage) {
+      uint8_t* st = stages + stage * G::STAGE;
+      const int blk = c.block_table[(long long)seq * c.max_blocks + kb];
+      if (blk < 0 || blk >= c.num_blocks) return;  // reported and masked by the consumer
+      const long long row0 = (long long)blk * 16;
+      for (int q = tid; q < D / 2; q += G::THREADS) {
+        const int r = q / (D / 32), col = q - r * (D / 32);
+        const long long goff = ((row0 + r) * c.hkv + h) * (D / 2) + col * 16;
+        cp_async16(st + r * (D / 2) + col * 16, c.k_cache + goff);
+        cp_async16(st + G::TILE + r * (D / 2) + col * 16, c.v_cache + goff);
+      }
+      if (tid < 32) {
+        const int r = tid & 15;
+        const long long soff = (row0 + r) * c.hkv + h;
+        if (tid < 16) cp_async4(st + 2 * G::TILE + r * 4, c.k_scale + soff);
+        else cp_async4(st + 2 * G::TILE + 64 + r * 4, c.v_scale + soff);
+      }
+    };
+
+    for (int s = 0; s < G::STAGES - 1; s++) {
+      if (s < nkb) issue(s, s);
+      cp_async_commit();
+    }
+
+    float oacc[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; t++) oacc[t][0] = oacc[t][1] = oacc[t][2] = oacc[t][3] = 0.f;
+    float mr0 = -INFINITY, mr1 = -INFINITY, lr0 = 0.f, lr1 = 0.f;
+    const int r0 = warp * 16 + g, r1 = r0 + 8;
+    const int qp0 = ctx + tok0 + (r0 < nrows ? r0 / c.group : 0);
+    const int qp1 = ctx + tok0 + (r1 < nrows ? r1 / c.group : 0);
+    const int lim0 = c.causal ? min(L, qp0 + 1) : L;
+    const int lim1 = c.causal ? min(L, qp1 + 1) : L;
+
+#pragma unroll 1
+    for (int kb = 0; kb < nkb; kb++) {
+      const int stage = kb % G::STAGES;
+      if (kb + G::STAGES - 1 < nkb) issue(kb + G::STAGES - 1, (kb + G::STAGES - 1) % G::STAGES);
+      cp_async_commit();
+      cp_async_wait<G::STAGES - 1>();
+      __syncthreads();
+      const int blk = c.block_table[(long long)seq * c.max_blocks + kb];
+      const bool bok = blk >= 0 && blk < c.num_blocks;
+      if (!bok && tid == 0) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
+      const uint8_t* st = stages + stage * G::STAGE;
+      // dequantise K and V codes of this block into f16 rows (natural order)
+      for (int q = tid; q < 2 * 16 * (D / 8); q += G::THREADS) {
+        const int which = q / (16 * (D / 8));
+        const int rem = q - which * 16 * (D / 8);
+        const int r = rem / (D / 8), w = rem - r * (D / 8);
+        const uint32_t x = bok ? reinterpret_cast<const uint32_t*>(st + which * G::TILE + r * (D / 2))[w] : 0x88888888u;
+        const uint32_t p0 = nib_to_f16x2(x), p1 = nib_to_f16x2(x >> 4), p2 = nib_to_f16x2(x >> 8),
+                       p3 = nib_to_f16x2(x >> 12);
+        // p_k = (element k, element k+4) -> natural order 0..7
+        uint4 o;
+        o.x = __byte_perm(p0, p1, 0x5410);
+        o.y = __byte_perm(p2, p3, 0x5410);
+        o.z = __byte_perm(p0, p1, 0x7632);
+        o.w = __byte_perm(p2, p3, 0x7632);
+        __half* dst = (which ? sV : sK) + r * G::HSTRIDE + w * 8;
+        *reinterpret_cast<uint4*>(dst) = o;
+      }
+      __syncthreads();
+      const float* sks = reinterpret_cast<const float*>(st + 2 * G::TILE);
+      const float* svs = sks + 16;
+
+      // S = Q' K^T : 16 rows x 16 keys per warp
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int s = 0; s < D / 16; s++) {
+        uint32_t a[4], bk[4];
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          ldmatrix_x4(a, sQ + (warp * 16 + (mi & 1) * 8 + rr) * G::HSTRIDE + 16 * s + (mi >> 1) * 8);
+          ldmatrix_x4(bk, sK + ((mi >> 1) * 8 + rr) * G::HSTRIDE + 16 * s + (mi & 1) * 8);
+        }
+        mma_16816(sacc[0], a, bk[0], bk[1]);
+        mma_16816(sacc[1], a, bk[2], bk[3]);
+      }
+      // scale, mask, online softmax (rows r0, r1; keys 2cq, 2cq+1, 8+2cq, 9+2cq)
+      float sv[2][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; nt++) {
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          const int key = nt * 8 + 2 * cq + e;
+          const int pos = kb * 16 + key;
+          const float ks = sks[key];
+          sv[nt][e] = (bok && pos < lim0) ? sacc[nt][e] * ks : -INFINITY;
+          sv[nt][2 + e] = (bok && pos < lim1) ? sacc[nt][2 + e] * ks : -INFINITY;
+          mx0 = fmaxf(mx0, sv[nt][e]);
+          mx1 = fmaxf(mx1, sv[nt][2 + e]);
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = fast_exp2(mr0 - mu0), al1 = fast_exp2(mr1 - mu1);
+      mr0 = mn0;
+      mr1 = mn1;
+      uint32_t pa[4];
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; nt++) {
+        float pw[4];
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          const int key = nt * 8 + 2 * cq + e;
+          const float vs = svs[key];
+          const float p0 = fast_exp2(sv[nt][e] - mu0);
+          const float p1 = fast_exp2(sv[nt][2 + e] - mu1);
+          ps0 += p0;
+          ps1 += p1;
+          pw[e] = sv[nt][e] == -INFINITY ? 0.f : p0 * vs;
+          pw[2 + e] = sv[nt][2 + e] == -INFINITY ? 0.f : p1 * vs;
+        }
+        pa[2 * nt + 0] = pack_f16x2(pw[0], pw[1]);  // row r0, keys nt*8 + 2cq..
+        pa[2 * nt + 1] = pack_f16x2(pw[2], pw[3]);  // row r1
+      }
+      lr0 = lr0 * al0 + ps0;
+      lr1 = lr1 * al1 + ps1;
+      // A fragment order: (r0, k 0-7), (r1, k 0-7), (r0, k 8-15), (r1, k 8-15)
+      const uint32_t afr[4] = {pa[0], pa[1], pa[2], pa[3]};
+#pragma unroll
+      for (int t = 0; t < NT; t += 2) {
+        uint32_t bv[4];
+        const int mi = lane >> 3, rr = lane & 7;
+        ldmatrix_x4_trans(bv, sV + ((mi & 1) * 8 + rr) * G::HSTRIDE + 8 * (t + (mi >> 1)));
+        oacc[t][0] *= al0; oacc[t][1] *= al0; oacc[t][2] *= al1; oacc[t][3] *= al1;
+        oacc[t + 1][0] *= al0; oacc[t + 1][1] *= al0; oacc[t + 1][2] *= al1; oacc[t + 1][3] *= al1;
+        mma_16816(oacc[t], afr, bv[0], bv[1]);
+        mma_16816(oacc[t + 1], afr, bv[2], bv[3]);
+      }
+    }
+    cp_async_wait<0>();
+
+    // epilogue: normalise, inverse rotation over d, signs, /b, bf16 store
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      lr0 += __shfl_xor_sync(0xffffffffu, lr0, o);
+      lr1 += __shfl_xor_sync(0xffffffffu, lr1, o);
+    }
+    const float inv0 = 1.f / (lr0 * (float)B), inv1 = 1.f / (lr1 * (float)B);
+    // thread values: row r0 -> oacc[t][0..1] (d = 8t + 2cq + e), row r1 -> oacc[t][2..3]
+#pragma unroll
+    for (int t = 0; t < NT; t++) {  // stage h = 1
+      float a = oacc[t][0], b = oacc[t][1];
+      oacc[t][0] = a + b; oacc[t][1] = a - b;
+      a = oacc[t][2]; b = oacc[t][3];
+      oacc[t][2] = a + b; oacc[t][3] = a - b;
+    }
+#pragma unroll
+    for (int lb = 0; lb < 2; lb++) {  // stages h = 2, 4 across the quad
+      if ((2 << lb) >= B) break;
+      const bool upper = (cq >> lb) & 1;
+#pragma unroll
+      for (int t = 0; t < NT; t++) {
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const float mine = oacc[t][e];
+          const float other = __shfl_xor_sync(0xffffffffu, mine, 1 << lb);
+          oacc[t][e] = upper ? other - mine : mine + other;
+        }
+      }
+    }
+#pragma unroll
+    for (int ht = 1; ht < NT; ht <<= 1) {  // stages h = 8, 16, ... over t
+      if (8 * ht >= B) break;
+#pragma unroll
+      for (int t = 0; t < NT; t++) {
+        if ((t & ht) == 0) {
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const float a = oacc[t][e], b = oacc[t + ht][e];
+            oacc[t][e] = a + b;
+            oacc[t + ht][e] = a - b;
+          }
+        }
+      }
+    }
+    if (r0 < nrows) {
+      const int j = r0 / c.group, jj = r0 - j * c.group;
+      uint16_t* dst = c.out + (long long)(q0 + tok0 + j) * c.out_stride + (long long)(h * c.group + jj) * D;
+#pragma unroll
+      for (int t = 0; t < NT; t++) {
+        const int d = 8 * t + 2 * cq;
+        reinterpret_cast<uint32_t*>(dst + d)[0] =
+            pack_bf16x2_rn(oacc[t][0] * inv0 * ssign[d], oacc[t][1] * inv0 * ssign[d + 1]);
+      }
+    }
+    if (r1 < nrows) {
+      const int j = r1 / c.group, jj = r1 - j * c.group;
+      uint16_t* dst = c.out + (long long)(q0 + tok0 + j) * c.out_stride + (long long)(h * c.group + jj) * D;
+#pragma unroll
+      for (int t = 0; t < NT; t++) {
+        const int d = 8 * t + 2 * cq;
+        reinterpret_cast<uint32_t*>(dst + d)[0] =
+            pack_bf16x2_rn(oacc[t][2] * inv1 * ssign[d], oacc[t][3] * inv1 * ssign[d + 1]);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launcher
+// ---------------------------------------------------------------------------
+template <typename K>
+static bool configure(K kern, int smem, int threads, int* occ_out, bool* done, int* occ_cache) {
+  if (!*done) {
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return false;
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem) != cudaSuccess || o < 1) return false;
+    *occ_cache = o;
+    *done = true;
+  }
+  *occ_out = *occ_cache;
+  return true;
+}
+
+template <int D>
+static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
+  WorkspaceLayout L;
+  workspace_layout(a.num_seqs, a.num_q_tokens, a.num_q_heads, a.num_kv_heads, a.head_size, &L);
+  PlanView pv = plan_view(a.workspace, L);
+  const int dev = current_device();
+  const int sms = sm_count(dev);
+  Common c;
+  c.q = static_cast<const uint16_t*>(a.q);
+  c.q_stride = a.q_stride;
+  c.k_cache = a.k_cache;
+  c.v_cache = a.v_cache;
+  c.k_scale = a.k_scale;
+  c.v_scale = a.v_scale;
+  c.block_table = a.block_table;
+  c.max_blocks = a.max_blocks_per_seq;
+  c.seq_lens = a.seq_lens;
+  c.qsl = a.query_start_loc;
+  c.num_seqs = a.num_seqs;
+  c.num_q_tokens = a.num_q_tokens;
+  c.hq = a.num_q_heads;
+  c.hkv = a.num_kv_heads;
+  c.group = a.num_q_heads / a.num_kv_heads;
+  c.num_blocks = a.num_blocks;
+  c.causal = a.causal;
+  c.qscale = a.softmax_scale * kLog2e / (float)Head<D>::b;
+  c.signs = a.signs;
+  c.out = static_cast<uint16_t*>(a.out);
+  c.out_stride = a.out_stride;
+  c.status = a.dev_status;
+  c.tile_tokens = kPrefillRows / c.group > 0 ? kPrefillRows / c.group : 1;
+  c.max_items = L.max_prefill_items;
+  if (c.group > kPrefillRows) return KV_INT4_ERR_HEADS;
+
+  // 1. prep
+  {
+    const long long rows = (long long)a.num_q_tokens * a.num_q_heads;
+    const long long grid = 1 + (rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta;
+    if (grid > 0x7fffffff) return KV_INT4_ERR_SIZE;
+    prep_kernel<D><<<(unsigned)grid, kPrepThreads, 0, stream>>>(c, pv);
+    if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
+  }
+  // 2. prefill
+  const bool may_prefill = c.group > kDecodeCols || (long long)a.max_query_len * c.group > kDecodeCols;
+  if (may_prefill) {
+    using G = PreGeom<D>;
+    static bool done[kMaxDevices] = {};
+    static int occ_c[kMaxDevices] = {};
+    int occ = 0;
+    if (!configure(prefill_kernel<D>, G::SMEM, G::THREADS, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
+    long long grid = (long long)sms * occ;
+    if (grid > L.max_prefill_items) grid = L.max_prefill_items;
+    if (grid < 1) grid = 1;
+    prefill_kernel<D><<<(unsigned)grid, G::THREADS, G::SMEM, stream>>>(PreParams{c, pv});
+    if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
+  }
+  // 3. decode + 4. reduce
+  if (c.group <= kDecodeCols) {
+    using G = DecGeom<D>;
+    static bool done[kMaxDevices] = {};
+    static int occ_c[kMaxDevices] = {};
+    int occ = 0;
+    if (!configure(decode_kernel<D>, G::SMEM, G::WARPS * 32, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
+    long long grid = (long long)sms * occ;
+    if (grid * G::WARPS > kMaxDecodeWarps) grid = kMaxDecodeWarps / G::WARPS;
+    const int total_warps = (int)grid * G::WARPS;
+    decode_kernel<D><<<(unsigned)grid, G::WARPS * 32, G::SMEM, stream>>>(DecParams{c, pv, total_warps});
+    if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
+    const long long rgrid = (long long)a.num_seqs * a.num_kv_heads;
+    if (rgrid > 0x7fffffff) return KV_INT4_ERR_SIZE;
+    reduce_kernel<D><<<(unsigned)rgrid, kDecodeCols * 32, 0, stream>>>(RedParams{c, pv, total_warps});
+    if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
+  }
+  return KV_INT4_OK;
+}
+
+int launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  switch (a.head_size) {
+    case 64: return launch_attention_t<64>(a, stream);
+    case 96: return launch_attention_t<96>(a, stream);
+    case 128: return launch_attention_t<128>(a, stream);
+    case 192: return launch_attention_t<192>(a, stream);
+    case 256: return launch_attention_t<256>(a, stream);
+    default: return KV_INT4_ERR_HEAD_SIZE;
+  }
+}
+
+}  // namespace kvint4

@@ -1,0 +1,123 @@
+// Device helpers shared by the write and attention kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvint4.h"
+
+namespace kvint4 {
+
+// ---------------------------------------------------------------------------
+// compile-time head geometry
+// ---------------------------------------------------------------------------
+template <int D>
+struct Head {
+  static constexpr int d = D;
+  static constexpr int b = D & -D;          // largest power-of-two divisor
+  static constexpr int n = D / b;           // number of Hadamard blocks
+  static constexpr int log2b = (b >= 256) ? 8 : (b >= 128) ? 7 : (b >= 64) ? 6 : (b >= 32) ? 5 : 4;
+  static constexpr int bytes = D / 2;       // packed INT4 bytes per head vector
+};
+
+__device__ __forceinline__ void flag(int32_t* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------------------
+// cp.async (LDGSTS) staging
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem)), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_addr(smem)), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32 bit manipulation (bf16 is the high half of an fp32 pattern)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// running max of |x| over both halves of a bf16x2 word (sign of the result is
+// meaningless; only the magnitude is used)
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// INT4 nibble -> f16 exact conversion.
+// An f16 with exponent field 25 (value 1024..2047) has unit spacing, so the
+// bit pattern 0x6400 | u is exactly 1024 + u for u in [0, 15].  A stored
+// nibble n is the two's-complement code c & 0xF; u = n ^ 8 = c + 8 is the
+// offset-binary form, so (n ^ 0x6408) is exactly 1032 + c and subtracting
+// 1032 (exact) yields c.  lo/hi halves are processed together as f16x2.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t nib_to_f16x2(uint32_t x) {
+  // takes the nibbles at bits [0,4) and [16,20) of x
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(x), "r"(0x000f000fu), "r"(0x64086408u));
+  // 0x6a = (a & b) ^ c
+  __half2 h = *reinterpret_cast<__half2*>(&r);
+  h = __hsub2(h, __half2half2(__ushort_as_half((unsigned short)0x6408)));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// tensor-core fragments (legacy warp-level MMA, f16 inputs, f32 accumulate)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+  return r;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+}  // namespace kvint4

@@ -1,0 +1,93 @@
+// Host-side internal interface between the C ABI (api.cu) and the kernel
+// launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvint4 {
+
+constexpr int kMaxDevices = 64;
+
+// current device index (clamped to [0, kMaxDevices)); -1 on failure
+int current_device();
+// cached multiprocessor count of device `dev`
+int sm_count(int dev);
+
+struct WriteArgs {
+  const void* k;
+  int64_t k_stride;
+  const void* v;
+  int64_t v_stride;
+  const int64_t* slot_mapping;
+  int num_tokens;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  float* k_scale;
+  float* v_scale;
+  int num_blocks;
+  int block_size;
+  int num_kv_heads;
+  int head_size;
+  const int8_t* signs;
+  int32_t* dev_status;
+};
+
+int launch_write(const WriteArgs& a, bool prerotated, cudaStream_t stream);
+
+struct AttnArgs {
+  const void* q;
+  int64_t q_stride;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;
+  int max_blocks_per_seq;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int num_seqs;
+  int num_q_tokens;
+  int max_query_len;
+  int max_seq_len;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_size;
+  int block_size;
+  int num_blocks;
+  float softmax_scale;
+  int causal;
+  const int8_t* signs;
+  void* out;
+  int64_t out_stride;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;
+};
+
+// Workspace layout, shared by the size query and the launcher.
+struct WorkspaceLayout {
+  size_t plan;          // int32 counters + per-seq schedule
+  size_t dseq;          // int32 [num_seqs] decode-sequence list
+  size_t dprefix;       // int64 [num_seqs + 1] block prefix over decode sequences
+  size_t pitems;        // int4 [max_prefill_items] prefill work list
+  size_t qrot;          // f16 [num_q_tokens][Hq][d] rotated, pre-scaled queries
+  size_t direct_o;      // f32 [num_seqs][Hkv][8][d]
+  size_t direct_ml;     // f32 [num_seqs][Hkv][8][2]
+  size_t warp_o;        // f32 [kMaxDecodeWarps][8][d]
+  size_t warp_ml;       // f32 [kMaxDecodeWarps][8][2]
+  size_t total;
+  int64_t max_prefill_items;
+};
+
+constexpr int kMaxDecodeWarps = 4096;
+constexpr int kDecodeCols = 8;      // query columns (q token x q head) per decode work unit
+constexpr int kPrefillRows = 64;    // query rows (q token x q head) per prefill tile
+
+bool workspace_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
+                      int head_size, WorkspaceLayout* out);
+
+int launch_attention(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace kvint4

@@ -1,0 +1,63 @@
+"""Shared test helpers: run the oracle on a synthetic workload, compare outputs."""
+
+import math
+
+import numpy as np
+import torch
+
+from oracle import kvint4_oracle as O
+
+
+def np_cache(w):
+    return [t.numpy() for t in w.empty_cache("cpu")]
+
+
+def oracle_write_history_and_step(w, caches=None):
+    """Oracle write of every history token and every step token (on CPU)."""
+    kc, vc, ks, vs = caches if caches is not None else np_cache(w)
+    signs = w.signs.numpy()
+    for s, (q, kv) in enumerate(w.seqs):
+        k, v = w.seq_kv(s, "cpu")
+        O.write_cache(k.float().numpy(), v.float().numpy(), w.slots(s, 0, kv).numpy(), kc, vc, ks, vs,
+                      w.block_size, signs)
+    return kc, vc, ks, vs
+
+
+def oracle_attention(w, q, caches, seqs=None, heads=None):
+    kc, vc, ks, vs = caches
+    qn = q.float().cpu().numpy()
+    bt = w.block_table.numpy()
+    sl = w.seq_lens.numpy()
+    qsl = w.query_start_loc.numpy()
+    scale = 1.0 / math.sqrt(w.head_size)
+    if seqs is None:
+        return O.attention(qn, kc, vc, ks, vs, bt, sl, qsl, w.num_kv_heads, w.block_size, scale, w.causal,
+                           w.signs.numpy())
+    out = {}
+    for s in seqs:
+        out[s] = O.attention_seq(qn, kc, vc, ks, vs, bt, sl, qsl, s, w.num_kv_heads, w.block_size, scale,
+                                 w.causal, w.signs.numpy(), q_heads=heads)
+    return out
+
+
+def corr(a, b):
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(np.corrcoef(a, b)[0, 1])
+
+
+def assert_close_attention(got, ref, atol=5e-2, rtol=5e-2, min_corr=0.9999, what=""):
+    """The attention bar: atol = rtol = 5e-2 elementwise and correlation >= 0.9999."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside atol=rtol={atol}; max abs err {err.max():.4g}"
+    c = corr(got, ref)
+    assert c >= min_corr, f"{what}: corr {c:.6f} < {min_corr}"
+    return float(err.max()), c
+
+
+def f32_bits(x):
+    return np.asarray(x, np.float32).view(np.uint32)
