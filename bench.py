@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark of the INT4 per-token-head KV cache hot path on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+write the step's new K/V (randomized Hadamard rotation, bf16 rounding,
+absmax scale, INT4 pack, slot scatter) and then paged attention over the
+INT4 cache (query rotation, dequantised tiles, online softmax, split-KV
+reduce, inverse rotation).  The default workload is the long-context decode
+batch (Llama-3-8B shape: 32 q / 8 kv heads, head 128, block 16, 256
+sequences x 32768 keys, a 9.1 GB cache, larger than L2, so no flush is
+needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+prints one JSON line.  Under torchrun (N > 1) every rank runs its own
+replica of the workload (weak scaling, no collective on the data path); the
+timed region is bracketed by a barrier and synchronize on every rank and
+the slowest rank's time is used.
+
+--impl reference times the fp64 CPU oracle on the host cores (rank 0 only)
+on a bounded sample of the same workload: each step is the oracle's write of
+one new token plus its attention for one (sequence, kv head) unit of the
+batch, i.e. 1/num_kv_heads of a decode token.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "INT4-KV paged decode: KV-read GB/s vs HBM peak, tokens/s; RHT+quant write GB/s"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_TEXT = {
+    "tiny": "tiny causal: 4 q / 4 kv heads, head 128, block 16, seqs (q,kv) = (4,128),(4,97)",
+    "phi3": "Phi-3-mini decode: 32 q / 32 kv heads, head 96 (b=32, n=3), block 16, batch 32 x kv 1024, 1% outlier channels x8",
+    "gqa": "Llama-3.2-1B GQA decode: 32 q / 8 kv heads, head 128, block 16, batch 64, kv ~ U[512, 8192]",
+    "mixed": "mixed varlen: 16 q / 4 kv heads, head 192 (b=64, n=3), block 16, 8 causal prefills q=kv ~ U[512,2048] + 120 decodes kv ~ U[1024,16384], shuffled order",
+    "long": "long-context decode: Llama-3-8B shape, 32 q / 8 kv heads, head 128, block 16, batch 256 x kv 32768",
+}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host side only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_setup(use_cuda: bool):
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if use_cuda else "gloo"
+        if use_cuda:
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own replica of the workload (weak scaling)."""
+    return base_seed + 7919 * rank
+
+
+def barrier(device):
+    import torch
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "int4_token_head_gb300", "csrc", kv.get("source", "attention.cu"))
+    if kv.get("source_sha") != source_sha(src):
+        return None
+    try:
+        return float(kv["bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--id={gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for_smi(dev_index: int) -> str:
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(dev_index).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return str(dev_index)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleUnits:
+    """A pool of (sequence, kv head) units of the workload, each with its own
+    oracle-written cache; a step is the oracle's write of the unit's new
+    token plus its attention for the unit's q heads."""
+
+    def __init__(self, w, n_units: int, gen_device: str):
+        import numpy as np
+        from oracle import kvint4_oracle as O
+        self.O, self.np = O, np
+        self.w = w
+        self.units = []
+        q_all = w.queries(gen_device).float().cpu().numpy()
+        qsl = w.query_start_loc.numpy()
+        order = [(s, h) for s in range(w.num_seqs) for h in range(w.num_kv_heads)]
+        stride = max(1, len(order) // max(1, n_units))
+        picks = order[::stride][:n_units]
+        for s, h in picks:
+            ql, L = w.seqs[s]
+            k, v = w.seq_kv(s, gen_device)
+            k = k[:, h:h + 1].float().cpu().numpy()
+            v = v[:, h:h + 1].float().cpu().numpy()
+            nblk = (L + w.block_size - 1) // w.block_size
+            kc = np.full((nblk, w.block_size, 1, w.head_size // 2), 0xA5, np.uint8)
+            vc = kc.copy()
+            ks = np.full((nblk, w.block_size, 1), np.nan, np.float32)
+            vs = ks.copy()
+            O.write_cache(k[:L - ql], v[:L - ql], np.arange(L - ql), kc, vc, ks, vs, w.block_size,
+                          w.signs.numpy())
+            q = q_all[qsl[s]:qsl[s + 1], h * w.group:(h + 1) * w.group]
+            self.units.append(dict(k_new=k[L - ql:], v_new=v[L - ql:], slots=np.arange(L - ql, L),
+                                   caches=(kc, vc, ks, vs), q=q, L=L, ql=ql, nblk=nblk))
+
+    def step(self, i: int):
+        u = self.units[i % len(self.units)]
+        O, np, w = self.O, self.np, self.w
+        kc, vc, ks, vs = u["caches"]
+        O.write_cache(u["k_new"], u["v_new"], u["slots"], kc, vc, ks, vs, w.block_size, w.signs.numpy())
+        return O.attention_seq(u["q"], kc, vc, ks, vs, np.arange(u["nblk"])[None], [u["L"]], [0, u["ql"]], 0, 1,
+                               w.block_size, 1.0 / math.sqrt(w.head_size), w.causal, w.signs.numpy())
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def time_oracle(w, gen_device, max_seconds: float, min_steps: int = 3, fixed_steps=None, warmup: int = 1,
+                n_units: int = 2):
+    pool = OracleUnits(w, n_units, gen_device)
+    for i in range(warmup):
+        pool.step(i)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        pool.step(n)
+        n += 1
+        el = time.perf_counter() - t0
+        if fixed_steps is not None:
+            if n >= fixed_steps:
+                break
+        elif n >= min_steps and el >= max_seconds:
+            break
+    el = time.perf_counter() - t0
+    tokens = n / w.num_kv_heads
+    return tokens / el, n, el, pool
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    from int4_token_head_gb300 import _lib, synthetic
+    from int4_token_head_gb300.paged import PagedKV
+
+    rank, world, local = dist_setup(use_cuda=True)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _lib.load()
+    overrides = {}
+    if args.batch:
+        overrides["batch"] = args.batch
+    w = synthetic.make_workload(args.workload, **overrides)
+    w = synthetic.make_workload(args.workload, seed=replica_seed(w.seed, rank), **overrides)
+    pk = PagedKV(w, device=str(dev))
+
+    # population of the history = the bulk write measurement (65,536-token chunks)
+    write_times = []
+    pk.populate_history(chunk_tokens=65536, timer=write_times)
+    torch.cuda.synchronize()
+    q, k_new, v_new, slots = pk.step_inputs()
+    out = torch.empty((w.num_q_tokens, w.num_q_heads, w.head_size), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        pk.step(q, k_new, v_new, slots, out)
+    torch.cuda.synchronize()
+    if pk.status.item() != 0:
+        raise RuntimeError(f"device status {pk.status.item()} during warm-up")
+
+    # ---- device-timed region: inputs resident in HBM ----
+    sampler = ClockSampler(gpu_id_for_smi(local))
+    barrier(dev)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    _lib.timing_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        pk.step(q, k_new, v_new, slots, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _lib.timing_enable(False)
+    kern = _lib.timing_collect()
+    clocks = sampler.stop()
+    barrier(dev)
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
+    ms_step = ms_total / args.steps
+    value = aggregate_throughput(w.num_q_tokens * args.steps, world, ms_total / 1e3)
+
+    # ---- end to end through the C ABI with host buffers ----
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_k, h_v, h_s = pin(q), pin(k_new), pin(v_new), pin(slots)
+    h_sl, h_qsl = pin(pk.seq_lens), pin(pk.query_start_loc)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_k, d_v, d_s = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(slots)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s, h_sl, h_qsl))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_s.copy_(h_s, non_blocking=True)
+        pk.seq_lens.copy_(h_sl, non_blocking=True)
+        pk.query_start_loc.copy_(h_qsl, non_blocking=True)
+        pk.step(d_q, d_k, d_v, d_s, out)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dev)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
+    e2e_value = aggregate_throughput(w.num_q_tokens * args.steps, world, e2e_ms / 1e3)
+    if pk.status.item() != 0:
+        raise RuntimeError(f"device status {pk.status.item()} during the timed region")
+
+    # ---- roofline of the dominant kernel ----
+    peak, peak_kind = load_peaks()
+    dom = max(("decode", "prefill"), key=lambda k: kern[k][0])
+    dom_ms, dom_n, _ = kern[dom]
+    d, hkv, hq = w.head_size, w.num_kv_heads, w.num_q_heads
+    if dom == "decode":
+        seqs = [(ql, kv) for ql, kv in w.seqs if ql * w.group <= 8 and w.group <= 8]
+    else:
+        seqs = [(ql, kv) for ql, kv in w.seqs if not (ql * w.group <= 8 and w.group <= 8)]
+    algo = sum(kv * hkv * 2 * (d // 2 + 4) + 4 * ((kv + 15) // 16) + ql * hq * d * 2 for ql, kv in seqs)
+    achieved = algo / (dom_ms / dom_n / 1e3) / 1e9 if dom_n else None
+    traffic = recorded_traffic(dom, args.workload)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
+                "traffic": traffic, "kernel": f"{dom}_kernel", "peak_source": f"{peak_kind} (HBM copy)",
+                "algorithmic_bytes_per_launch": algo,
+                "avg_launch_ms": round(dom_ms / dom_n, 5) if dom_n else None}
+
+    # whole-attention and write throughput
+    attn_bytes = pk.kv_bytes_read()
+    attn_ms = sum(kern[k][0] for k in ("prep", "prefill", "decode", "reduce")) / args.steps
+    wr_gbs = [pk.write_bytes(n) / (ms / 1e3) / 1e9 for ms, n in write_times if ms > 0]
+    write_info = {"median_gbs": round(statistics.median(wr_gbs), 1) if wr_gbs else None,
+                  "frac": round(statistics.median(wr_gbs) / peak, 4) if wr_gbs else None,
+                  "chunks": len(wr_gbs), "tokens_per_chunk": write_times[0][1] if write_times else 0,
+                  "step_write_us": round(kern["write"][0] / max(1, kern["write"][1]) * 1e3, 2)}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 codes, f16 mma / f32 accumulate, f32 rotation",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q; no dataset or weights)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+                   "global_batch": w.num_seqs * world, "seq_len": w.max_seq_len,
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "inputs larger than L2 (cache %.2f GB), no flush" % (
+                       (pk.k_cache.numel() * 2 + pk.k_scale.numel() * 8) / 1e9)},
+        "roofline": roofline,
+        "kv_read_gbs": round(attn_bytes / (attn_ms / 1e3) / 1e9, 1) if attn_ms else None,
+        "write": write_info,
+        "kernels_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in kern.items()},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(sum(v[1] for v in kern.values())),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, el, _ = time_oracle(w, str(dev), max_seconds=args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                                  "sample": f"{n} (sequence, kv head) units of this batch, each the oracle's "
+                                            f"write of one new token + attention for its {w.group} q heads "
+                                            f"over {w.max_seq_len} keys; {el:.1f} s; 1 unit = 1/{w.num_kv_heads} token"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from int4_token_head_gb300 import synthetic
+    overrides = {"batch": args.batch} if args.batch else {}
+    w = synthetic.make_workload(args.workload, **overrides)
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    v, n, el, _ = time_oracle(w, gen, max_seconds=0, fixed_steps=args.steps, warmup=args.warmup, n_units=4)
+    result = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / n * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q; no dataset or weights)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+                   "global_batch": w.num_seqs, "seq_len": w.max_seq_len, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": f"each step: the oracle's write of one new token + attention for one "
+                                   f"(sequence, kv head) unit ({w.group} q heads over {w.max_seq_len} keys), "
+                                   f"cycling over 4 units; 1 unit = 1/{w.num_kv_heads} token"},
+        "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="long")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch size (reduced-size cases)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -172,6 +172,26 @@ KVINT4_API int kv_int4_attention(const void* q, int64_t q_token_stride,
                       void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
 
+/*
+ * Kernel timing for benchmarks (off by default, per host thread; not part of
+ * the method).  While enabled on the calling thread, every kv_int4_write and
+ * kv_int4_attention call records a pair of CUDA events on its stream around
+ * each of its kernels.  kv_int4_timing_collect waits for the recorded events
+ * and writes, per kernel kind, the summed device time in ms, the number of
+ * timed launches and the number of launches that could not be timed (more
+ * than 4096 pending, or an event error); then it clears the record.  Arrays
+ * have KV_INT4_TIMED_KINDS entries, in the order KV_INT4_TIMED_*.  Any
+ * pointer may be NULL.  Returns KV_INT4_ERR_CUDA if an event query failed.
+ */
+#define KV_INT4_TIMED_KINDS 5
+#define KV_INT4_TIMED_WRITE 0    /* the write kernel */
+#define KV_INT4_TIMED_PREP 1     /* attention: schedule + query rotation */
+#define KV_INT4_TIMED_PREFILL 2  /* attention: prefill tiles */
+#define KV_INT4_TIMED_DECODE 3   /* attention: split-KV decode */
+#define KV_INT4_TIMED_REDUCE 4   /* attention: split merge + inverse rotation */
+KVINT4_API int kv_int4_timing_enable(int enable);
+KVINT4_API int kv_int4_timing_collect(double* ms, int* launches, int* dropped);
+
 /* kv_int4_status_string -- a static, human-readable name for a KV_INT4_* code. */
 KVINT4_API const char* kv_int4_status_string(int status);
 

@@ -34,6 +34,8 @@ _SIGNATURES = {
                                   c_int, c_float, c_int, c_void_p, c_void_p, c_int64, c_void_p, c_size_t,
                                   c_void_p, c_void_p]),
     "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
+    "kv_int4_timing_enable": (c_int, [c_int]),
+    "kv_int4_timing_collect": (c_int, [c_void_p, c_void_p, c_void_p]),
     "kv_int4_version": (c_int, []),
 }
 
@@ -134,6 +136,24 @@ def write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, signs,
                                  _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                  nb, bs, hkv, d, _ptr(signs), _ptr(dev_status), _stream(stream))
         _raise(code, "kv_int4_write")
+
+
+TIMED_KINDS = ("write", "prep", "prefill", "decode", "reduce")
+
+
+def timing_enable(enable: bool = True):
+    """Record CUDA events around every kernel the library launches from this thread."""
+    load().kv_int4_timing_enable(int(bool(enable)))
+
+
+def timing_collect():
+    """{kind: (total_ms, launches, dropped)} since the last collect (waits for the events)."""
+    n = len(TIMED_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    drop = (ctypes.c_int * n)()
+    _raise(load().kv_int4_timing_collect(ms, cnt, drop), "kv_int4_timing_collect")
+    return {k: (ms[i], cnt[i], drop[i]) for i, k in enumerate(TIMED_KINDS)}
 
 
 def attention_workspace_size(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_size) -> int:

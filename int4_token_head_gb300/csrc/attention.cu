@@ -974,7 +974,9 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     const long long rows = (long long)a.num_q_tokens * a.num_q_heads;
     const long long grid = 1 + (rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta;
     if (grid > 0x7fffffff) return KV_INT4_ERR_SIZE;
+    timing_begin(kTimedPrep, stream);
     prep_kernel<D><<<(unsigned)grid, kPrepThreads, 0, stream>>>(c, pv);
+    timing_end(kTimedPrep, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   // 2. prefill
@@ -988,7 +990,9 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     long long grid = (long long)sms * occ;
     if (grid > L.max_prefill_items) grid = L.max_prefill_items;
     if (grid < 1) grid = 1;
+    timing_begin(kTimedPrefill, stream);
     prefill_kernel<D><<<(unsigned)grid, G::THREADS, G::SMEM, stream>>>(PreParams{c, pv});
+    timing_end(kTimedPrefill, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   // 3. decode + 4. reduce
@@ -1001,11 +1005,15 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     long long grid = (long long)sms * occ;
     if (grid * G::WARPS > kMaxDecodeWarps) grid = kMaxDecodeWarps / G::WARPS;
     const int total_warps = (int)grid * G::WARPS;
+    timing_begin(kTimedDecode, stream);
     decode_kernel<D><<<(unsigned)grid, G::WARPS * 32, G::SMEM, stream>>>(DecParams{c, pv, total_warps});
+    timing_end(kTimedDecode, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
     const long long rgrid = (long long)a.num_seqs * a.num_kv_heads;
     if (rgrid > 0x7fffffff) return KV_INT4_ERR_SIZE;
+    timing_begin(kTimedReduce, stream);
     reduce_kernel<D><<<(unsigned)rgrid, kDecodeCols * 32, 0, stream>>>(RedParams{c, pv, total_warps});
+    timing_end(kTimedReduce, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   return KV_INT4_OK;

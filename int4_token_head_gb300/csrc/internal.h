@@ -90,4 +90,10 @@ bool workspace_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_k
 
 int launch_attention(const AttnArgs& a, cudaStream_t stream);
 
+// opt-in kernel timing (timing.cu); kinds match the order documented in kvint4.h
+enum TimedKind { kTimedWrite = 0, kTimedPrep = 1, kTimedPrefill = 2, kTimedDecode = 3, kTimedReduce = 4 };
+constexpr int kTimedKinds = 5;
+void timing_begin(TimedKind kind, cudaStream_t stream);
+void timing_end(TimedKind kind, cudaStream_t stream);
+
 }  // namespace kvint4

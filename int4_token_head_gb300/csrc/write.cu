@@ -288,11 +288,13 @@ static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
   const int64_t tiles = (units + G::UT - 1) / G::UT;
   const int64_t cap = (int64_t)sm_count(dev) * occ[dev];
   const int grid = (int)(tiles < cap ? tiles : cap);
+  timing_begin(kTimedWrite, stream);
   write_kernel<D, PREROT><<<grid, G::NT, G::SMEM, stream>>>(
       static_cast<const uint16_t*>(a.k), a.k_stride, static_cast<const uint16_t*>(a.v), a.v_stride,
       a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale,
       (int64_t)a.num_blocks * a.block_size, a.num_kv_heads, FastDiv(2u * a.num_kv_heads), a.signs,
       a.dev_status);
+  timing_end(kTimedWrite, stream);
   return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
 }
 
