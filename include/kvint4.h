@@ -55,6 +55,8 @@ extern "C" {
 #define KV_INT4_ERR_WORKSPACE 6     /* workspace NULL or smaller than kv_int4_attention_workspace_size() */
 #define KV_INT4_ERR_SIZE 7          /* a negative count, or a size that overflows the index types */
 #define KV_INT4_ERR_CUDA 8          /* a CUDA call or kernel launch failed */
+#define KV_INT4_ERR_SCRATCH_LIMIT 9 /* kv_int4_attention_noalloc: the call needs more workspace than
+                                       KV_INT4_NOALLOC_SCRATCH_BYTES */
 
 /* device-side status bits (ORed into *dev_status) */
 #define KV_INT4_DEV_BAD_SLOT 1      /* slot_mapping entry >= num_blocks * block_size */
@@ -171,6 +173,47 @@ KVINT4_API int kv_int4_attention(const void* q, int64_t q_token_stride,
                       const int8_t* signs, void* out, int64_t out_token_stride,
                       void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
+
+/*
+ * kv_int4_attention_noalloc -- kv_int4_attention without a caller-provided
+ * workspace, for callers that cannot allocate device memory.  (The method's
+ * pages have no counterpart of this entry point: it only changes where the
+ * workspace lives.)
+ *
+ * Who needs it: code that runs inside a host framework or plugin that owns
+ * all device allocations and hands it none, and pipelines whose buffers are
+ * all sized up front and that must not call cudaMalloc in their steady state
+ * (an allocation can synchronise the device, or fail under memory pressure).
+ *
+ * Arguments, layouts, results and errors are those of kv_int4_attention,
+ * minus workspace and workspace_bytes.  The workspace is instead a static
+ * device array of KV_INT4_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which
+ * loads the library holds until the process exits.  A call whose
+ * kv_int4_attention_workspace_size(...) exceeds that returns
+ * KV_INT4_ERR_SCRATCH_LIMIT and enqueues nothing.  The function allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library call).
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address and keeps it; that call may load the library's device code
+ * on the device, so make it before any stream capture begins.
+ *
+ * All calls on a device share the one array, which keeps the last call's
+ * contents; nothing in it needs clearing (each call rewrites what it reads).
+ * Calls whose work overlaps on the GPU -- different streams, or host threads
+ * without ordering -- race on the array and give wrong results: order them,
+ * e.g. by issuing them on one stream.
+ */
+#define KV_INT4_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+KVINT4_API int kv_int4_attention_noalloc(const void* q, int64_t q_token_stride,
+                                         const uint8_t* k_cache, const uint8_t* v_cache,
+                                         const float* k_scale_cache, const float* v_scale_cache,
+                                         const int32_t* block_table, int max_blocks_per_seq,
+                                         const int32_t* seq_lens, const int32_t* query_start_loc,
+                                         int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len,
+                                         int num_q_heads, int num_kv_heads, int head_size,
+                                         int block_size, int num_blocks, float softmax_scale, int causal,
+                                         const int8_t* signs, void* out, int64_t out_token_stride,
+                                         int32_t* dev_status, void* stream);
 
 /*
  * Kernel timing for benchmarks (off by default, per host thread; not part of

@@ -33,6 +33,10 @@ _SIGNATURES = {
                                   c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                   c_int, c_float, c_int, c_void_p, c_void_p, c_int64, c_void_p, c_size_t,
                                   c_void_p, c_void_p]),
+    "kv_int4_attention_noalloc": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                          c_int, c_int, c_int, c_float, c_int, c_void_p, c_void_p, c_int64,
+                                          c_void_p, c_void_p]),
     "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
     "kv_int4_timing_enable": (c_int, [c_int]),
     "kv_int4_timing_collect": (c_int, [c_void_p, c_void_p, c_void_p]),
@@ -40,6 +44,8 @@ _SIGNATURES = {
 }
 
 OK = 0
+ERR_SCRATCH_LIMIT = 9
+NOALLOC_SCRATCH_BYTES = 64 << 20
 DEV_BAD_SLOT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SIGNS = 1, 2, 4, 8
 
 
@@ -185,3 +191,36 @@ def attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, quer
                                  float(softmax_scale), int(bool(causal)), _ptr(signs), _ptr(out), os_,
                                  _ptr(workspace), int(workspace.numel()), _ptr(dev_status), _stream(stream))
     _raise(code, "kv_int4_attention")
+
+
+def attention_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, query_start_loc,
+                      max_query_len, max_seq_len, softmax_scale, causal, signs, out,
+                      dev_status: Optional[torch.Tensor] = None, stream=None):
+    """kv_int4_attention_noalloc: attention whose workspace is the library's
+    static device scratch (for callers that cannot allocate device memory).
+
+    Same arguments as attention() without ``workspace``.  Calls that overlap
+    on the GPU share the scratch and race; issue them in order (one stream).
+    Raises KvInt4Error(ERR_SCRATCH_LIMIT) when the sizes need more workspace
+    than NOALLOC_SCRATCH_BYTES.
+    """
+    nb, bs, hkv, d = _cache_dims(k_cache, v_cache, k_scale, v_scale)
+    _check(q.dim() == 3 and q.shape[2] == d, "q must be [tokens, q_heads, d]")
+    hq = q.shape[1]
+    qs = _token_major(q, "q", hq, d)
+    os_ = _token_major(out, "out", hq, d)
+    _check(out.shape[0] == q.shape[0], "out must match q")
+    _check(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous(),
+           "block_table must be contiguous int32 [seqs, max_blocks]")
+    _check(seq_lens.dtype == torch.int32 and query_start_loc.dtype == torch.int32, "seq_lens/query_start_loc int32")
+    num_seqs = seq_lens.shape[0]
+    _check(query_start_loc.shape[0] == num_seqs + 1 and block_table.shape[0] == num_seqs, "metadata shapes")
+    _check(signs.dtype == torch.int8 and signs.numel() == d, "signs must be int8 [d]")
+    lib = load()
+    code = lib.kv_int4_attention_noalloc(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                         _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+                                         _ptr(query_start_loc), int(num_seqs), int(q.shape[0]), int(max_query_len),
+                                         int(max_seq_len), int(hq), int(hkv), int(d), int(bs), int(nb),
+                                         float(softmax_scale), int(bool(causal)), _ptr(signs), _ptr(out), os_,
+                                         _ptr(dev_status), _stream(stream))
+    _raise(code, "kv_int4_attention_noalloc")

@@ -83,6 +83,9 @@ const char* kv_int4_status_string(int status) {
     case KV_INT4_ERR_WORKSPACE: return "workspace is NULL or smaller than kv_int4_attention_workspace_size()";
     case KV_INT4_ERR_SIZE: return "a count is negative or a size overflows the index types";
     case KV_INT4_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case KV_INT4_ERR_SCRATCH_LIMIT:
+      return "the call needs more workspace than the static no-allocation scratch holds "
+             "(KV_INT4_NOALLOC_SCRATCH_BYTES); use kv_int4_attention with a caller workspace";
     default: return "unknown status";
   }
 }
