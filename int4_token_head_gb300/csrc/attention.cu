@@ -90,6 +90,8 @@ struct Common {
   int64_t out_stride;
   int32_t* status;
   int tile_tokens;  // prefill: query tokens per 64-row tile
+  int hg;           // decode: kv heads per CTA (largest divisor of hkv <= 8)
+  int ng;           // decode: head groups per sequence (hkv / hg)
   long long max_items;  // capacity of the prefill item list
 };
 
@@ -229,20 +231,26 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
 // ---------------------------------------------------------------------------
 template <int D>
 struct DecGeom {
-  static constexpr int WARPS = 8;
   static constexpr int STAGES = 4;
-  static constexpr int TILE = 16 * D / 2;              // bytes of one 16-key code tile
-  static constexpr int STAGE = 2 * TILE + 2 * 16 * 4;  // K codes, V codes, K scales, V scales
-  static constexpr int WARP_SMEM = STAGES * STAGE + 16;
-  static constexpr int SMEM = WARPS * WARP_SMEM;
-  static constexpr int KW = D / 32;   // K words per row per thread (quarter row)
-  static constexpr int VB = D / 16;   // V bytes per row per thread (eighth row)
+  static constexpr int KROW = D / 2;        // K tile row stride (bytes)
+  static constexpr int VROW = D / 2 + 16;   // V tile row stride, padded: conflict-free V fragment loads
+  static constexpr int KTILE = 16 * KROW;
+  static constexpr int VTILE = 16 * VROW;
+  static constexpr int HTILE = KTILE + VTILE;  // one head's K and V codes of one block
+  static constexpr int KW = D / 32;     // K words per row per thread (quarter row)
+  static constexpr int VB = D / 16;     // V bytes per row per thread (eighth row)
   static constexpr int KSTEPS = D / 16;
+  static constexpr int CHR = D / 32;    // 16-byte chunks per code row
+  // per stage: hg head tiles, then scales [K/V][hg][16]
+  __host__ __device__ static constexpr int stage_bytes(int hg) { return hg * (HTILE + 128); }
+  __host__ __device__ static constexpr int smem_bytes(int hg) { return STAGES * stage_bytes(hg) + 16; }
+  static_assert(HTILE % 16 == 0, "tile alignment");
 };
 
+// Walk over the decode positions (sequence i, head group grp, block kb).
 struct DecWalk {
   int i;      // index into the decode-sequence list
-  int h;      // kv head
+  int grp;    // head group
   int kb;     // block within the sequence
   int nblk;   // blocks of the sequence
   int seq;    // sequence id
@@ -252,13 +260,13 @@ __device__ __forceinline__ void walk_load(DecWalk& w, const Common& c, const Pla
   w.seq = pv.dseq[w.i];
   w.nblk = (c.seq_lens[w.seq] + 15) / 16;
 }
-__device__ __forceinline__ void walk_next(DecWalk& w, const Common& c, const PlanView& pv, bool reload) {
+__device__ __forceinline__ void walk_next(DecWalk& w, const Common& c, const PlanView& pv) {
   if (++w.kb == w.nblk) {
     w.kb = 0;
-    if (++w.h == c.hkv) {
-      w.h = 0;
+    if (++w.grp == c.ng) {
+      w.grp = 0;
       ++w.i;
-      if (reload) walk_load(w, c, pv);
+      walk_load(w, c, pv);
     }
   }
 }
@@ -284,7 +292,8 @@ __device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint8_t* p) {
   }
 }
 
-// f16x2 (key a, key b) pairs for the thread's D/8 head dimensions
+// f16x2 (key a, key b) pairs for the thread's D/8 head dimensions: even local
+// offsets hold 1024 + u (u = c + 8), odd ones 1024 + 16u.
 template <int D>
 __device__ __forceinline__ void v_pairs(uint32_t (&P)[D / 8], const uint8_t* ra, const uint8_t* rb) {
   constexpr int VB = D / 16;
@@ -294,13 +303,17 @@ __device__ __forceinline__ void v_pairs(uint32_t (&P)[D / 8], const uint8_t* ra,
     lds_words<VB / 4, VB>(wb, rb);
 #pragma unroll
     for (int k = 0; k < VB / 4; k++) {
-      const uint32_t xx = __byte_perm(wa[k], wb[k], 0x5410);
-      const uint32_t yy = __byte_perm(wa[k], wb[k], 0x7632);
-#pragma unroll
-      for (int t = 0; t < 4; t++) {
-        P[8 * k + t] = nib_to_f16x2(xx >> (4 * t));
-        P[8 * k + 4 + t] = nib_to_f16x2(yy >> (4 * t));
-      }
+      const uint32_t xx = __byte_perm(wa[k], wb[k], 0x5410);  // a.b0 a.b1 b.b0 b.b1
+      const uint32_t yy = __byte_perm(wa[k], wb[k], 0x7632);  // a.b2 a.b3 b.b2 b.b3
+      const uint32_t x8 = xx >> 8, y8 = yy >> 8;
+      P[8 * k + 0] = nib_lo(xx);
+      P[8 * k + 1] = nib_hi(xx);
+      P[8 * k + 2] = nib_lo(x8);
+      P[8 * k + 3] = nib_hi(x8);
+      P[8 * k + 4] = nib_lo(yy);
+      P[8 * k + 5] = nib_hi(yy);
+      P[8 * k + 6] = nib_lo(y8);
+      P[8 * k + 7] = nib_hi(y8);
     }
   } else {
     static_assert(VB % 2 == 0, "V bytes per thread must be even");
@@ -309,8 +322,11 @@ __device__ __forceinline__ void v_pairs(uint32_t (&P)[D / 8], const uint8_t* ra,
       const uint32_t ha = reinterpret_cast<const uint16_t*>(ra)[k];
       const uint32_t hb = reinterpret_cast<const uint16_t*>(rb)[k];
       const uint32_t xx = __byte_perm(ha, hb, 0x5410);
-#pragma unroll
-      for (int t = 0; t < 4; t++) P[4 * k + t] = nib_to_f16x2(xx >> (4 * t));
+      const uint32_t x8 = xx >> 8;
+      P[4 * k + 0] = nib_lo(xx);
+      P[4 * k + 1] = nib_hi(xx);
+      P[4 * k + 2] = nib_lo(x8);
+      P[4 * k + 3] = nib_hi(x8);
     }
   }
 }
@@ -318,35 +334,55 @@ __device__ __forceinline__ void v_pairs(uint32_t (&P)[D / 8], const uint8_t* ra,
 struct DecParams {
   Common c;
   PlanView pv;
-  int total_warps;
+  int num_ctas;
 };
 
+// Work decomposition: stream-K over the flattened (decode sequence, head
+// group, 16-key block) positions; CTA r takes positions
+// [Tb*r/R, Tb*(r+1)/R).  A CTA has one warp per kv head of the group; for
+// every position all its threads copy the block's codes and scales of the
+// group's heads -- contiguous runs of the cache -- into per-head padded tiles,
+// and each warp then computes its own head.  Every (segment, head) piece of
+// a CTA's range writes (o', m, l): to the sequence's direct slot if the
+// piece starts the segment, else to the CTA's slot.
+//
+// Score arithmetic.  A K fragment holds 1032 + c at the low-nibble positions
+// and 1152 + 16c at the high-nibble ones; the q' fragment carries 16 q' at the
+// low positions and q' at the high ones, so the MMA yields
+//   acc = 16 (q' . c) + bias,  bias = sum_low 16 q' * 1032 + sum_high q' * 1152,
+// and bias is itself one MMA of a constant A fragment against q' per segment.
+// The V side works the same way: even head dimensions accumulate
+// p'(1032 + c), odd ones p'(1152 + 16c); right after each block's MMA a
+// second MMA of a constant (-1032 / -1152) A fragment against the same P'^T
+// removes that block's offset, so the running accumulator only ever holds
+// one block's worth of offset (accumulating the offset over thousands of keys
+// would cost the fp32 accumulator the signal's low bits).
 template <int D>
-__global__ void __launch_bounds__(DecGeom<D>::WARPS * 32) decode_kernel(DecParams prm) {
+__global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   using G = DecGeom<D>;
   const Common& c = prm.c;
   const PlanView& pv = prm.pv;
   extern __shared__ __align__(16) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int HG = c.hg;
+  const int tid = threadIdx.x, nthr = HG * 32;
+  const int hl = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
-  uint8_t* wsm = smem + warp * G::WARP_SMEM;
-  int* sflag = reinterpret_cast<int*>(wsm + G::STAGES * G::STAGE);
+  const int SB = G::stage_bytes(HG);
+  int* sflag = reinterpret_cast<int*>(smem + G::STAGES * SB);
 
   const int n_dseq = pv.plan[0];
   if (n_dseq == 0) return;
-  const long long per_head = pv.dprefix[n_dseq];
-  const long long Tb = per_head * c.hkv;
-  const int W = prm.total_warps;
-  const int wid = blockIdx.x * G::WARPS + warp;
-  const long long P0 = Tb * wid / W, P1 = Tb * (wid + 1) / W;
+  const long long Tb = pv.dprefix[n_dseq] * c.ng;
+  const int R = prm.num_ctas;
+  const long long P0 = Tb * blockIdx.x / R, P1 = Tb * (blockIdx.x + 1) / R;
   if (P0 >= P1) return;
 
-  // locate P0: largest i with dprefix[i] * hkv <= P0 (32-ary search)
+  // locate P0: largest i with dprefix[i] * ng <= P0 (32-ary search, per warp)
   int lo = 0, hi = n_dseq;  // invariant: key(lo) <= P0 < key(hi)
   while (hi - lo > 1) {
     const long long span = hi - lo;
     const int probe = lo + (int)((span * lane) / 32);
-    const bool le = lane == 0 || pv.dprefix[probe] * c.hkv <= P0;
+    const bool le = lane == 0 || pv.dprefix[probe] * c.ng <= P0;
     const unsigned m = __ballot_sync(0xffffffffu, le);
     const int last = 31 - __clz(m);
     const int nlo = lo + (int)((span * last) / 32);
@@ -358,73 +394,106 @@ __global__ void __launch_bounds__(DecGeom<D>::WARPS * 32) decode_kernel(DecParam
   cw.i = lo;
   walk_load(cw, c, pv);
   {
-    const long long off = P0 - pv.dprefix[cw.i] * c.hkv;
-    cw.h = (int)(off / cw.nblk);
-    cw.kb = (int)(off - (long long)cw.h * cw.nblk);
+    const long long off = P0 - pv.dprefix[cw.i] * c.ng;
+    cw.grp = (int)(off / cw.nblk);
+    cw.kb = (int)(off - (long long)cw.grp * cw.nblk);
   }
   DecWalk pw = cw;
 
-  auto issue = [&](const DecWalk& w, int stage) {
-    uint8_t* st = wsm + stage * G::STAGE;
-    const int blk = c.block_table[(long long)w.seq * c.max_blocks + w.kb];
+  // thread-constant parts of the staging addresses: CHR chunks per thread
+  int c_soff[G::CHR];
+  long long c_goff[G::CHR];
+  bool c_isv[G::CHR];
+#pragma unroll
+  for (int j = 0; j < G::CHR; j++) {
+    const int idx = tid + nthr * j;  // ((kv * 16 + r) * HG + h) * CHR + col
+    const int col = idx % G::CHR;
+    const int rest = idx / G::CHR;
+    const int h = rest % HG;
+    const int kvr = rest / HG;
+    const int kv = kvr / 16, r = kvr % 16;
+    c_isv[j] = kv != 0;
+    c_soff[j] = h * G::HTILE + (kv ? G::KTILE + r * G::VROW : r * G::KROW) + col * 16;
+    c_goff[j] = ((long long)r * c.hkv + h) * (D / 2) + col * 16;
+  }
+  // one 4-byte scale per thread: [K/V][row][h]
+  const int s_kv = tid / (16 * HG), s_rem = tid % (16 * HG);
+  const int s_r = s_rem / HG, s_h = s_rem % HG;
+  const int s_soff = HG * G::HTILE + (s_kv * HG + s_h) * 64 + s_r * 4;
+  const float* s_src = s_kv ? c.v_scale : c.k_scale;
+  const long long blk_bytes = 16ll * c.hkv * (D / 2);
+
+  auto block_id = [&](const DecWalk& w) { return c.block_table[(long long)w.seq * c.max_blocks + w.kb]; };
+  auto issue = [&](const DecWalk& w, int blk, int stage) {
+    uint8_t* st = smem + stage * SB;
     const bool ok = blk >= 0 && blk < c.num_blocks;
-    if (!ok) {
-      if (lane == 0) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
-    } else {
-      const long long row0 = (long long)blk * 16;
-      for (int q = lane; q < D / 2; q += 32) {
-        const int r = q / (D / 32), col = q - r * (D / 32);
-        const long long goff = ((row0 + r) * c.hkv + w.h) * (D / 2) + col * 16;
-        cp_async16(st + r * (D / 2) + col * 16, c.k_cache + goff);
-        cp_async16(st + G::TILE + r * (D / 2) + col * 16, c.v_cache + goff);
-      }
-      const int r = lane & 15;
-      const long long soff = (row0 + r) * c.hkv + w.h;
-      if (lane < 16) cp_async4(st + 2 * G::TILE + r * 4, c.k_scale + soff);
-      else cp_async4(st + 2 * G::TILE + 64 + r * 4, c.v_scale + soff);
+    if (ok) {
+      const long long h0 = (long long)w.grp * HG;
+      const long long base = (long long)blk * blk_bytes + h0 * (D / 2);
+#pragma unroll
+      for (int j = 0; j < G::CHR; j++)
+        cp_async16(st + c_soff[j], (c_isv[j] ? c.v_cache : c.k_cache) + base + c_goff[j]);
+      cp_async4(st + s_soff, s_src + ((long long)blk * 16 + s_r) * c.hkv + h0 + s_h);
     }
-    if (lane == 0) sflag[stage] = ok;
+    if (tid == 0) {
+      sflag[stage] = ok;
+      if (!ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
+    }
   };
 
+  // producer: issue block ppos, prefetching the next block id one step ahead
   long long ppos = P0;
+  int pblk = block_id(pw);
 #pragma unroll 1
   for (int s = 0; s < G::STAGES - 1; s++) {
     if (ppos < P1) {
-      issue(pw, s);
-      ppos++;
-      if (ppos < P1) walk_next(pw, c, pv, true);
+      issue(pw, pblk, s);
+      if (++ppos < P1) {
+        walk_next(pw, c, pv);
+        pblk = block_id(pw);
+      }
     }
     cp_async_commit();
   }
 
-  // per-segment state
+  // per-segment state of this warp's head
   uint32_t qb[G::KSTEPS][2];
   float oacc[G::KSTEPS][4];
-  float m0, m1, l0, l1;
+  float m0, m1, l0, l1, bias0, bias1;
   int lim0, lim1;  // keys visible to columns 2cq, 2cq+1
-  int L = 0;
   bool first_piece = cw.kb == 0;
 
   auto begin_segment = [&]() {
     const int seq = cw.seq;
+    const int head = cw.grp * HG + hl;
     const int q0 = c.qsl[seq];
     const int ql = c.qsl[seq + 1] - q0;
-    L = c.seq_lens[seq];
+    const int L = c.seq_lens[seq];
     const int ctx = L - ql;
     // B fragments of this lane's column n = g
     const int n = g;
     const bool colok = n < ql * c.group;
     const int j = n / c.group, jj = n - j * c.group;
-    const __half* qrow = pv.qrot + ((long long)(q0 + (colok ? j : 0)) * c.hq + cw.h * c.group + (colok ? jj : 0)) * D;
+    const __half* qrow = pv.qrot + ((long long)(q0 + (colok ? j : 0)) * c.hq + head * c.group + (colok ? jj : 0)) * D;
+    const __half2 x16 = __float2half2_rn(16.f);
 #pragma unroll
     for (int w = 0; w < G::KW; w++) {
       uint4 v = make_uint4(0, 0, 0, 0);
       if (colok) v = *reinterpret_cast<const uint4*>(qrow + 8 * (cq * G::KW + w));
-      qb[2 * w][0] = __byte_perm(v.x, v.z, 0x5410);
+      uint32_t lo0 = __byte_perm(v.x, v.z, 0x5410), lo1 = __byte_perm(v.y, v.w, 0x5410);
+      __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&lo0), x16);
+      __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&lo1), x16);
+      qb[2 * w][0] = *reinterpret_cast<uint32_t*>(&h0);
       qb[2 * w][1] = __byte_perm(v.x, v.z, 0x7632);
-      qb[2 * w + 1][0] = __byte_perm(v.y, v.w, 0x5410);
+      qb[2 * w + 1][0] = *reinterpret_cast<uint32_t*>(&h1);
       qb[2 * w + 1][1] = __byte_perm(v.y, v.w, 0x7632);
     }
+    float bacc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t abias[4] = {kF16x2_1032, kF16x2_1032, kF16x2_1152, kF16x2_1152};
+#pragma unroll
+    for (int s = 0; s < G::KSTEPS; s++) mma_16816(bacc, abias, qb[s][0], qb[s][1]);
+    bias0 = bacc[0];
+    bias1 = bacc[1];
     const int col0 = 2 * cq, col1 = 2 * cq + 1;
     const int j0 = min(col0 / c.group, max(ql - 1, 0)), j1 = min(col1 / c.group, max(ql - 1, 0));
     lim0 = c.causal ? min(L, ctx + j0 + 1) : L;
@@ -445,20 +514,23 @@ __global__ void __launch_bounds__(DecGeom<D>::WARPS * 32) decode_kernel(DecParam
     float* dst_o;
     float* dst_ml;
     if (first_piece) {
-      const long long slot = (long long)cw.i * c.hkv + cw.h;
+      const long long slot = (long long)cw.i * c.hkv + cw.grp * HG + hl;
       dst_o = pv.direct_o + slot * kDecodeCols * D;
       dst_ml = pv.direct_ml + slot * kDecodeCols * 2;
     } else {
-      dst_o = pv.warp_o + (long long)wid * kDecodeCols * D;
-      dst_ml = pv.warp_ml + (long long)wid * kDecodeCols * 2;
+      const long long slot = (long long)blockIdx.x * HG + hl;
+      dst_o = pv.warp_o + slot * kDecodeCols * D;
+      dst_ml = pv.warp_ml + slot * kDecodeCols * 2;
     }
-    // thread holds d = g*D/8 + r (r = 2i + {0,1}) for columns 2cq, 2cq+1
+    // thread holds d = g*D/8 + r (r = 2i, and r = 2i+1 scaled by 16)
     float* o0 = dst_o + (2 * cq) * D + g * (D / 8);
     float* o1 = dst_o + (2 * cq + 1) * D + g * (D / 8);
 #pragma unroll
     for (int i = 0; i < G::KSTEPS; i += 2) {
-      *reinterpret_cast<float4*>(o0 + 2 * i) = make_float4(oacc[i][0], oacc[i][2], oacc[i + 1][0], oacc[i + 1][2]);
-      *reinterpret_cast<float4*>(o1 + 2 * i) = make_float4(oacc[i][1], oacc[i][3], oacc[i + 1][1], oacc[i + 1][3]);
+      *reinterpret_cast<float4*>(o0 + 2 * i) =
+          make_float4(oacc[i][0], oacc[i][2] * 0.0625f, oacc[i + 1][0], oacc[i + 1][2] * 0.0625f);
+      *reinterpret_cast<float4*>(o1 + 2 * i) =
+          make_float4(oacc[i][1], oacc[i][3] * 0.0625f, oacc[i + 1][1], oacc[i + 1][3] * 0.0625f);
     }
     if (g == 0) {
       dst_ml[(2 * cq) * 2 + 0] = m0;
@@ -471,49 +543,50 @@ __global__ void __launch_bounds__(DecGeom<D>::WARPS * 32) decode_kernel(DecParam
   begin_segment();
   int stage = 0;
   const long long nblocks = P1 - P0;
+  // rows g (even d: offset 1032) and g + 8 (odd d: offset 1152)
+  const uint32_t vcorr[4] = {kF16x2_M1032, kF16x2_M1152, kF16x2_M1032, kF16x2_M1152};
 #pragma unroll 1
   for (long long it = 0; it < nblocks; it++) {
+    cp_async_wait<G::STAGES - 2>();
+    __syncthreads();  // this block's copies visible; every warp done with the previous stage
     if (ppos < P1) {
-      issue(pw, (stage + G::STAGES - 1) % G::STAGES);
-      ppos++;
-      if (ppos < P1) walk_next(pw, c, pv, true);
+      issue(pw, pblk, (stage + G::STAGES - 1) % G::STAGES);
+      if (++ppos < P1) {
+        walk_next(pw, c, pv);
+        pblk = block_id(pw);
+      }
     }
     cp_async_commit();
-    cp_async_wait<G::STAGES - 1>();
-    __syncwarp();
 
-    const uint8_t* st = wsm + stage * G::STAGE;
+    const uint8_t* stg = smem + stage * SB;
+    const uint8_t* st = stg + hl * G::HTILE;
     const bool bok = sflag[stage] != 0;
-    const float* sks = reinterpret_cast<const float*>(st + 2 * G::TILE);
-    const float* svs = sks + 16;
+    const float* sks = reinterpret_cast<const float*>(stg + HG * G::HTILE + hl * 64);
+    const float* svs = reinterpret_cast<const float*>(stg + HG * G::HTILE + (HG + hl) * 64);
 
-    // ---- S^T = K Q'^T ----
+    // ---- S^T = K Q'^T (biased, x16) ----
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
     {
       uint32_t xk[G::KW], yk[G::KW];
-      lds_words<G::KW, D / 8>(xk, st + g * (D / 2) + cq * (D / 8));
-      lds_words<G::KW, D / 8>(yk, st + (g + 8) * (D / 2) + cq * (D / 8));
+      lds_words<G::KW, D / 8>(xk, st + g * G::KROW + cq * (D / 8));
+      lds_words<G::KW, D / 8>(yk, st + (g + 8) * G::KROW + cq * (D / 8));
 #pragma unroll
       for (int w = 0; w < G::KW; w++) {
-#pragma unroll
-        for (int e = 0; e < 2; e++) {
-          uint32_t a[4];
-          a[0] = nib_to_f16x2(xk[w] >> (8 * e));
-          a[1] = nib_to_f16x2(yk[w] >> (8 * e));
-          a[2] = nib_to_f16x2(xk[w] >> (8 * e + 4));
-          a[3] = nib_to_f16x2(yk[w] >> (8 * e + 4));
-          mma_16816(sacc, a, qb[2 * w + e][0], qb[2 * w + e][1]);
-        }
+        const uint32_t x = xk[w], y = yk[w], x8 = x >> 8, y8 = y >> 8;
+        const uint32_t a0[4] = {nib_lo(x), nib_lo(y), nib_hi(x), nib_hi(y)};
+        mma_16816(sacc, a0, qb[2 * w][0], qb[2 * w][1]);
+        const uint32_t a1[4] = {nib_lo(x8), nib_lo(y8), nib_hi(x8), nib_hi(y8)};
+        mma_16816(sacc, a1, qb[2 * w + 1][0], qb[2 * w + 1][1]);
       }
     }
     const int pos0 = cw.kb * 16 + g, pos1 = pos0 + 8;
     const bool v00 = bok && pos0 < lim0, v01 = bok && pos0 < lim1;
     const bool v10 = bok && pos1 < lim0, v11 = bok && pos1 < lim1;
-    const float ks0 = sks[g], ks1 = sks[g + 8];
-    const float s00 = v00 ? sacc[0] * ks0 : -INFINITY;
-    const float s01 = v01 ? sacc[1] * ks0 : -INFINITY;
-    const float s10 = v10 ? sacc[2] * ks1 : -INFINITY;
-    const float s11 = v11 ? sacc[3] * ks1 : -INFINITY;
+    const float ks0 = sks[g] * 0.0625f, ks1 = sks[g + 8] * 0.0625f;
+    const float s00 = v00 ? (sacc[0] - bias0) * ks0 : -INFINITY;
+    const float s01 = v01 ? (sacc[1] - bias1) * ks0 : -INFINITY;
+    const float s10 = v10 ? (sacc[2] - bias0) * ks1 : -INFINITY;
+    const float s11 = v11 ? (sacc[3] - bias1) * ks1 : -INFINITY;
     float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -534,29 +607,34 @@ __global__ void __launch_bounds__(DecGeom<D>::WARPS * 32) decode_kernel(DecParam
     const uint32_t M1 = pack_f16x2(v10 ? p10 * vs1 : 0.f, v11 ? p11 * vs1 : 0.f);
     const uint32_t b0 = movmatrix_trans(M0), b1 = movmatrix_trans(M1);
 
-    // ---- O'^T += V^T P'^T ----
-    {
-      uint32_t P01[D / 8], P89[D / 8];
-      const uint8_t* sv = st + G::TILE + g * G::VB;
-      v_pairs<D>(P01, sv + (2 * cq) * (D / 2), sv + (2 * cq + 1) * (D / 2));
-      v_pairs<D>(P89, sv + (2 * cq + 8) * (D / 2), sv + (2 * cq + 9) * (D / 2));
+    // ---- O'^T += V^T P'^T (offset removed per block) ----
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
       for (int i = 0; i < G::KSTEPS; i++) {
         oacc[i][0] *= al0;
         oacc[i][1] *= al1;
         oacc[i][2] *= al0;
         oacc[i][3] *= al1;
-        const uint32_t a[4] = {P01[2 * i], P01[2 * i + 1], P89[2 * i], P89[2 * i + 1]};
-        mma_16816(oacc[i], a, b0, b1);
       }
     }
-    __syncwarp();
+    {
+      uint32_t P01[D / 8], P89[D / 8];
+      const uint8_t* sv = st + G::KTILE + g * G::VB;
+      v_pairs<D>(P01, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW);
+      v_pairs<D>(P89, sv + (2 * cq + 8) * G::VROW, sv + (2 * cq + 9) * G::VROW);
+#pragma unroll
+      for (int i = 0; i < G::KSTEPS; i++) {
+        const uint32_t a[4] = {P01[2 * i], P01[2 * i + 1], P89[2 * i], P89[2 * i + 1]};
+        mma_16816(oacc[i], a, b0, b1);
+        mma_16816(oacc[i], vcorr, b0, b1);
+      }
+    }
 
     const bool last_in_seg = cw.kb == cw.nblk - 1;
     const bool last_in_range = it + 1 == nblocks;
     if (last_in_seg || last_in_range) flush();
     if (!last_in_range) {
-      walk_next(cw, c, pv, true);
+      walk_next(cw, c, pv);
       if (last_in_seg) {
         first_piece = true;
         begin_segment();
@@ -573,7 +651,7 @@ __global__ void __launch_bounds__(DecGeom<D>::WARPS * 32) decode_kernel(DecParam
 struct RedParams {
   Common c;
   PlanView pv;
-  int total_warps;
+  int num_ctas;
 };
 
 template <int D>
@@ -591,9 +669,10 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (col >= ql * c.group) return;
   const int nblk = (c.seq_lens[seq] + 15) / 16;
-  const long long Tb = pv.dprefix[n_dseq] * c.hkv;
-  const long long sbeg = pv.dprefix[i] * c.hkv + (long long)h * nblk, send = sbeg + nblk;
-  const int W = prm.total_warps;
+  const int grp = h / c.hg, hl = h - grp * c.hg;
+  const long long Tb = pv.dprefix[n_dseq] * c.ng;
+  const long long sbeg = pv.dprefix[i] * c.ng + (long long)grp * nblk, send = sbeg + nblk;
+  const int W = prm.num_ctas;
   auto wstart = [&](long long w) { return Tb * w / W; };
 
   constexpr int PER = D / 32;
@@ -603,14 +682,15 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   float Lsum = pv.direct_ml[((long long)seg * kDecodeCols + col) * 2 + 1];
 #pragma unroll
   for (int k = 0; k < PER; k++) acc[k] = od[lane + 32 * k];
-  // warps whose (non-empty) range starts strictly inside this segment
+  // CTAs whose (non-empty) range starts strictly inside this segment
   long long w = (sbeg * W) / Tb;
   while (w < W && wstart(w) <= sbeg) w++;
   for (; w < W && wstart(w) < send; w++) {
     if (wstart(w + 1) <= wstart(w)) continue;
-    const float* ow = pv.warp_o + (w * kDecodeCols + col) * D;
-    const float mw = pv.warp_ml[(w * kDecodeCols + col) * 2];
-    const float lw = pv.warp_ml[(w * kDecodeCols + col) * 2 + 1];
+    const long long slot = w * c.hg + hl;
+    const float* ow = pv.warp_o + (slot * kDecodeCols + col) * D;
+    const float mw = pv.warp_ml[(slot * kDecodeCols + col) * 2];
+    const float lw = pv.warp_ml[(slot * kDecodeCols + col) * 2 + 1];
     const float Mn = fmaxf(M, mw);
     const float Mu = Mn == -INFINITY ? 0.f : Mn;
     const float a = fast_exp2(M - Mu), b = fast_exp2(mw - Mu);
@@ -967,6 +1047,13 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.status = a.dev_status;
   c.tile_tokens = kPrefillRows / c.group > 0 ? kPrefillRows / c.group : 1;
   c.max_items = L.max_prefill_items;
+  c.hg = 1;
+  for (int h = 8; h >= 1; h--)
+    if (a.num_kv_heads % h == 0) {
+      c.hg = h;
+      break;
+    }
+  c.ng = a.num_kv_heads / c.hg;
   if (c.group > kPrefillRows) return KV_INT4_ERR_HEADS;
 
   // 1. prep
@@ -998,21 +1085,32 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   // 3. decode + 4. reduce
   if (c.group <= kDecodeCols) {
     using G = DecGeom<D>;
-    static bool done[kMaxDevices] = {};
-    static int occ_c[kMaxDevices] = {};
-    int occ = 0;
-    if (!configure(decode_kernel<D>, G::SMEM, G::WARPS * 32, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
-    long long grid = (long long)sms * occ;
-    if (grid * G::WARPS > kMaxDecodeWarps) grid = kMaxDecodeWarps / G::WARPS;
-    const int total_warps = (int)grid * G::WARPS;
+    static bool attr_done[kMaxDevices] = {};
+    static int occ_cache[kMaxDevices][9] = {};
+    if (!attr_done[dev]) {
+      if (cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::smem_bytes(8)) !=
+          cudaSuccess)
+        return KV_INT4_ERR_CUDA;
+      attr_done[dev] = true;
+    }
+    const int threads = c.hg * 32, smem = G::smem_bytes(c.hg);
+    if (!occ_cache[dev][c.hg]) {
+      int o = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<D>, threads, smem) != cudaSuccess || o < 1)
+        return KV_INT4_ERR_CUDA;
+      occ_cache[dev][c.hg] = o;
+    }
+    long long grid = (long long)sms * occ_cache[dev][c.hg];
+    if (grid * c.hg > kMaxDecodeWarps) grid = kMaxDecodeWarps / c.hg;
+    const int num_ctas = (int)grid;
     timing_begin(kTimedDecode, stream);
-    decode_kernel<D><<<(unsigned)grid, G::WARPS * 32, G::SMEM, stream>>>(DecParams{c, pv, total_warps});
+    decode_kernel<D><<<(unsigned)grid, threads, smem, stream>>>(DecParams{c, pv, num_ctas});
     timing_end(kTimedDecode, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
     const long long rgrid = (long long)a.num_seqs * a.num_kv_heads;
     if (rgrid > 0x7fffffff) return KV_INT4_ERR_SIZE;
     timing_begin(kTimedReduce, stream);
-    reduce_kernel<D><<<(unsigned)rgrid, kDecodeCols * 32, 0, stream>>>(RedParams{c, pv, total_warps});
+    reduce_kernel<D><<<(unsigned)rgrid, kDecodeCols * 32, 0, stream>>>(RedParams{c, pv, num_ctas});
     timing_end(kTimedReduce, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }

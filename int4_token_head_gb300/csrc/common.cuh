@@ -86,6 +86,28 @@ __device__ __forceinline__ uint32_t nib_to_f16x2(uint32_t x) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The same exactness with the bias folded away from the subtraction: the
+// low nibble of a byte (bits [0,4) and [16,20) of x) becomes 1024 + u, and the
+// high nibble (bits [4,8) and [20,24)) becomes 1024 + 16u, one lop3 each.
+// Callers remove the constant offsets (1032 and 1152 per unit of the other
+// operand) and the factor 16 arithmetically.
+__device__ __forceinline__ uint32_t nib_lo(uint32_t x) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(x), "r"(0x000f000fu), "r"(0x64086408u));
+  return r;
+}
+__device__ __forceinline__ uint32_t nib_hi(uint32_t x) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(x), "r"(0x00f000f0u), "r"(0x64806480u));
+  return r;
+}
+constexpr uint32_t kF16x2_1032 = 0x64086408u;  // (1032, 1032)
+constexpr uint32_t kF16x2_1152 = 0x64806480u;  // (1152, 1152)
+constexpr uint32_t kF16x2_ONE = 0x3c003c00u;   // (1, 1)
+constexpr uint32_t kF16x2_M1032 = 0xe408e408u; // (-1032, -1032)
+constexpr uint32_t kF16x2_M1152 = 0xe480e480u; // (-1152, -1152)
+constexpr uint32_t kF16x2_16 = 0x4c004c00u;    // (16, 16)
+
 // ---------------------------------------------------------------------------
 // tensor-core fragments (legacy warp-level MMA, f16 inputs, f32 accumulate)
 // ---------------------------------------------------------------------------
