@@ -61,7 +61,9 @@ def load(path: Optional[str] = None):
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or _build.build()
+        # KVINT4_LIBRARY selects a specific build of the library (for example a
+        # locally modified one); otherwise the in-tree library is built if stale.
+        p = path or os.environ.get("KVINT4_LIBRARY") or _build.build()
         lib = ctypes.CDLL(p)
         for name, (res, args) in _SIGNATURES.items():
             fn = getattr(lib, name)

@@ -236,7 +236,9 @@ struct DecGeom {
   static constexpr int VROW = D / 2 + 16;   // V tile row stride, padded: conflict-free V fragment loads
   static constexpr int KTILE = 16 * KROW;
   static constexpr int VTILE = 16 * VROW;
-  static constexpr int HTILE = KTILE + VTILE;  // one head's K and V codes of one block
+  // one head's K and V codes of one block, padded to 64 mod 128 bytes so that
+  // the copies of neighbouring heads' rows fall in different bank halves
+  static constexpr int HTILE = ((KTILE + VTILE + 63) / 128) * 128 + 64;
   static constexpr int KW = D / 32;     // K words per row per thread (quarter row)
   static constexpr int VB = D / 16;     // V bytes per row per thread (eighth row)
   static constexpr int KSTEPS = D / 16;
@@ -292,41 +294,57 @@ __device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint8_t* p) {
   }
 }
 
-// f16x2 (key a, key b) pairs for the thread's D/8 head dimensions: even local
-// offsets hold 1024 + u (u = c + 8), odd ones 1024 + 16u.
+// O'^T += V^T P'^T for the thread's D/8 head dimensions, one m-tile at a time:
+// each m-tile's A fragment is (keys ka,kb; d even), (ka,kb; d odd),
+// (kc,kd; d even), (kc,kd; d odd), built by one lop3 each from byte-interleaved
+// words of the four key rows, followed by the per-block offset correction.
 template <int D>
-__device__ __forceinline__ void v_pairs(uint32_t (&P)[D / 8], const uint8_t* ra, const uint8_t* rb) {
+__device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], const uint8_t* ra, const uint8_t* rb,
+                                        const uint8_t* rc, const uint8_t* rd, uint32_t b0, uint32_t b1,
+                                        const uint32_t (&vcorr)[4]) {
   constexpr int VB = D / 16;
   if constexpr (VB % 4 == 0) {
-    uint32_t wa[VB / 4], wb[VB / 4];
+    uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
     lds_words<VB / 4, VB>(wa, ra);
     lds_words<VB / 4, VB>(wb, rb);
+    lds_words<VB / 4, VB>(wc, rc);
+    lds_words<VB / 4, VB>(wd, rd);
 #pragma unroll
     for (int k = 0; k < VB / 4; k++) {
-      const uint32_t xx = __byte_perm(wa[k], wb[k], 0x5410);  // a.b0 a.b1 b.b0 b.b1
-      const uint32_t yy = __byte_perm(wa[k], wb[k], 0x7632);  // a.b2 a.b3 b.b2 b.b3
-      const uint32_t x8 = xx >> 8, y8 = yy >> 8;
-      P[8 * k + 0] = nib_lo(xx);
-      P[8 * k + 1] = nib_hi(xx);
-      P[8 * k + 2] = nib_lo(x8);
-      P[8 * k + 3] = nib_hi(x8);
-      P[8 * k + 4] = nib_lo(yy);
-      P[8 * k + 5] = nib_hi(yy);
-      P[8 * k + 6] = nib_lo(y8);
-      P[8 * k + 7] = nib_hi(y8);
+      uint32_t src01[4], src89[4];
+      src01[0] = __byte_perm(wa[k], wb[k], 0x5410);
+      src01[2] = __byte_perm(wa[k], wb[k], 0x7632);
+      src89[0] = __byte_perm(wc[k], wd[k], 0x5410);
+      src89[2] = __byte_perm(wc[k], wd[k], 0x7632);
+      src01[1] = src01[0] >> 8;
+      src01[3] = src01[2] >> 8;
+      src89[1] = src89[0] >> 8;
+      src89[3] = src89[2] >> 8;
+#pragma unroll
+      for (int t = 0; t < 4; t++) {
+        const uint32_t a[4] = {nib_lo(src01[t]), nib_hi(src01[t]), nib_lo(src89[t]), nib_hi(src89[t])};
+        mma_16816(oacc[4 * k + t], a, b0, b1);
+        mma_16816(oacc[4 * k + t], vcorr, b0, b1);
+      }
     }
   } else {
-    static_assert(VB % 2 == 0, "V bytes per thread must be even");
 #pragma unroll
     for (int k = 0; k < VB / 2; k++) {
       const uint32_t ha = reinterpret_cast<const uint16_t*>(ra)[k];
       const uint32_t hb = reinterpret_cast<const uint16_t*>(rb)[k];
-      const uint32_t xx = __byte_perm(ha, hb, 0x5410);
-      const uint32_t x8 = xx >> 8;
-      P[4 * k + 0] = nib_lo(xx);
-      P[4 * k + 1] = nib_hi(xx);
-      P[4 * k + 2] = nib_lo(x8);
-      P[4 * k + 3] = nib_hi(x8);
+      const uint32_t hc = reinterpret_cast<const uint16_t*>(rc)[k];
+      const uint32_t hd = reinterpret_cast<const uint16_t*>(rd)[k];
+      uint32_t src01[2], src89[2];
+      src01[0] = __byte_perm(ha, hb, 0x5410);
+      src89[0] = __byte_perm(hc, hd, 0x5410);
+      src01[1] = src01[0] >> 8;
+      src89[1] = src89[0] >> 8;
+#pragma unroll
+      for (int t = 0; t < 2; t++) {
+        const uint32_t a[4] = {nib_lo(src01[t]), nib_hi(src01[t]), nib_lo(src89[t]), nib_hi(src89[t])};
+        mma_16816(oacc[2 * k + t], a, b0, b1);
+        mma_16816(oacc[2 * k + t], vcorr, b0, b1);
+      }
     }
   }
 }
@@ -401,39 +419,42 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   DecWalk pw = cw;
 
   // thread-constant parts of the staging addresses: CHR chunks per thread
-  int c_soff[G::CHR];
-  long long c_goff[G::CHR];
-  bool c_isv[G::CHR];
+  // (chunk index ((kv * 16 + r) * HG + h) * CHR + col: consecutive threads read
+  // consecutive bytes of the cache)
+  uint32_t c_saddr[G::CHR];      // shared address within stage 0
+  const uint8_t* c_src[G::CHR];  // cache address within block 0, head group 0
 #pragma unroll
   for (int j = 0; j < G::CHR; j++) {
-    const int idx = tid + nthr * j;  // ((kv * 16 + r) * HG + h) * CHR + col
+    const int idx = tid + nthr * j;
     const int col = idx % G::CHR;
     const int rest = idx / G::CHR;
     const int h = rest % HG;
     const int kvr = rest / HG;
     const int kv = kvr / 16, r = kvr % 16;
-    c_isv[j] = kv != 0;
-    c_soff[j] = h * G::HTILE + (kv ? G::KTILE + r * G::VROW : r * G::KROW) + col * 16;
-    c_goff[j] = ((long long)r * c.hkv + h) * (D / 2) + col * 16;
+    c_saddr[j] = smem_addr(smem) + h * G::HTILE + (kv ? G::KTILE + r * G::VROW : r * G::KROW) + col * 16;
+    c_src[j] = (kv ? c.v_cache : c.k_cache) + ((long long)r * c.hkv + h) * (D / 2) + col * 16;
   }
   // one 4-byte scale per thread: [K/V][row][h]
   const int s_kv = tid / (16 * HG), s_rem = tid % (16 * HG);
   const int s_r = s_rem / HG, s_h = s_rem % HG;
-  const int s_soff = HG * G::HTILE + (s_kv * HG + s_h) * 64 + s_r * 4;
-  const float* s_src = s_kv ? c.v_scale : c.k_scale;
-  const long long blk_bytes = 16ll * c.hkv * (D / 2);
+  const uint32_t s_saddr = smem_addr(smem) + HG * G::HTILE + (s_kv * HG + s_h) * 64 + s_r * 4;
+  const float* s_src = (s_kv ? c.v_scale : c.k_scale) + (long long)s_r * c.hkv + s_h;
+  const uint32_t blk_bytes = 16u * c.hkv * (D / 2);  // < 2^32 (host-checked head counts)
+  const uint32_t blk_scales = 16u * c.hkv;
 
   auto block_id = [&](const DecWalk& w) { return c.block_table[(long long)w.seq * c.max_blocks + w.kb]; };
   auto issue = [&](const DecWalk& w, int blk, int stage) {
-    uint8_t* st = smem + stage * SB;
     const bool ok = blk >= 0 && blk < c.num_blocks;
     if (ok) {
-      const long long h0 = (long long)w.grp * HG;
-      const long long base = (long long)blk * blk_bytes + h0 * (D / 2);
+      const uint32_t soff = (uint32_t)(stage * SB);
+      const uint32_t goff = (uint32_t)(w.grp * HG * (D / 2));
 #pragma unroll
-      for (int j = 0; j < G::CHR; j++)
-        cp_async16(st + c_soff[j], (c_isv[j] ? c.v_cache : c.k_cache) + base + c_goff[j]);
-      cp_async4(st + s_soff, s_src + ((long long)blk * 16 + s_r) * c.hkv + h0 + s_h);
+      for (int j = 0; j < G::CHR; j++) {
+        const uint8_t* src = c_src[j] + (uint64_t)(uint32_t)blk * blk_bytes + goff;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(c_saddr[j] + soff), "l"(src));
+      }
+      const float* ssrc = s_src + (uint64_t)(uint32_t)blk * blk_scales + w.grp * HG;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s_saddr + soff), "l"(ssrc));
     }
     if (tid == 0) {
       sflag[stage] = ok;
@@ -461,6 +482,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   float oacc[G::KSTEPS][4];
   float m0, m1, l0, l1, bias0, bias1;
   int lim0, lim1;  // keys visible to columns 2cq, 2cq+1
+  int lim_warp;    // smallest of all columns' limits
   bool first_piece = cw.kb == 0;
 
   auto begin_segment = [&]() {
@@ -498,6 +520,9 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const int j0 = min(col0 / c.group, max(ql - 1, 0)), j1 = min(col1 / c.group, max(ql - 1, 0));
     lim0 = c.causal ? min(L, ctx + j0 + 1) : L;
     lim1 = c.causal ? min(L, ctx + j1 + 1) : L;
+    lim_warp = min(lim0, lim1);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) lim_warp = min(lim_warp, __shfl_xor_sync(0xffffffffu, lim_warp, o));
 #pragma unroll
     for (int i = 0; i < G::KSTEPS; i++) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
     m0 = m1 = -INFINITY;
@@ -542,11 +567,11 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
 
   begin_segment();
   int stage = 0;
-  const long long nblocks = P1 - P0;
+  const int nblocks = (int)(P1 - P0);
   // rows g (even d: offset 1032) and g + 8 (odd d: offset 1152)
   const uint32_t vcorr[4] = {kF16x2_M1032, kF16x2_M1152, kF16x2_M1032, kF16x2_M1152};
 #pragma unroll 1
-  for (long long it = 0; it < nblocks; it++) {
+  for (int it = 0; it < nblocks; it++) {
     cp_async_wait<G::STAGES - 2>();
     __syncthreads();  // this block's copies visible; every warp done with the previous stage
     if (ppos < P1) {
@@ -580,35 +605,35 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
       }
     }
     const int pos0 = cw.kb * 16 + g, pos1 = pos0 + 8;
-    const bool v00 = bok && pos0 < lim0, v01 = bok && pos0 < lim1;
-    const bool v10 = bok && pos1 < lim0, v11 = bok && pos1 < lim1;
     const float ks0 = sks[g] * 0.0625f, ks1 = sks[g + 8] * 0.0625f;
-    const float s00 = v00 ? (sacc[0] - bias0) * ks0 : -INFINITY;
-    const float s01 = v01 ? (sacc[1] - bias1) * ks0 : -INFINITY;
-    const float s10 = v10 ? (sacc[2] - bias0) * ks1 : -INFINITY;
-    const float s11 = v11 ? (sacc[3] - bias1) * ks1 : -INFINITY;
-    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    float s00 = (sacc[0] - bias0) * ks0, s01 = (sacc[1] - bias1) * ks0;
+    float s10 = (sacc[2] - bias0) * ks1, s11 = (sacc[3] - bias1) * ks1;
+    // keys past a column's visible length (or in an invalid block) only occur
+    // in blocks that reach past the warp's smallest limit
+    const bool full = bok && cw.kb * 16 + 16 <= lim_warp;
+    if (!full) {
+      s00 = (bok && pos0 < lim0) ? s00 : -INFINITY;
+      s01 = (bok && pos0 < lim1) ? s01 : -INFINITY;
+      s10 = (bok && pos1 < lim0) ? s10 : -INFINITY;
+      s11 = (bok && pos1 < lim1) ? s11 : -INFINITY;
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
-    const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
-    l0 = l0 * al0 + p00 + p10;
-    l1 = l1 * al1 + p01 + p11;
-    const float vs0 = svs[g], vs1 = svs[g + 8];
-    const uint32_t M0 = pack_f16x2(v00 ? p00 * vs0 : 0.f, v01 ? p01 * vs0 : 0.f);
-    const uint32_t M1 = pack_f16x2(v10 ? p10 * vs1 : 0.f, v11 ? p11 * vs1 : 0.f);
-    const uint32_t b0 = movmatrix_trans(M0), b1 = movmatrix_trans(M1);
-
-    // ---- O'^T += V^T P'^T (offset removed per block) ----
-    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+    // exact running max: reduce across the key lanes only when some lane
+    // holds a score above its column's current max
+    if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // a column with no visible key yet keeps m = -inf (and alpha = 1)
+      const float al0 = mn0 == -INFINITY ? 1.f : fast_exp2(m0 - mn0);
+      const float al1 = mn1 == -INFINITY ? 1.f : fast_exp2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int i = 0; i < G::KSTEPS; i++) {
         oacc[i][0] *= al0;
@@ -617,17 +642,28 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
         oacc[i][3] *= al1;
       }
     }
+    const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+    const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
+    const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
+    l0 += p00 + p10;
+    l1 += p01 + p11;
+    const float vs0 = svs[g], vs1 = svs[g + 8];
+    float q00 = p00 * vs0, q01 = p01 * vs0, q10 = p10 * vs1, q11 = p11 * vs1;
+    if (!full) {  // masked keys may carry unwritten (NaN) scales: select, do not multiply
+      q00 = s00 == -INFINITY ? 0.f : q00;
+      q01 = s01 == -INFINITY ? 0.f : q01;
+      q10 = s10 == -INFINITY ? 0.f : q10;
+      q11 = s11 == -INFINITY ? 0.f : q11;
+    }
+    const uint32_t M0 = pack_f16x2(q00, q01);
+    const uint32_t M1 = pack_f16x2(q10, q11);
+    const uint32_t b0 = movmatrix_trans(M0), b1 = movmatrix_trans(M1);
+
+    // ---- O'^T += V^T P'^T (offset removed per block) ----
     {
-      uint32_t P01[D / 8], P89[D / 8];
       const uint8_t* sv = st + G::KTILE + g * G::VB;
-      v_pairs<D>(P01, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW);
-      v_pairs<D>(P89, sv + (2 * cq + 8) * G::VROW, sv + (2 * cq + 9) * G::VROW);
-#pragma unroll
-      for (int i = 0; i < G::KSTEPS; i++) {
-        const uint32_t a[4] = {P01[2 * i], P01[2 * i + 1], P89[2 * i], P89[2 * i + 1]};
-        mma_16816(oacc[i], a, b0, b1);
-        mma_16816(oacc[i], vcorr, b0, b1);
-      }
+      pv_mmas<D>(oacc, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW, sv + (2 * cq + 8) * G::VROW,
+                 sv + (2 * cq + 9) * G::VROW, b0, b1, vcorr);
     }
 
     const bool last_in_seg = cw.kb == cw.nblk - 1;
