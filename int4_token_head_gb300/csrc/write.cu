@@ -267,6 +267,458 @@ write_kernel(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* _
   cp_async_wait<0>();
 }
 
+// ---------------------------------------------------------------------------
+// Token-aligned variant (used whenever a token's 2*Hkv head vectors fit in one
+// tile): a tile is TT whole tokens, so every thread's copy sources and its
+// compute unit's (token offset, K/V, head) are fixed per thread and only the
+// tile's first token changes.  Sign masks are packed per element pair and the
+// butterflies run on packed fp32 pairs (two IEEE adds per instruction, the
+// same roundings as the scalar form).
+// ---------------------------------------------------------------------------
+template <int D, bool PREROT>
+__global__ void __launch_bounds__(WriteGeom<D>::NT)
+write_kernel_tok(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* __restrict__ v,
+                 int64_t v_stride, const int64_t* __restrict__ slot_mapping, int num_tokens,
+                 uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
+                 float* __restrict__ v_scale, int64_t num_slots, int hkv, int tt_per_tile,
+                 const int8_t* __restrict__ signs, int32_t* status) {
+  using G = WriteGeom<D>;
+  constexpr int B = G::B, SEG = G::SEG, F = G::F, TPV = G::TPV, UT = G::UT, NT = G::NT;
+  constexpr int CPT = (UT * G::CHUNKS) / NT;  // copy chunks per thread per tile
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint2* smask = reinterpret_cast<uint2*>(smem + G::STAGES * G::STAGE_BYTES);  // [D/2] (lo, hi) sign bits
+  uint32_t* samax = reinterpret_cast<uint32_t*>(smask + D / 2);                 // [TPV][UT]
+
+  const int tid = threadIdx.x;
+  const int units_per_token = 2 * hkv;
+  const int units = tt_per_tile * units_per_token;  // <= UT
+  const int num_tiles = (num_tokens + tt_per_tile - 1) / tt_per_tile;
+
+  if (!PREROT) {
+    for (int p = tid; p < D / 2; p += NT) {
+      const int s0 = signs[2 * p], s1 = signs[2 * p + 1];
+      if (blockIdx.x == 0 && ((s0 != 1 && s0 != -1) || (s1 != 1 && s1 != -1))) flag(status, KV_INT4_DEV_BAD_SIGNS);
+      smask[p] = make_uint2(s0 < 0 ? 0x80000000u : 0u, s1 < 0 ? 0x80000000u : 0u);
+    }
+  }
+
+  // copy slots of this thread (tile-invariant): chunk idx = tid + NT * q
+  const uint16_t* c_src[CPT];
+  int c_tok[CPT];    // token offset within the tile, or -1 if unused
+  int64_t c_strd[CPT];
+#pragma unroll
+  for (int q = 0; q < CPT; q++) {
+    const int idx = tid + NT * q;
+    const int uu = idx / G::CHUNKS, c = idx % G::CHUNKS;
+    const int tt = uu / units_per_token, w = uu % units_per_token;
+    const int kv = w >= hkv, h = kv ? w - hkv : w;
+    c_tok[q] = uu < units ? tt : -1;
+    c_src[q] = (kv ? v : k) + (int64_t)tt * (kv ? v_stride : k_stride) + h * D + c * 8;
+    c_strd[q] = (int64_t)tt_per_tile * (kv ? v_stride : k_stride);
+  }
+  auto issue = [&](int tile, int stage) {
+    const uint32_t dst0 = smem_addr(stages + stage * G::STAGE_BYTES);
+    const int t0 = tile * tt_per_tile;
+#pragma unroll
+    for (int q = 0; q < CPT; q++) {
+      const int idx = tid + NT * q;
+      const int uu = idx / G::CHUNKS, c = idx % G::CHUNKS;
+      if (c_tok[q] >= 0 && t0 + c_tok[q] < num_tokens) {
+        const uint16_t* src = c_src[q] + (int64_t)tile * c_strd[q];
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst0 + uu * G::VSTRIDE + c * 16), "l"(src));
+      }
+    }
+  };
+
+  const int j = tid / UT;       // segment index within the vector
+  const int u = tid - j * UT;   // vector index within the tile
+  const int blk = j / F;        // Hadamard block
+  const int jj = j - blk * F;   // row of H_F
+  const int u_tt = u / units_per_token, u_w = u % units_per_token;
+  const int u_kv = u_w >= hkv, u_h = u_kv ? u_w - hkv : u_w;
+  uint8_t* const u_cache = u_kv ? v_cache : k_cache;
+  float* const u_scale = u_kv ? v_scale : k_scale;
+
+  int tile = blockIdx.x;
+  const int tstep = gridDim.x;
+#pragma unroll 1
+  for (int s = 0; s < G::STAGES - 1; s++) {
+    const int tt = tile + s * tstep;
+    if (tt < num_tiles) issue(tt, s);
+    cp_async_commit();
+  }
+  __syncthreads();  // sign masks visible
+
+  int stage = 0;
+#pragma unroll 1
+  for (; tile < num_tiles; tile += tstep) {
+    {
+      const int tn = tile + (G::STAGES - 1) * tstep;
+      if (tn < num_tiles) issue(tn, (stage + G::STAGES - 1) % G::STAGES);
+      cp_async_commit();
+    }
+    cp_async_wait<G::STAGES - 1>();
+    __syncthreads();
+
+    const uint8_t* sv = stages + stage * G::STAGE_BYTES + u * G::VSTRIDE;
+    const int t = tile * tt_per_tile + u_tt;
+    const bool active = u < units && t < num_tokens;
+
+    uint32_t packed[SEG / 2];
+    uint32_t amax = 0;
+    if (active) {
+      if (PREROT) {
+        const uint4* src = reinterpret_cast<const uint4*>(sv + (blk * B + jj * SEG) * 2);
+#pragma unroll
+        for (int c = 0; c < SEG / 8; c++) {
+          const uint4 qv = src[c];
+          packed[4 * c + 0] = qv.x;
+          packed[4 * c + 1] = qv.y;
+          packed[4 * c + 2] = qv.z;
+          packed[4 * c + 3] = qv.w;
+        }
+      } else {
+        float2 W[SEG / 2];  // element pairs (2i, 2i+1)
+#pragma unroll
+        for (int m = 0; m < F; m++) {
+          const int e0 = blk * B + m * SEG;
+          const uint4* src = reinterpret_cast<const uint4*>(sv + e0 * 2);
+          const uint4* msk = reinterpret_cast<const uint4*>(smask + e0 / 2);
+          const bool neg = (__popc(jj & m) & 1) != 0;  // H_F[jj][m] = -1
+#pragma unroll
+          for (int c = 0; c < SEG / 8; c++) {
+            const uint4 qv = src[c];
+            const uint4 m01 = msk[2 * c], m23 = msk[2 * c + 1];
+            const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
+            const uint32_t mlo[4] = {m01.x, m01.z, m23.x, m23.z};
+            const uint32_t mhi[4] = {m01.y, m01.w, m23.y, m23.w};
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+              const float lo = __uint_as_float(words[p] * 65536u + mlo[p]);    // adding 2^31 flips the sign bit
+              const float hi = __uint_as_float((words[p] & 0xffff0000u) ^ mhi[p]);
+              const float2 z = make_float2(lo, hi);
+              const int i = 4 * c + p;
+              if (m == 0) W[i] = z;
+              else W[i] = neg ? f2sub(W[i], z) : f2add(W[i], z);
+            }
+          }
+        }
+        // H_SEG: the stage pairing adjacent elements inside a pair, then packed stages
+#pragma unroll
+        for (int i = 0; i < SEG / 2; i++) W[i] = make_float2(W[i].x + W[i].y, W[i].x - W[i].y);
+#pragma unroll
+        for (int hp = 1; hp < SEG / 2; hp <<= 1) {
+#pragma unroll
+          for (int i = 0; i < SEG / 2; i++) {
+            if ((i & hp) == 0) {
+              const float2 a = W[i], b = W[i + hp];
+              W[i] = f2add(a, b);
+              W[i + hp] = f2sub(a, b);
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < SEG / 2; i++) packed[i] = pack_bf16x2_rn(W[i].x, W[i].y);
+      }
+#pragma unroll
+      for (int p = 0; p < SEG / 2; p++) amax = absmax_bf16x2(amax, packed[p]);
+      const uint32_t alo = amax & 0x7fffu, ahi = (amax >> 16) & 0x7fffu;
+      amax = alo > ahi ? alo : ahi;
+    }
+    if (TPV > 1) {
+      samax[j * UT + u] = amax;
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < TPV; q++) {
+        const uint32_t o = samax[q * UT + u];
+        amax = o > amax ? o : amax;
+      }
+    }
+
+    if (active) {
+      const int64_t slot = slot_mapping[t];
+      if (slot >= num_slots) {
+        if (j == 0) flag(status, KV_INT4_DEV_BAD_SLOT);
+      } else if (slot >= 0) {
+        const float a = __uint_as_float(amax << 16);
+        float sc = 0.f, r = 0.f;
+        if (a >= kFlushAbsmax) {
+          sc = __fdiv_rn(a, 7.0f);
+          r = __frcp_rn(sc);
+        }
+        const float2 r2 = make_float2(r, r), magic2 = make_float2(kCodeMagic, kCodeMagic);
+        uint32_t out[SEG / 8];
+#pragma unroll
+        for (int wq = 0; wq < SEG / 8; wq++) {
+          uint32_t bytes[4];
+#pragma unroll
+          for (int p = 0; p < 4; p++) {
+            const uint32_t pw = packed[4 * wq + p];
+            const float2 tq = f2fma(make_float2(__uint_as_float(pw * 65536u), __uint_as_float(pw & 0xffff0000u)), r2, magic2);
+            bytes[p] = __float_as_uint(tq.y) * 16u + __float_as_uint(tq.x);  // low byte: (c_lo + 8) + 16 (c_hi + 8)
+          }
+          const uint32_t x01 = __byte_perm(bytes[0], bytes[1], 0x0040);
+          const uint32_t x23 = __byte_perm(bytes[2], bytes[3], 0x0040);
+          out[wq] = __byte_perm(x01, x23, 0x5410) ^ 0x88888888u;  // offset binary -> two's complement
+        }
+        uint4* dst = reinterpret_cast<uint4*>(u_cache + (slot * hkv + u_h) * (int64_t)(D / 2) + (blk * B + jj * SEG) / 2);
+#pragma unroll
+        for (int q = 0; q < SEG / 32; q++) dst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+        if (j == 0) u_scale[slot * hkv + u_h] = sc;
+      }
+    }
+    __syncthreads();  // the stage (and the absmax buffer) may now be overwritten
+    stage = (stage + 1) % G::STAGES;
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core variant of the rotation (the default for head sizes up to 192).
+//
+// H_b = H_{b/16} (x) H_16 (Sylvester; the group index is the high part of
+// the element index), so for each 16-element group q the 16-point transform
+// of the sign-flipped inputs, z_q = H_16 . D_q . x_q, is a 16 x 16 matrix
+// product with exact +-1 entries: one bf16 mma.sync (inputs exact, fp32
+// accumulation) handles 16 head vectors x one group x 8 outputs.  The
+// remaining log2(b/16) stages across groups of a Hadamard block are fp32
+// butterflies on values that the same thread already holds for every group.
+// The output columns of the MMA are permuted (B_q's columns) so that each lane
+// ends up with four consecutive outputs, i.e. two whole code bytes, per group.
+// ---------------------------------------------------------------------------
+template <int D>
+struct TcGeom {
+  static constexpr int B = D & -D;
+  static constexpr int NG = D / 16;        // 16-element groups per head vector
+  static constexpr int GB = B / 16;        // groups per Hadamard block
+  static constexpr int WARPS = 4;
+  static constexpr int MIN_CTAS = 3;       // register budget: three CTAs per SM
+  static constexpr int NT = WARPS * 32;
+  static constexpr int UT = WARPS * 16;    // head vectors per tile (16 rows per warp)
+  static constexpr int VSTRIDE = 2 * D + 16;
+  static constexpr int STAGE_BYTES = UT * VSTRIDE;
+  static constexpr int STAGES = 3;
+  static constexpr int CHUNKS = D / 8;
+  static constexpr int OROW = D / 2 + 16;  // output staging row (bytes), padded against bank conflicts
+  static constexpr int BFRAG_BYTES = NG * 2 * 32 * 8;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BFRAG_BYTES + WARPS * 16 * OROW;
+  static_assert(VSTRIDE % 32 == 16, "padded stride must be an odd number of 16-byte units");
+};
+
+// output o (0..15) of MMA column n of n-tile t: lane c holds columns 2c, 2c+1,
+// i.e. outputs 4c + 2t and 4c + 2t + 1
+__device__ __forceinline__ int tc_out_index(int t, int n) { return 4 * (n >> 1) + 2 * t + (n & 1); }
+
+template <int D>
+__global__ void __launch_bounds__(TcGeom<D>::NT, TcGeom<D>::MIN_CTAS)
+write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* __restrict__ v, int64_t v_stride,
+                const int64_t* __restrict__ slot_mapping, int num_tokens, uint8_t* __restrict__ k_cache,
+                uint8_t* __restrict__ v_cache, float* __restrict__ k_scale, float* __restrict__ v_scale,
+                int64_t num_slots, int hkv, int tt_per_tile, const int8_t* __restrict__ signs, int32_t* status) {
+  using G = TcGeom<D>;
+  constexpr int NG = G::NG, GB = G::GB, UT = G::UT, NT = G::NT;
+  constexpr int CPT = (UT * G::CHUNKS) / NT;  // copy chunks per thread per tile
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint2* sbfrag = reinterpret_cast<uint2*>(smem + G::STAGES * G::STAGE_BYTES);  // [NG][2][32]
+  uint8_t* sout = smem + G::STAGES * G::STAGE_BYTES + G::BFRAG_BYTES;           // [WARPS][16][OROW]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, cq = lane & 3;
+  const int units_per_token = 2 * hkv;
+  const int units = tt_per_tile * units_per_token;  // <= UT
+  const int num_tiles = (num_tokens + tt_per_tile - 1) / tt_per_tile;
+
+  // B_q fragments of D_q . H_16 (columns permuted), bf16 +-1
+  for (int e = tid; e < NG * 2 * 32; e += NT) {
+    const int q = e / 64, t = (e / 32) & 1, l = e & 31;
+    const int lg = l >> 2, lc = l & 3;
+    const int o = tc_out_index(t, lg);
+    uint32_t w[2];
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+      uint32_t pair = 0;
+#pragma unroll
+      for (int e2 = 0; e2 < 2; e2++) {
+        const int i = 2 * lc + 8 * half + e2;  // k index (input element within the group)
+        const int sgn = signs[16 * q + i];
+        const bool neg = ((__popc(i & o) & 1) != 0) != (sgn < 0);
+        pair |= (neg ? 0xbf80u : 0x3f80u) << (16 * e2);
+        if (blockIdx.x == 0 && t == 0 && lg == 0 && sgn != 1 && sgn != -1) flag(status, KV_INT4_DEV_BAD_SIGNS);
+      }
+      w[half] = pair;
+    }
+    sbfrag[e] = make_uint2(w[0], w[1]);
+  }
+
+  // copy slots of this thread (tile-invariant): chunk idx = tid + NT * q
+  const uint16_t* c_src[CPT];
+  int c_tok[CPT];  // token offset within the tile | K/V << 16, or -1 if unused
+#pragma unroll
+  for (int q = 0; q < CPT; q++) {
+    const int idx = tid + NT * q;
+    const int uu = idx / G::CHUNKS, c = idx % G::CHUNKS;
+    const int tt = uu / units_per_token, w = uu % units_per_token;
+    const int kv = w >= hkv, h = kv ? w - hkv : w;
+    c_tok[q] = uu < units ? tt | (kv << 16) : -1;
+    c_src[q] = (kv ? v : k) + (int64_t)tt * (kv ? v_stride : k_stride) + h * D + c * 8;
+  }
+  const int64_t k_tile_stride = (int64_t)tt_per_tile * k_stride, v_tile_stride = (int64_t)tt_per_tile * v_stride;
+  auto issue = [&](int tile, int stage) {
+    const uint32_t dst0 = smem_addr(stages + stage * G::STAGE_BYTES);
+    const int t0 = tile * tt_per_tile;
+#pragma unroll
+    for (int q = 0; q < CPT; q++) {
+      const int idx = tid + NT * q;
+      const int uu = idx / G::CHUNKS, c = idx % G::CHUNKS;
+      if (c_tok[q] >= 0 && t0 + (c_tok[q] & 0xffff) < num_tokens) {
+        const uint16_t* src = c_src[q] + (int64_t)tile * ((c_tok[q] >> 16) ? v_tile_stride : k_tile_stride);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst0 + uu * G::VSTRIDE + c * 16), "l"(src));
+      }
+    }
+  };
+
+  // this thread's two rows (head vectors) within the warp's 16: g and g + 8
+  int r_tt[2], r_kv[2], r_h[2];
+#pragma unroll
+  for (int rr = 0; rr < 2; rr++) {
+    const int uu = warp * 16 + g + 8 * rr;
+    r_tt[rr] = uu < units ? uu / units_per_token : -1;
+    const int w = uu % units_per_token;
+    r_kv[rr] = w >= hkv;
+    r_h[rr] = r_kv[rr] ? w - hkv : w;
+  }
+  // ldmatrix row address for this lane: matrices (rows 0-7|8-15) x (k 0-7|8-15)
+  const int a_row = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int a_col = (lane >> 4) * 8;
+  uint8_t* const wout = sout + warp * 16 * G::OROW;
+
+  int tile = blockIdx.x;
+  const int tstep = gridDim.x;
+#pragma unroll 1
+  for (int s = 0; s < G::STAGES - 1; s++) {
+    const int tt = tile + s * tstep;
+    if (tt < num_tiles) issue(tt, s);
+    cp_async_commit();
+  }
+  // slots of this thread's rows, loaded one tile ahead
+  auto load_slots = [&](int tl, int64_t (&sl)[2]) {
+#pragma unroll
+    for (int rr = 0; rr < 2; rr++) {
+      const int tok = tl * tt_per_tile + r_tt[rr];
+      sl[rr] = (tl < num_tiles && r_tt[rr] >= 0 && tok < num_tokens) ? slot_mapping[tok] : -1;
+    }
+  };
+  int64_t next_slot[2];
+  load_slots(tile, next_slot);
+  __syncthreads();  // B fragments visible
+
+  int stage = 0;
+#pragma unroll 1
+  for (; tile < num_tiles; tile += tstep) {
+    int64_t r_slot[2] = {next_slot[0], next_slot[1]};
+    load_slots(tile + tstep, next_slot);
+    {
+      const int tn = tile + (G::STAGES - 1) * tstep;
+      if (tn < num_tiles) issue(tn, (stage + G::STAGES - 1) % G::STAGES);
+      cp_async_commit();
+    }
+    cp_async_wait<G::STAGES - 1>();
+    __syncthreads();
+
+    const uint8_t* sa = stages + stage * G::STAGE_BYTES + a_row * G::VSTRIDE + a_col * 2;
+    uint32_t pk[2][NG][2];  // [n-tile][group][row g / row g+8]: bf16x2 of outputs (4c+2t, 4c+2t+1)
+#pragma unroll
+    for (int t = 0; t < 2; t++) {
+      float cacc[NG][4];
+#pragma unroll
+      for (int q = 0; q < NG; q++) {
+        uint32_t a[4];
+        ldmatrix_x4(a, sa + q * 32);
+        const uint2 bf = sbfrag[(q * 2 + t) * 32 + lane];
+        mma_16816_bf16_z(cacc[q], a, bf.x, bf.y);
+      }
+      // cross-group stages of each Hadamard block
+#pragma unroll
+      for (int h = 1; h < GB; h <<= 1) {
+#pragma unroll
+        for (int q = 0; q < NG; q++) {
+          if ((q & h) == 0) {
+            const float2 a0 = make_float2(cacc[q][0], cacc[q][1]), a1 = make_float2(cacc[q][2], cacc[q][3]);
+            const float2 b0 = make_float2(cacc[q + h][0], cacc[q + h][1]), b1 = make_float2(cacc[q + h][2], cacc[q + h][3]);
+            const float2 s0 = f2add(a0, b0), s1 = f2add(a1, b1), d0 = f2sub(a0, b0), d1 = f2sub(a1, b1);
+            cacc[q][0] = s0.x; cacc[q][1] = s0.y; cacc[q][2] = s1.x; cacc[q][3] = s1.y;
+            cacc[q + h][0] = d0.x; cacc[q + h][1] = d0.y; cacc[q + h][2] = d1.x; cacc[q + h][3] = d1.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NG; q++) {
+        pk[t][q][0] = pack_bf16x2_rn(cacc[q][0], cacc[q][1]);
+        pk[t][q][1] = pack_bf16x2_rn(cacc[q][2], cacc[q][3]);
+      }
+    }
+
+    // this thread's rows: slot (or -1: nothing to store)
+#pragma unroll
+    for (int rr = 0; rr < 2; rr++) {
+      if (r_slot[rr] >= num_slots) {
+        if (cq == 0 && r_kv[rr] == 0 && r_h[rr] == 0) flag(status, KV_INT4_DEV_BAD_SLOT);
+        r_slot[rr] = -1;
+      }
+    }
+    // per row: absmax over the 4 lanes of the quad, scale, codes
+#pragma unroll
+    for (int rr = 0; rr < 2; rr++) {
+      uint32_t am = 0;
+#pragma unroll
+      for (int t = 0; t < 2; t++)
+#pragma unroll
+        for (int q = 0; q < NG; q++) am = absmax_bf16x2(am, pk[t][q][rr]);
+      uint32_t a16 = max(am & 0x7fffu, (am >> 16) & 0x7fffu);
+      a16 = max(a16, __shfl_xor_sync(0xffffffffu, a16, 1));
+      a16 = max(a16, __shfl_xor_sync(0xffffffffu, a16, 2));
+      const float amax = __uint_as_float(a16 << 16);
+      float sc = 0.f, r = 0.f;
+      if (amax >= kFlushAbsmax) {
+        sc = __fdiv_rn(amax, 7.0f);
+        r = __frcp_rn(sc);
+      }
+      const float2 r2 = make_float2(r, r), magic2 = make_float2(kCodeMagic, kCodeMagic);
+      uint8_t* orow = wout + (g + 8 * rr) * G::OROW;
+#pragma unroll
+      for (int q = 0; q < NG; q++) {
+        uint32_t bytes[2];
+#pragma unroll
+        for (int t = 0; t < 2; t++) {
+          const uint32_t pw = pk[t][q][rr];
+          const float2 tq = f2fma(make_float2(__uint_as_float(pw * 65536u), __uint_as_float(pw & 0xffff0000u)), r2, magic2);
+          bytes[t] = (__float_as_uint(tq.y) * 16u + __float_as_uint(tq.x)) ^ 0x88u;  // (c_lo & 15) | (c_hi & 15) << 4
+        }
+        // outputs 4cq..4cq+3 of group q = bytes 8q + 2cq, 8q + 2cq + 1
+        *reinterpret_cast<uint16_t*>(orow + 8 * q + 2 * cq) = (uint16_t)__byte_perm(bytes[0], bytes[1], 0x0040);
+      }
+      if (cq == 0 && r_slot[rr] >= 0) (r_kv[rr] ? v_scale : k_scale)[r_slot[rr] * hkv + r_h[rr]] = sc;
+    }
+    __syncwarp();
+    // 16-byte stores: the quad of rows g, g + 8 stores those rows' chunks
+    constexpr int CPR = D / 32;  // 16-byte chunks per code row
+#pragma unroll
+    for (int rr = 0; rr < 2; rr++) {
+      if (r_slot[rr] < 0) continue;
+      uint8_t* dst = (r_kv[rr] ? v_cache : k_cache) + (r_slot[rr] * hkv + r_h[rr]) * (int64_t)(D / 2);
+#pragma unroll
+      for (int ch = cq; ch < CPR; ch += 4)
+        *reinterpret_cast<uint4*>(dst + ch * 16) =
+            *reinterpret_cast<const uint4*>(wout + (g + 8 * rr) * G::OROW + ch * 16);
+    }
+    __syncthreads();  // the stage may now be overwritten (and the output staging reused)
+    stage = (stage + 1) % G::STAGES;
+  }
+  cp_async_wait<0>();
+}
+
 template <int D, bool PREROT>
 static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
   using G = WriteGeom<D>;
@@ -284,9 +736,56 @@ static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, G::NT, G::SMEM) != cudaSuccess || o < 1) return KV_INT4_ERR_CUDA;
     occ[dev] = o;
   }
+  if constexpr (!PREROT && D <= 192) {
+    using T = TcGeom<D>;
+    if (2 * a.num_kv_heads <= T::UT) {
+      auto tckern = write_kernel_tc<D>;
+      static bool tc_done[kMaxDevices] = {};
+      static int tc_occ[kMaxDevices] = {};
+      if (!tc_done[dev]) {
+        if (cudaFuncSetAttribute(tckern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) != cudaSuccess)
+          return KV_INT4_ERR_CUDA;
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tckern, T::NT, T::SMEM) != cudaSuccess || o < 1)
+          return KV_INT4_ERR_CUDA;
+        tc_occ[dev] = o;
+        tc_done[dev] = true;
+      }
+      const int tt = T::UT / (2 * a.num_kv_heads);
+      const int64_t tiles = ((int64_t)a.num_tokens + tt - 1) / tt;
+      const int64_t tcap = (int64_t)sm_count(dev) * tc_occ[dev];
+      const int grid = (int)(tiles < tcap ? tiles : tcap);
+      timing_begin(kTimedWrite, stream);
+      tckern<<<grid, T::NT, T::SMEM, stream>>>(
+          static_cast<const uint16_t*>(a.k), a.k_stride, static_cast<const uint16_t*>(a.v), a.v_stride,
+          a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale,
+          (int64_t)a.num_blocks * a.block_size, a.num_kv_heads, tt, a.signs, a.dev_status);
+      timing_end(kTimedWrite, stream);
+      return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
+    }
+  }
+  const int64_t cap = (int64_t)sm_count(dev) * occ[dev];
+  if (2 * a.num_kv_heads <= G::UT) {
+    auto tkern = write_kernel_tok<D, PREROT>;
+    static bool tconfigured[kMaxDevices] = {};
+    if (!tconfigured[dev]) {
+      if (cudaFuncSetAttribute(tkern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM) != cudaSuccess)
+        return KV_INT4_ERR_CUDA;
+      tconfigured[dev] = true;
+    }
+    const int tt = G::UT / (2 * a.num_kv_heads);
+    const int64_t tiles = ((int64_t)a.num_tokens + tt - 1) / tt;
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    timing_begin(kTimedWrite, stream);
+    tkern<<<grid, G::NT, G::SMEM, stream>>>(
+        static_cast<const uint16_t*>(a.k), a.k_stride, static_cast<const uint16_t*>(a.v), a.v_stride,
+        a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale,
+        (int64_t)a.num_blocks * a.block_size, a.num_kv_heads, tt, a.signs, a.dev_status);
+    timing_end(kTimedWrite, stream);
+    return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
+  }
   const int64_t units = (int64_t)a.num_tokens * 2 * a.num_kv_heads;
   const int64_t tiles = (units + G::UT - 1) / G::UT;
-  const int64_t cap = (int64_t)sm_count(dev) * occ[dev];
   const int grid = (int)(tiles < cap ? tiles : cap);
   timing_begin(kTimedWrite, stream);
   write_kernel<D, PREROT><<<grid, G::NT, G::SMEM, stream>>>(

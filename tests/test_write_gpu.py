@@ -176,3 +176,28 @@ def test_write_tiny_workload_matches_oracle_history():
     mask = ~np.isnan(ref[2])
     diff = np.abs(O.unpack_codes(got[0][mask]).astype(int) - O.unpack_codes(ref[0][mask]).astype(int))
     assert diff.max() <= 1
+
+
+@pytest.mark.parametrize("d,hkv", [(192, 40), (96, 36), (128, 70)])
+def test_write_many_heads_generic_tiling(d, hkv):
+    """More kv heads than fit whole tokens into one tile (the tile then spans
+    token boundaries): codes and scales still bit-exact on the prerotated
+    path, and within one code end to end."""
+    T, nb = 53, 8
+    ky = _rotated_inputs(T, hkv, d, 300 + d)
+    vy = _rotated_inputs(T, hkv, d, 400 + d)
+    g = torch.Generator().manual_seed(d + hkv)
+    slots = torch.randperm(nb * 16, generator=g)[:T].to(torch.int64)
+    got, status = _run_gpu_write(ky, vy, slots, nb, _signs(d, 0), prerotated=True)
+    ref = _oracle_write(ky, vy, slots, nb, _signs(d, 0), prerotated=True)
+    assert status == 0
+    for a, b in zip(got, ref):
+        if a.dtype == np.float32:
+            assert np.array_equal(f32_bits(a), f32_bits(b))
+        else:
+            assert np.array_equal(a, b)
+    k = torch.randn((T, hkv, d), generator=g).to(torch.bfloat16)
+    got, status = _run_gpu_write(k, k, slots, nb, _signs(d, 5))
+    ref = _oracle_write(k, k, slots, nb, _signs(d, 5))
+    diff = np.abs(O.unpack_codes(got[0]).astype(int) - O.unpack_codes(ref[0]).astype(int))
+    assert diff.max() <= 1
