@@ -496,15 +496,30 @@ struct TcGeom {
   static constexpr int MIN_CTAS = 3;       // register budget: three CTAs per SM
   static constexpr int NT = WARPS * 32;
   static constexpr int UT = WARPS * 16;    // head vectors per tile (16 rows per warp)
-  static constexpr int VSTRIDE = 2 * D + 16;
+  // Staging layout (measured on GB300): for d = 128 rows padded by 16 bytes
+  // with 3 stages are fastest; for the other head sizes unpadded rows whose
+  // 16-byte chunks are XOR-swizzled, with 4 stages.  Both make the ldmatrix
+  // reads of eight rows bank-conflict free.
+  static constexpr bool SWIZZLE = D % 128 != 0;
+  static constexpr int VSTRIDE = SWIZZLE ? 2 * D : 2 * D + 16;
   static constexpr int STAGE_BYTES = UT * VSTRIDE;
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = SWIZZLE ? 4 : 3;
   static constexpr int CHUNKS = D / 8;
   static constexpr int OROW = D / 2 + 16;  // output staging row (bytes), padded against bank conflicts
   static constexpr int BFRAG_BYTES = NG * 2 * 32 * 8;
   static constexpr int SMEM = STAGES * STAGE_BYTES + BFRAG_BYTES + WARPS * 16 * OROW;
-  static_assert(VSTRIDE % 32 == 16, "padded stride must be an odd number of 16-byte units");
 };
+
+// Physical 16-byte chunk of logical chunk c in staged row `row`.  Rows that
+// are a multiple of 128 bytes XOR the chunk with row % 8 (eight rows read by
+// one ldmatrix land in eight different bank groups); 192-byte rows (d = 96)
+// alternate bank halves, so XOR with (row / 2) % 4 inside each 64-byte group.
+template <int D>
+__device__ __forceinline__ int tc_swz(int row, int c) {
+  if constexpr (!TcGeom<D>::SWIZZLE) return c;
+  else if constexpr ((2 * D) % 128 == 0) return c ^ (row & 7);
+  else return c ^ ((row >> 1) & 3);
+}
 
 // output o (0..15) of MMA column n of n-tile t: lane c holds columns 2c, 2c+1,
 // i.e. outputs 4c + 2t and 4c + 2t + 1
@@ -574,7 +589,8 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
       const int uu = idx / G::CHUNKS, c = idx % G::CHUNKS;
       if (c_tok[q] >= 0 && t0 + (c_tok[q] & 0xffff) < num_tokens) {
         const uint16_t* src = c_src[q] + (int64_t)tile * ((c_tok[q] >> 16) ? v_tile_stride : k_tile_stride);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst0 + uu * G::VSTRIDE + c * 16), "l"(src));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst0 + uu * G::VSTRIDE + tc_swz<D>(uu, c) * 16),
+                     "l"(src));
       }
     }
   };
@@ -589,9 +605,9 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
     r_kv[rr] = w >= hkv;
     r_h[rr] = r_kv[rr] ? w - hkv : w;
   }
-  // ldmatrix row address for this lane: matrices (rows 0-7|8-15) x (k 0-7|8-15)
+  // ldmatrix row for this lane: matrices (rows 0-7|8-15) x (k 0-7|8-15)
   const int a_row = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-  const int a_col = (lane >> 4) * 8;
+  const int a_half = lane >> 4;  // which 16-byte half of a 16-element group
   uint8_t* const wout = sout + warp * 16 * G::OROW;
 
   int tile = blockIdx.x;
@@ -619,15 +635,15 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
   for (; tile < num_tiles; tile += tstep) {
     int64_t r_slot[2] = {next_slot[0], next_slot[1]};
     load_slots(tile + tstep, next_slot);
+    cp_async_wait<G::STAGES - 2>();
+    __syncthreads();  // this tile's copies visible; every warp is past the previous tile's MMAs
     {
       const int tn = tile + (G::STAGES - 1) * tstep;
       if (tn < num_tiles) issue(tn, (stage + G::STAGES - 1) % G::STAGES);
       cp_async_commit();
     }
-    cp_async_wait<G::STAGES - 1>();
-    __syncthreads();
 
-    const uint8_t* sa = stages + stage * G::STAGE_BYTES + a_row * G::VSTRIDE + a_col * 2;
+    const uint8_t* sa = stages + stage * G::STAGE_BYTES + a_row * G::VSTRIDE;
     uint32_t pk[2][NG][2];  // [n-tile][group][row g / row g+8]: bf16x2 of outputs (4c+2t, 4c+2t+1)
 #pragma unroll
     for (int t = 0; t < 2; t++) {
@@ -635,7 +651,7 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
 #pragma unroll
       for (int q = 0; q < NG; q++) {
         uint32_t a[4];
-        ldmatrix_x4(a, sa + q * 32);
+        ldmatrix_x4(a, sa + tc_swz<D>(a_row, 2 * q + a_half) * 16);
         const uint2 bf = sbfrag[(q * 2 + t) * 32 + lane];
         mma_16816_bf16_z(cacc[q], a, bf.x, bf.y);
       }
@@ -713,7 +729,7 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
         *reinterpret_cast<uint4*>(dst + ch * 16) =
             *reinterpret_cast<const uint4*>(wout + (g + 8 * rr) * G::OROW + ch * 16);
     }
-    __syncthreads();  // the stage may now be overwritten (and the output staging reused)
+    __syncwarp();  // the warp's output staging may now be reused
     stage = (stage + 1) % G::STAGES;
   }
   cp_async_wait<0>();
