@@ -12,13 +12,17 @@
 //     sequence list with block prefix sums, prefill tile list); the other
 //     CTAs rotate every query once and pre-scale it by
 //     softmax_scale * log2(e) / b, stored as f16 (scores are then base-2).
-//  2. prefill (only if some sequence has q_len * G > 8 or G > 8): one CTA per
-//     64-row tile of (query token x q head of one kv group), FA2-style
-//     mma.sync with K/V dequantised once per block into f16 shared tiles.
-//  3. decode: stream-K over the flattened (decode sequence, kv head, block)
-//     space; every warp takes an equal contiguous range, so the split-KV
-//     load balance is exact.  Per block the warp computes S^T = K Q'^T with
-//     the 16 keys as the MMA M dimension (q_len*G <= 8 query columns as N),
+//  2. prefill (only for sequences whose q_len * G exceeds the decode column
+//     budget, or G > 8): one CTA per 64-row tile of (query token x q head of
+//     one kv group), FA2-style mma.sync with K/V dequantised once per block
+//     into f16 shared tiles.
+//  3. decode: stream-K over the flattened (decode sequence, head group,
+//     position) space, a position being one or two consecutive 16-key
+//     blocks; every CTA takes an equal contiguous range, so the split-KV
+//     load balance is exact.  The CTA stages each block of its head group
+//     into shared memory; per block a warp computes S^T = K Q'^T for its
+//     head with the 16 keys as the MMA M dimension (q_len*G <= 8 query
+//     columns as N; two blocks of a position share the 8 columns),
 //     converting INT4 nibbles straight into f16 A fragments in registers
 //     (the in-register order of head dimensions is a permutation applied
 //     consistently to q', which leaves q'.K unchanged); P is transposed with
@@ -92,11 +96,13 @@ struct Common {
   int tile_tokens;  // prefill: query tokens per 64-row tile
   int hg;           // decode: kv heads per CTA (largest divisor of hkv <= 8)
   int ng;           // decode: head groups per sequence (hkv / hg)
+  int np;           // decode: 16-key blocks per schedule position (1 or 2)
+  int dcols;        // decode: query columns per block (8 / np); longer queries go to prefill
   long long max_items;  // capacity of the prefill item list
 };
 
-__device__ __forceinline__ bool is_decode_kind(int qlen, int group) {
-  return group <= kDecodeCols && qlen * group <= kDecodeCols;
+__device__ __forceinline__ bool is_decode_kind(int qlen, const Common& c) {
+  return c.group <= c.dcols && qlen * c.group <= c.dcols;
 }
 
 // ---------------------------------------------------------------------------
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
         if (bad) {
           flag(c.status, KV_INT4_DEV_BAD_SEQ);
         } else if (ql > 0) {
-          kind = is_decode_kind(ql, c.group) ? 1 : 2;
+          kind = is_decode_kind(ql, c) ? 1 : 2;
           nblk = (L + 15) / 16;
           if (kind == 2) ntiles = (ql + c.tile_tokens - 1) / c.tile_tokens;
         }
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
       long long tot_b;
       int tot_c;
       const int ex_a = block_exclusive_scan<int>(kind == 1, &tot_a, s_i32);
-      const long long ex_b = block_exclusive_scan<long long>(kind == 1 ? nblk : 0, &tot_b, s_i64);
+      const long long ex_b = block_exclusive_scan<long long>(kind == 1 ? (nblk + c.np - 1) / c.np : 0, &tot_b, s_i64);
       const int ex_c = block_exclusive_scan<int>(ntiles, &tot_c, s_i32);
       if (kind == 1) {
         pv.dseq[n_dseq + ex_a] = s;
@@ -227,11 +233,20 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
 }
 
 // ---------------------------------------------------------------------------
-// 3. decode: stream-K, one warp per equal range of (segment, block) positions
+// 3. decode: stream-K over (segment, position) units, one CTA per head group
 // ---------------------------------------------------------------------------
-template <int D>
+// A position is NP consecutive 16-key blocks of one segment.  With NP > 1 the
+// blocks share one score accumulator: block j owns query columns
+// [j * COLS, (j + 1) * COLS) (COLS = 8 / NP >= the sequence's q_len * G), so
+// one softmax pass, one barrier and one V offset correction serve NP blocks.
+// Each column keeps its own running (m, l, o'); the reduce kernel merges the
+// NP columns of a query with the log-sum-exp rule like any other split.
+template <int D, int NP>
 struct DecGeom {
-  static constexpr int STAGES = 4;
+  static constexpr int COLS = kDecodeCols / NP;  // query columns per block
+  // ring of single-block slots: NP consumed per iteration, the rest in flight
+  static constexpr int NS = NP == 1 ? 4 : 2 * NP + 1;
+  static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
   static constexpr int KROW = D / 2;        // K tile row stride (bytes)
   static constexpr int VROW = D / 2 + 16;   // V tile row stride, padded: conflict-free V fragment loads
   static constexpr int KTILE = 16 * KROW;
@@ -243,32 +258,37 @@ struct DecGeom {
   static constexpr int VB = D / 16;     // V bytes per row per thread (eighth row)
   static constexpr int KSTEPS = D / 16;
   static constexpr int CHR = D / 32;    // 16-byte chunks per code row
-  // per stage: hg head tiles, then scales [K/V][hg][16]
-  __host__ __device__ static constexpr int stage_bytes(int hg) { return hg * (HTILE + 128); }
-  __host__ __device__ static constexpr int smem_bytes(int hg) { return STAGES * stage_bytes(hg) + 16; }
+  // per slot: hg head tiles, then scales [K/V][hg][16]
+  __host__ __device__ static constexpr int slot_bytes(int hg) { return hg * (HTILE + 128); }
+  __host__ __device__ static constexpr int smem_bytes(int hg) { return NS * slot_bytes(hg) + 32; }
   static_assert(HTILE % 16 == 0, "tile alignment");
+  static_assert(WAIT >= 0 && NS <= 8, "slot ring");
 };
 
-// Walk over the decode positions (sequence i, head group grp, block kb).
+// Walk over the decode units (sequence i, head group grp, position kp).
 struct DecWalk {
   int i;      // index into the decode-sequence list
   int grp;    // head group
-  int kb;     // block within the sequence
-  int nblk;   // blocks of the sequence
+  int kp;     // position within the sequence
+  int npos;   // positions of the sequence
+  int nblk;   // 16-key blocks of the sequence
   int seq;    // sequence id
 };
 
+template <int NP>
 __device__ __forceinline__ void walk_load(DecWalk& w, const Common& c, const PlanView& pv) {
   w.seq = pv.dseq[w.i];
   w.nblk = (c.seq_lens[w.seq] + 15) / 16;
+  w.npos = (w.nblk + NP - 1) / NP;
 }
+template <int NP>
 __device__ __forceinline__ void walk_next(DecWalk& w, const Common& c, const PlanView& pv) {
-  if (++w.kb == w.nblk) {
-    w.kb = 0;
+  if (++w.kp == w.npos) {
+    w.kp = 0;
     if (++w.grp == c.ng) {
       w.grp = 0;
       ++w.i;
-      walk_load(w, c, pv);
+      walk_load<NP>(w, c, pv);
     }
   }
 }
@@ -297,8 +317,9 @@ __device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint8_t* p) {
 // O'^T += V^T P'^T for the thread's D/8 head dimensions, one m-tile at a time:
 // each m-tile's A fragment is (keys ka,kb; d even), (ka,kb; d odd),
 // (kc,kd; d even), (kc,kd; d odd), built by one lop3 each from byte-interleaved
-// words of the four key rows, followed by the per-block offset correction.
-template <int D>
+// words of the four key rows.  With CORR the block's offset correction
+// follows every m-tile's MMA.
+template <int D, bool CORR>
 __device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], const uint8_t* ra, const uint8_t* rb,
                                         const uint8_t* rc, const uint8_t* rd, uint32_t b0, uint32_t b1,
                                         const uint32_t (&vcorr)[4]) {
@@ -324,7 +345,7 @@ __device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], const uint8_t*
       for (int t = 0; t < 4; t++) {
         const uint32_t a[4] = {nib_lo(src01[t]), nib_hi(src01[t]), nib_lo(src89[t]), nib_hi(src89[t])};
         mma_16816(oacc[4 * k + t], a, b0, b1);
-        mma_16816(oacc[4 * k + t], vcorr, b0, b1);
+        if constexpr (CORR) mma_16816(oacc[4 * k + t], vcorr, b0, b1);
       }
     }
   } else {
@@ -343,7 +364,7 @@ __device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], const uint8_t*
       for (int t = 0; t < 2; t++) {
         const uint32_t a[4] = {nib_lo(src01[t]), nib_hi(src01[t]), nib_lo(src89[t]), nib_hi(src89[t])};
         mma_16816(oacc[2 * k + t], a, b0, b1);
-        mma_16816(oacc[2 * k + t], vcorr, b0, b1);
+        if constexpr (CORR) mma_16816(oacc[2 * k + t], vcorr, b0, b1);
       }
     }
   }
@@ -356,13 +377,13 @@ struct DecParams {
 };
 
 // Work decomposition: stream-K over the flattened (decode sequence, head
-// group, 16-key block) positions; CTA r takes positions
-// [Tb*r/R, Tb*(r+1)/R).  A CTA has one warp per kv head of the group; for
-// every position all its threads copy the block's codes and scales of the
-// group's heads -- contiguous runs of the cache -- into per-head padded tiles,
-// and each warp then computes its own head.  Every (segment, head) piece of
-// a CTA's range writes (o', m, l): to the sequence's direct slot if the
-// piece starts the segment, else to the CTA's slot.
+// group, position) units; CTA r takes units [T*r/R, T*(r+1)/R).  A CTA has
+// one warp per kv head of the group; for every block all its threads copy
+// the block's codes and scales of the group's heads -- contiguous runs of the
+// cache -- into per-head padded tiles, and each warp then computes its own
+// head.  Every (segment, head) piece of a CTA's range writes (o', m, l) for
+// all 8 columns: to the sequence's direct slot if the piece starts the
+// segment, else to the CTA's slot.
 //
 // Score arithmetic.  A K fragment holds 1032 + c at the low-nibble positions
 // and 1152 + 16c at the high-nibble ones; the q' fragment carries 16 q' at the
@@ -370,14 +391,14 @@ struct DecParams {
 //   acc = 16 (q' . c) + bias,  bias = sum_low 16 q' * 1032 + sum_high q' * 1152,
 // and bias is itself one MMA of a constant A fragment against q' per segment.
 // The V side works the same way: even head dimensions accumulate
-// p'(1032 + c), odd ones p'(1152 + 16c); right after each block's MMA a
-// second MMA of a constant (-1032 / -1152) A fragment against the same P'^T
-// removes that block's offset, so the running accumulator only ever holds
-// one block's worth of offset (accumulating the offset over thousands of keys
-// would cost the fp32 accumulator the signal's low bits).
-template <int D>
+// p'(1032 + c), odd ones p'(1152 + 16c); right after each position's MMAs a
+// further MMA of a constant (-1032 / -1152) A fragment against the same P'^T
+// removes that position's offset, so the running accumulator only ever holds
+// one block's worth of offset per column (accumulating the offset over
+// thousands of keys would cost the fp32 accumulator the signal's low bits).
+template <int D, int NP>
 __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
-  using G = DecGeom<D>;
+  using G = DecGeom<D, NP>;
   const Common& c = prm.c;
   const PlanView& pv = prm.pv;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -385,14 +406,14 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   const int tid = threadIdx.x, nthr = HG * 32;
   const int hl = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
-  const int SB = G::stage_bytes(HG);
-  int* sflag = reinterpret_cast<int*>(smem + G::STAGES * SB);
+  const int SB = G::slot_bytes(HG);
+  int* sflag = reinterpret_cast<int*>(smem + G::NS * SB);
 
   const int n_dseq = pv.plan[0];
   if (n_dseq == 0) return;
-  const long long Tb = pv.dprefix[n_dseq] * c.ng;
+  const long long Tu = pv.dprefix[n_dseq] * c.ng;
   const int R = prm.num_ctas;
-  const long long P0 = Tb * blockIdx.x / R, P1 = Tb * (blockIdx.x + 1) / R;
+  const long long P0 = Tu * blockIdx.x / R, P1 = Tu * (blockIdx.x + 1) / R;
   if (P0 >= P1) return;
 
   // locate P0: largest i with dprefix[i] * ng <= P0 (32-ary search, per warp)
@@ -410,18 +431,18 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   }
   DecWalk cw;
   cw.i = lo;
-  walk_load(cw, c, pv);
+  walk_load<NP>(cw, c, pv);
   {
     const long long off = P0 - pv.dprefix[cw.i] * c.ng;
-    cw.grp = (int)(off / cw.nblk);
-    cw.kb = (int)(off - (long long)cw.grp * cw.nblk);
+    cw.grp = (int)(off / cw.npos);
+    cw.kp = (int)(off - (long long)cw.grp * cw.npos);
   }
   DecWalk pw = cw;
 
   // thread-constant parts of the staging addresses: CHR chunks per thread
   // (chunk index ((kv * 16 + r) * HG + h) * CHR + col: consecutive threads read
   // consecutive bytes of the cache)
-  uint32_t c_saddr[G::CHR];      // shared address within stage 0
+  uint32_t c_saddr[G::CHR];      // shared address within slot 0
   const uint8_t* c_src[G::CHR];  // cache address within block 0, head group 0
 #pragma unroll
   for (int j = 0; j < G::CHR; j++) {
@@ -442,40 +463,50 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   const uint32_t blk_bytes = 16u * c.hkv * (D / 2);  // < 2^32 (host-checked head counts)
   const uint32_t blk_scales = 16u * c.hkv;
 
-  auto block_id = [&](const DecWalk& w) { return c.block_table[(long long)w.seq * c.max_blocks + w.kb]; };
-  auto issue = [&](const DecWalk& w, int blk, int stage) {
+  // block j of a position, or kAbsent past the end of the sequence (NP > 1)
+  constexpr int kAbsent = -0x7fffffff - 1;
+  auto block_at = [&](const DecWalk& w, int j) {
+    const int kb = w.kp * NP + j;
+    return kb < w.nblk ? c.block_table[(long long)w.seq * c.max_blocks + kb] : kAbsent;
+  };
+  auto issue = [&](int blk, int grp, int slot) {
     const bool ok = blk >= 0 && blk < c.num_blocks;
     if (ok) {
-      const uint32_t soff = (uint32_t)(stage * SB);
-      const uint32_t goff = (uint32_t)(w.grp * HG * (D / 2));
+      const uint32_t soff = (uint32_t)(slot * SB);
+      const uint32_t goff = (uint32_t)(grp * HG * (D / 2));
 #pragma unroll
       for (int j = 0; j < G::CHR; j++) {
         const uint8_t* src = c_src[j] + (uint64_t)(uint32_t)blk * blk_bytes + goff;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(c_saddr[j] + soff), "l"(src));
       }
-      const float* ssrc = s_src + (uint64_t)(uint32_t)blk * blk_scales + w.grp * HG;
+      const float* ssrc = s_src + (uint64_t)(uint32_t)blk * blk_scales + grp * HG;
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s_saddr + soff), "l"(ssrc));
     }
     if (tid == 0) {
-      sflag[stage] = ok;
-      if (!ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
+      sflag[slot] = ok;
+      if (!ok && blk != kAbsent) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
     }
   };
 
-  // producer: issue block ppos, prefetching the next block id one step ahead
+  // producer: one block per call into the next ring slot, the next block id
+  // loaded one call ahead; one commit group per call (empty past the range)
   long long ppos = P0;
-  int pblk = block_id(pw);
-#pragma unroll 1
-  for (int s = 0; s < G::STAGES - 1; s++) {
+  int pj = 0, ps = 0;
+  int pblk = block_at(pw, 0);
+  auto produce = [&]() {
     if (ppos < P1) {
-      issue(pw, pblk, s);
-      if (++ppos < P1) {
-        walk_next(pw, c, pv);
-        pblk = block_id(pw);
+      issue(pblk, pw.grp, ps);
+      ps = ps + 1 == G::NS ? 0 : ps + 1;
+      if (++pj == NP) {
+        pj = 0;
+        if (++ppos < P1) walk_next<NP>(pw, c, pv);
       }
+      if (ppos < P1) pblk = block_at(pw, pj);
     }
     cp_async_commit();
-  }
+  };
+#pragma unroll 1
+  for (int s = 0; s < G::NS - NP; s++) produce();
 
   // per-segment state of this warp's head
   uint32_t qb[G::KSTEPS][2];
@@ -483,7 +514,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   float m0, m1, l0, l1, bias0, bias1;
   int lim0, lim1;  // keys visible to columns 2cq, 2cq+1
   int lim_warp;    // smallest of all columns' limits
-  bool first_piece = cw.kb == 0;
+  bool first_piece = cw.kp == 0;
 
   auto begin_segment = [&]() {
     const int seq = cw.seq;
@@ -492,8 +523,8 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const int ql = c.qsl[seq + 1] - q0;
     const int L = c.seq_lens[seq];
     const int ctx = L - ql;
-    // B fragments of this lane's column n = g
-    const int n = g;
+    // B fragments of this lane's column g, which holds query column g % COLS
+    const int n = g & (G::COLS - 1);
     const bool colok = n < ql * c.group;
     const int j = n / c.group, jj = n - j * c.group;
     const __half* qrow = pv.qrot + ((long long)(q0 + (colok ? j : 0)) * c.hq + head * c.group + (colok ? jj : 0)) * D;
@@ -516,7 +547,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     for (int s = 0; s < G::KSTEPS; s++) mma_16816(bacc, abias, qb[s][0], qb[s][1]);
     bias0 = bacc[0];
     bias1 = bacc[1];
-    const int col0 = 2 * cq, col1 = 2 * cq + 1;
+    const int col0 = (2 * cq) & (G::COLS - 1), col1 = (2 * cq + 1) & (G::COLS - 1);
     const int j0 = min(col0 / c.group, max(ql - 1, 0)), j1 = min(col1 / c.group, max(ql - 1, 0));
     lim0 = c.causal ? min(L, ctx + j0 + 1) : L;
     lim1 = c.causal ? min(L, ctx + j1 + 1) : L;
@@ -566,32 +597,41 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   };
 
   begin_segment();
-  int stage = 0;
-  const int nblocks = (int)(P1 - P0);
+  const int jb = (cq * NP) >> 2;  // block of this thread's score columns 2cq, 2cq+1
+  const int jv = (g * NP) >> 3;   // block of this lane's P'^T column g
+  int cs = 0;                     // slot of the iteration's first block
+  const int nunits = (int)(P1 - P0);
   // rows g (even d: offset 1032) and g + 8 (odd d: offset 1152)
   const uint32_t vcorr[4] = {kF16x2_M1032, kF16x2_M1152, kF16x2_M1032, kF16x2_M1152};
 #pragma unroll 1
-  for (int it = 0; it < nblocks; it++) {
-    cp_async_wait<G::STAGES - 2>();
-    __syncthreads();  // this block's copies visible; every warp done with the previous stage
-    if (ppos < P1) {
-      issue(pw, pblk, (stage + G::STAGES - 1) % G::STAGES);
-      if (++ppos < P1) {
-        walk_next(pw, c, pv);
-        pblk = block_id(pw);
-      }
+  for (int it = 0; it < nunits; it++) {
+    cp_async_wait<G::WAIT>();
+    __syncthreads();  // this position's copies visible; every warp done with the previous slots
+#pragma unroll
+    for (int j = 0; j < NP; j++) produce();
+
+    int slot[NP];
+    slot[0] = cs;
+#pragma unroll
+    for (int j = 1; j < NP; j++) slot[j] = slot[j - 1] + 1 == G::NS ? 0 : slot[j - 1] + 1;
+    bool allok = true;
+    int my = slot[0];
+#pragma unroll
+    for (int j = 0; j < NP; j++) {
+      allok = allok && sflag[slot[j]] != 0;
+      if (j > 0 && jb == j) my = slot[j];
     }
-    cp_async_commit();
+    const uint8_t* mstg = smem + my * SB;
+    const bool bok = sflag[my] != 0;
+    const float* sks = reinterpret_cast<const float*>(mstg + HG * G::HTILE + hl * 64);
+    const float* svs = reinterpret_cast<const float*>(mstg + HG * G::HTILE + (HG + hl) * 64);
 
-    const uint8_t* stg = smem + stage * SB;
-    const uint8_t* st = stg + hl * G::HTILE;
-    const bool bok = sflag[stage] != 0;
-    const float* sks = reinterpret_cast<const float*>(stg + HG * G::HTILE + hl * 64);
-    const float* svs = reinterpret_cast<const float*>(stg + HG * G::HTILE + (HG + hl) * 64);
-
-    // ---- S^T = K Q'^T (biased, x16) ----
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-    {
+    // ---- S^T = K Q'^T (biased, x16), one accumulator per block ----
+    float sacc[NP][4];
+#pragma unroll
+    for (int j = 0; j < NP; j++) {
+      sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+      const uint8_t* st = smem + slot[j] * SB + hl * G::HTILE;
       uint32_t xk[G::KW], yk[G::KW];
       lds_words<G::KW, D / 8>(xk, st + g * G::KROW + cq * (D / 8));
       lds_words<G::KW, D / 8>(yk, st + (g + 8) * G::KROW + cq * (D / 8));
@@ -599,18 +639,25 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
       for (int w = 0; w < G::KW; w++) {
         const uint32_t x = xk[w], y = yk[w], x8 = x >> 8, y8 = y >> 8;
         const uint32_t a0[4] = {nib_lo(x), nib_lo(y), nib_hi(x), nib_hi(y)};
-        mma_16816(sacc, a0, qb[2 * w][0], qb[2 * w][1]);
+        mma_16816(sacc[j], a0, qb[2 * w][0], qb[2 * w][1]);
         const uint32_t a1[4] = {nib_lo(x8), nib_lo(y8), nib_hi(x8), nib_hi(y8)};
-        mma_16816(sacc, a1, qb[2 * w + 1][0], qb[2 * w + 1][1]);
+        mma_16816(sacc[j], a1, qb[2 * w + 1][0], qb[2 * w + 1][1]);
       }
     }
-    const int pos0 = cw.kb * 16 + g, pos1 = pos0 + 8;
+    float sa[4] = {sacc[0][0], sacc[0][1], sacc[0][2], sacc[0][3]};
+#pragma unroll
+    for (int j = 1; j < NP; j++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) sa[e] = jb == j ? sacc[j][e] : sa[e];
+
+    const int kb0 = cw.kp * NP;
+    const int pos0 = (kb0 + jb) * 16 + g, pos1 = pos0 + 8;
     const float ks0 = sks[g] * 0.0625f, ks1 = sks[g + 8] * 0.0625f;
-    float s00 = (sacc[0] - bias0) * ks0, s01 = (sacc[1] - bias1) * ks0;
-    float s10 = (sacc[2] - bias0) * ks1, s11 = (sacc[3] - bias1) * ks1;
-    // keys past a column's visible length (or in an invalid block) only occur
-    // in blocks that reach past the warp's smallest limit
-    const bool full = bok && cw.kb * 16 + 16 <= lim_warp;
+    float s00 = (sa[0] - bias0) * ks0, s01 = (sa[1] - bias1) * ks0;
+    float s10 = (sa[2] - bias0) * ks1, s11 = (sa[3] - bias1) * ks1;
+    // keys past a column's visible length (or in an invalid or absent block)
+    // only occur in positions that reach past the warp's smallest limit
+    const bool full = allok && (kb0 + NP) * 16 <= lim_warp;
     if (!full) {
       s00 = (bok && pos0 < lim0) ? s00 : -INFINITY;
       s01 = (bok && pos0 < lim1) ? s01 : -INFINITY;
@@ -659,24 +706,36 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const uint32_t M1 = pack_f16x2(q10, q11);
     const uint32_t b0 = movmatrix_trans(M0), b1 = movmatrix_trans(M1);
 
-    // ---- O'^T += V^T P'^T (offset removed per block) ----
-    {
-      const uint8_t* sv = st + G::KTILE + g * G::VB;
-      pv_mmas<D>(oacc, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW, sv + (2 * cq + 8) * G::VROW,
-                 sv + (2 * cq + 9) * G::VROW, b0, b1, vcorr);
+    // ---- O'^T += V^T P'^T (offset removed per position) ----
+    if constexpr (NP == 1) {
+      const uint8_t* sv = smem + slot[0] * SB + hl * G::HTILE + G::KTILE + g * G::VB;
+      pv_mmas<D, true>(oacc, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW, sv + (2 * cq + 8) * G::VROW,
+                       sv + (2 * cq + 9) * G::VROW, b0, b1, vcorr);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NP; j++) {
+        // block j's probabilities only: the other blocks' columns are zero
+        const uint32_t bj0 = jv == j ? b0 : 0u, bj1 = jv == j ? b1 : 0u;
+        const uint8_t* sv = smem + slot[j] * SB + hl * G::HTILE + G::KTILE + g * G::VB;
+        pv_mmas<D, false>(oacc, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW, sv + (2 * cq + 8) * G::VROW,
+                          sv + (2 * cq + 9) * G::VROW, bj0, bj1, vcorr);
+      }
+#pragma unroll
+      for (int i = 0; i < G::KSTEPS; i++) mma_16816(oacc[i], vcorr, b0, b1);
     }
 
-    const bool last_in_seg = cw.kb == cw.nblk - 1;
-    const bool last_in_range = it + 1 == nblocks;
+    const bool last_in_seg = cw.kp == cw.npos - 1;
+    const bool last_in_range = it + 1 == nunits;
     if (last_in_seg || last_in_range) flush();
     if (!last_in_range) {
-      walk_next(cw, c, pv);
+      walk_next<NP>(cw, c, pv);
       if (last_in_seg) {
         first_piece = true;
         begin_segment();
       }
     }
-    stage = (stage + 1) % G::STAGES;
+    cs += NP;
+    if (cs >= G::NS) cs -= G::NS;
   }
   cp_async_wait<0>();
 }
@@ -703,37 +762,44 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   const int seq = pv.dseq[i];
   const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
   const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (col >= ql * c.group) return;
+  if (col >= ql * c.group) return;  // ql * group <= dcols
   const int nblk = (c.seq_lens[seq] + 15) / 16;
+  const int npos = (nblk + c.np - 1) / c.np;
   const int grp = h / c.hg, hl = h - grp * c.hg;
-  const long long Tb = pv.dprefix[n_dseq] * c.ng;
-  const long long sbeg = pv.dprefix[i] * c.ng + (long long)grp * nblk, send = sbeg + nblk;
+  const long long Tu = pv.dprefix[n_dseq] * c.ng;
+  const long long sbeg = pv.dprefix[i] * c.ng + (long long)grp * npos, send = sbeg + npos;
   const int W = prm.num_ctas;
-  auto wstart = [&](long long w) { return Tb * w / W; };
+  auto wstart = [&](long long w) { return Tu * w / W; };
 
   constexpr int PER = D / 32;
   float acc[PER];
-  const float* od = pv.direct_o + ((long long)seg * kDecodeCols + col) * D;
-  float M = pv.direct_ml[((long long)seg * kDecodeCols + col) * 2];
-  float Lsum = pv.direct_ml[((long long)seg * kDecodeCols + col) * 2 + 1];
 #pragma unroll
-  for (int k = 0; k < PER; k++) acc[k] = od[lane + 32 * k];
+  for (int k = 0; k < PER; k++) acc[k] = 0.f;
+  float M = -INFINITY, Lsum = 0.f;
+  // a piece's columns col, col + dcols, ... hold the same query over
+  // disjoint key blocks
+  auto merge_slot = [&](const float* o_base, const float* ml_base) {
+    for (int sub = 0; sub < c.np; sub++) {
+      const int cc = col + sub * c.dcols;
+      const float* ow = o_base + cc * D;
+      const float mw = ml_base[cc * 2], lw = ml_base[cc * 2 + 1];
+      const float Mn = fmaxf(M, mw);
+      const float Mu = Mn == -INFINITY ? 0.f : Mn;
+      const float a = fast_exp2(M - Mu), b = fast_exp2(mw - Mu);
+#pragma unroll
+      for (int k = 0; k < PER; k++) acc[k] = acc[k] * a + ow[lane + 32 * k] * b;
+      Lsum = Lsum * a + lw * b;
+      M = Mn;
+    }
+  };
+  merge_slot(pv.direct_o + (long long)seg * kDecodeCols * D, pv.direct_ml + (long long)seg * kDecodeCols * 2);
   // CTAs whose (non-empty) range starts strictly inside this segment
-  long long w = (sbeg * W) / Tb;
+  long long w = (sbeg * W) / Tu;
   while (w < W && wstart(w) <= sbeg) w++;
   for (; w < W && wstart(w) < send; w++) {
     if (wstart(w + 1) <= wstart(w)) continue;
     const long long slot = w * c.hg + hl;
-    const float* ow = pv.warp_o + (slot * kDecodeCols + col) * D;
-    const float mw = pv.warp_ml[(slot * kDecodeCols + col) * 2];
-    const float lw = pv.warp_ml[(slot * kDecodeCols + col) * 2 + 1];
-    const float Mn = fmaxf(M, mw);
-    const float Mu = Mn == -INFINITY ? 0.f : Mn;
-    const float a = fast_exp2(M - Mu), b = fast_exp2(mw - Mu);
-#pragma unroll
-    for (int k = 0; k < PER; k++) acc[k] = acc[k] * a + ow[lane + 32 * k] * b;
-    Lsum = Lsum * a + lw * b;
-    M = Mn;
+    merge_slot(pv.warp_o + slot * kDecodeCols * D, pv.warp_ml + slot * kDecodeCols * 2);
   }
   float* r = srow[col];
   const float inv = 1.f / (Lsum * (float)B);
@@ -1092,6 +1158,47 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.ng = a.num_kv_heads / c.hg;
   if (c.group > kPrefillRows) return KV_INT4_ERR_HEADS;
 
+  // decode configuration: blocks per schedule position and the kernel's
+  // occupancy.  Pairing blocks needs q_len * G <= 4 for every decode
+  // sequence; when the batch also holds prefills (q_len * G > 8 somewhere),
+  // decode is sized for single-token queries and longer ones go to prefill.
+  const bool any_decode = c.group <= kDecodeCols;
+  int dec_occ = 0;
+  if (any_decode) {
+    static bool attr_done[kMaxDevices][2] = {};
+    static int occ_cache[kMaxDevices][2][9] = {};
+    auto occupancy = [&](auto kern, int np, int smem_max, int smem) -> int {
+      if (!attr_done[dev][np - 1]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess) return 0;
+        attr_done[dev][np - 1] = true;
+      }
+      if (!occ_cache[dev][np - 1][c.hg]) {
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.hg * 32, smem) != cudaSuccess || o < 1) return 0;
+        occ_cache[dev][np - 1][c.hg] = o;
+      }
+      return occ_cache[dev][np - 1][c.hg];
+    };
+    const int occ1 = occupancy(decode_kernel<D, 1>, 1, DecGeom<D, 1>::smem_bytes(8), DecGeom<D, 1>::smem_bytes(c.hg));
+    if (occ1 < 1) return KV_INT4_ERR_CUDA;
+    const long long mq = (long long)(a.max_query_len > 0 ? a.max_query_len : 1) * c.group;
+    const long long cols = mq <= kDecodeCols ? mq : c.group;
+    c.np = 1;
+    dec_occ = occ1;
+    if (cols <= kDecodeCols / 2) {
+      const int occ2 =
+          occupancy(decode_kernel<D, 2>, 2, DecGeom<D, 2>::smem_bytes(8), DecGeom<D, 2>::smem_bytes(c.hg));
+      if (occ2 < 1) return KV_INT4_ERR_CUDA;
+      if (occ2 >= occ1) {
+        c.np = 2;
+        dec_occ = occ2;
+      }
+    }
+  } else {
+    c.np = 1;
+  }
+  c.dcols = kDecodeCols / c.np;
+
   // 1. prep
   {
     const long long rows = (long long)a.num_q_tokens * a.num_q_heads;
@@ -1103,7 +1210,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   // 2. prefill
-  const bool may_prefill = c.group > kDecodeCols || (long long)a.max_query_len * c.group > kDecodeCols;
+  const bool may_prefill = c.group > c.dcols || (long long)a.max_query_len * c.group > c.dcols;
   if (may_prefill) {
     using G = PreGeom<D>;
     static bool done[kMaxDevices] = {};
@@ -1119,28 +1226,18 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   // 3. decode + 4. reduce
-  if (c.group <= kDecodeCols) {
-    using G = DecGeom<D>;
-    static bool attr_done[kMaxDevices] = {};
-    static int occ_cache[kMaxDevices][9] = {};
-    if (!attr_done[dev]) {
-      if (cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::smem_bytes(8)) !=
-          cudaSuccess)
-        return KV_INT4_ERR_CUDA;
-      attr_done[dev] = true;
-    }
-    const int threads = c.hg * 32, smem = G::smem_bytes(c.hg);
-    if (!occ_cache[dev][c.hg]) {
-      int o = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<D>, threads, smem) != cudaSuccess || o < 1)
-        return KV_INT4_ERR_CUDA;
-      occ_cache[dev][c.hg] = o;
-    }
-    long long grid = (long long)sms * occ_cache[dev][c.hg];
+  if (any_decode) {
+    long long grid = (long long)sms * dec_occ;
     if (grid * c.hg > kMaxDecodeWarps) grid = kMaxDecodeWarps / c.hg;
     const int num_ctas = (int)grid;
+    const int threads = c.hg * 32;
     timing_begin(kTimedDecode, stream);
-    decode_kernel<D><<<(unsigned)grid, threads, smem, stream>>>(DecParams{c, pv, num_ctas});
+    if (c.np == 2)
+      decode_kernel<D, 2><<<(unsigned)grid, threads, DecGeom<D, 2>::smem_bytes(c.hg), stream>>>(
+          DecParams{c, pv, num_ctas});
+    else
+      decode_kernel<D, 1><<<(unsigned)grid, threads, DecGeom<D, 1>::smem_bytes(c.hg), stream>>>(
+          DecParams{c, pv, num_ctas});
     timing_end(kTimedDecode, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
     const long long rgrid = (long long)a.num_seqs * a.num_kv_heads;
