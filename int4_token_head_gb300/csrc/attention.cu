@@ -248,14 +248,15 @@ struct DecGeom {
   static constexpr int NS = NP == 1 ? 4 : 2 * NP + 1;
   static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
   static constexpr int KROW = D / 2;        // K tile row stride (bytes)
-  static constexpr int VROW = D / 2 + 16;   // V tile row stride, padded: conflict-free V fragment loads
+  // V tile row stride: an odd multiple of 16 bytes, so that the 8 rows of
+  // an ldmatrix piece fall in distinct bank groups
+  static constexpr int VROW = (D / 32) % 2 ? D / 2 : D / 2 + 16;
   static constexpr int KTILE = 16 * KROW;
   static constexpr int VTILE = 16 * VROW;
   // one head's K and V codes of one block, padded to 64 mod 128 bytes so that
   // the copies of neighbouring heads' rows fall in different bank halves
   static constexpr int HTILE = ((KTILE + VTILE + 63) / 128) * 128 + 64;
   static constexpr int KW = D / 32;     // K words per row per thread (quarter row)
-  static constexpr int VB = D / 16;     // V bytes per row per thread (eighth row)
   static constexpr int KSTEPS = D / 16;
   static constexpr int CHR = D / 32;    // 16-byte chunks per code row
   // per slot: hg head tiles, then scales [K/V][hg][16]
@@ -314,59 +315,47 @@ __device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint8_t* p) {
   }
 }
 
-// O'^T += V^T P'^T for the thread's D/8 head dimensions, one m-tile at a time:
-// each m-tile's A fragment is (keys ka,kb; d even), (ka,kb; d odd),
-// (kc,kd; d even), (kc,kd; d odd), built by one lop3 each from byte-interleaved
-// words of the four key rows.  With CORR the block's offset correction
-// follows every m-tile's MMA.
+// O'^T += V^T P'^T.  ldmatrix.trans of an 8-key x 16-byte piece of the V
+// tile gives each lane one word holding bytes (2g, 2g+1) of keys 2cq and
+// 2cq+1, so one lop3 yields an A-fragment register (two keys, one head
+// dimension) and a shift by 8 exposes the second byte.  Chunk ch (bytes
+// [16 ch, 16 ch + 16) of each V row) feeds m-tiles 2 ch and 2 ch + 1, whose
+// rows g and g + 8 are head dimensions 32 ch + 4g + 2e and 32 ch + 4g + 2e + 1
+// (e = 0, 1; the odd ones carry the factor 16 of the high nibble).  With CORR
+// the block's offset correction follows every m-tile's MMA.
 template <int D, bool CORR>
-__device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], const uint8_t* ra, const uint8_t* rb,
-                                        const uint8_t* rc, const uint8_t* rd, uint32_t b0, uint32_t b1,
+__device__ __forceinline__ void pv_mma_chunk(float (&oacc)[D / 16][4], int ch, uint32_t r_lo, uint32_t r_hi,
+                                             uint32_t b0, uint32_t b1, const uint32_t (&vcorr)[4]) {
+  const uint32_t s_lo = r_lo >> 8, s_hi = r_hi >> 8;
+  const uint32_t a0[4] = {nib_lo(r_lo), nib_hi(r_lo), nib_lo(r_hi), nib_hi(r_hi)};
+  mma_16816(oacc[2 * ch], a0, b0, b1);
+  if constexpr (CORR) mma_16816(oacc[2 * ch], vcorr, b0, b1);
+  const uint32_t a1[4] = {nib_lo(s_lo), nib_hi(s_lo), nib_lo(s_hi), nib_hi(s_hi)};
+  mma_16816(oacc[2 * ch + 1], a1, b0, b1);
+  if constexpr (CORR) mma_16816(oacc[2 * ch + 1], vcorr, b0, b1);
+}
+
+// vaddr: shared address of this lane's ldmatrix row in chunk pair 0 (lane l
+// addresses key 8 ((l >> 3) & 1) + (l & 7) of chunk (l >> 4))
+template <int D, bool CORR>
+__device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], uint32_t vaddr, uint32_t b0, uint32_t b1,
                                         const uint32_t (&vcorr)[4]) {
-  constexpr int VB = D / 16;
-  if constexpr (VB % 4 == 0) {
-    uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
-    lds_words<VB / 4, VB>(wa, ra);
-    lds_words<VB / 4, VB>(wb, rb);
-    lds_words<VB / 4, VB>(wc, rc);
-    lds_words<VB / 4, VB>(wd, rd);
+  constexpr int CH = D / 32;  // 16-byte chunks per V row
 #pragma unroll
-    for (int k = 0; k < VB / 4; k++) {
-      uint32_t src01[4], src89[4];
-      src01[0] = __byte_perm(wa[k], wb[k], 0x5410);
-      src01[2] = __byte_perm(wa[k], wb[k], 0x7632);
-      src89[0] = __byte_perm(wc[k], wd[k], 0x5410);
-      src89[2] = __byte_perm(wc[k], wd[k], 0x7632);
-      src01[1] = src01[0] >> 8;
-      src01[3] = src01[2] >> 8;
-      src89[1] = src89[0] >> 8;
-      src89[3] = src89[2] >> 8;
-#pragma unroll
-      for (int t = 0; t < 4; t++) {
-        const uint32_t a[4] = {nib_lo(src01[t]), nib_hi(src01[t]), nib_lo(src89[t]), nib_hi(src89[t])};
-        mma_16816(oacc[4 * k + t], a, b0, b1);
-        if constexpr (CORR) mma_16816(oacc[4 * k + t], vcorr, b0, b1);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < VB / 2; k++) {
-      const uint32_t ha = reinterpret_cast<const uint16_t*>(ra)[k];
-      const uint32_t hb = reinterpret_cast<const uint16_t*>(rb)[k];
-      const uint32_t hc = reinterpret_cast<const uint16_t*>(rc)[k];
-      const uint32_t hd = reinterpret_cast<const uint16_t*>(rd)[k];
-      uint32_t src01[2], src89[2];
-      src01[0] = __byte_perm(ha, hb, 0x5410);
-      src89[0] = __byte_perm(hc, hd, 0x5410);
-      src01[1] = src01[0] >> 8;
-      src89[1] = src89[0] >> 8;
-#pragma unroll
-      for (int t = 0; t < 2; t++) {
-        const uint32_t a[4] = {nib_lo(src01[t]), nib_hi(src01[t]), nib_lo(src89[t]), nib_hi(src89[t])};
-        mma_16816(oacc[2 * k + t], a, b0, b1);
-        if constexpr (CORR) mma_16816(oacc[2 * k + t], vcorr, b0, b1);
-      }
-    }
+  for (int p = 0; p < CH / 2; p++) {
+    uint32_t r[4];
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(vaddr + p * 32));
+    pv_mma_chunk<D, CORR>(oacc, 2 * p, r[0], r[1], b0, b1, vcorr);
+    pv_mma_chunk<D, CORR>(oacc, 2 * p + 1, r[2], r[3], b0, b1, vcorr);
+  }
+  if constexpr (CH % 2) {
+    uint32_t r[2];
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(vaddr + (CH / 2) * 32));
+    pv_mma_chunk<D, CORR>(oacc, CH - 1, r[0], r[1], b0, b1, vcorr);
   }
 }
 
@@ -578,14 +567,14 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
       dst_o = pv.warp_o + slot * kDecodeCols * D;
       dst_ml = pv.warp_ml + slot * kDecodeCols * 2;
     }
-    // thread holds d = g*D/8 + r (r = 2i, and r = 2i+1 scaled by 16)
-    float* o0 = dst_o + (2 * cq) * D + g * (D / 8);
-    float* o1 = dst_o + (2 * cq + 1) * D + g * (D / 8);
+    // m-tiles 2ch, 2ch+1 hold d = 32 ch + 4g + {0, 1, 2, 3} (odd d scaled by 16)
+    float* o0 = dst_o + (2 * cq) * D + 4 * g;
+    float* o1 = dst_o + (2 * cq + 1) * D + 4 * g;
 #pragma unroll
     for (int i = 0; i < G::KSTEPS; i += 2) {
-      *reinterpret_cast<float4*>(o0 + 2 * i) =
+      *reinterpret_cast<float4*>(o0 + 16 * i) =
           make_float4(oacc[i][0], oacc[i][2] * 0.0625f, oacc[i + 1][0], oacc[i + 1][2] * 0.0625f);
-      *reinterpret_cast<float4*>(o1 + 2 * i) =
+      *reinterpret_cast<float4*>(o1 + 16 * i) =
           make_float4(oacc[i][1], oacc[i][3] * 0.0625f, oacc[i + 1][1], oacc[i + 1][3] * 0.0625f);
     }
     if (g == 0) {
@@ -599,6 +588,9 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   begin_segment();
   const int jb = (cq * NP) >> 2;  // block of this thread's score columns 2cq, 2cq+1
   const int jv = (g * NP) >> 3;   // block of this lane's P'^T column g
+  // this lane's ldmatrix row of the V tile in slot 0
+  const uint32_t v_lane = smem_addr(smem) + hl * G::HTILE + G::KTILE +
+                          (((lane >> 3) & 1) * 8 + (lane & 7)) * G::VROW + (lane >> 4) * 16;
   int cs = 0;                     // slot of the iteration's first block
   const int nunits = (int)(P1 - P0);
   // rows g (even d: offset 1032) and g + 8 (odd d: offset 1152)
@@ -708,17 +700,13 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
 
     // ---- O'^T += V^T P'^T (offset removed per position) ----
     if constexpr (NP == 1) {
-      const uint8_t* sv = smem + slot[0] * SB + hl * G::HTILE + G::KTILE + g * G::VB;
-      pv_mmas<D, true>(oacc, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW, sv + (2 * cq + 8) * G::VROW,
-                       sv + (2 * cq + 9) * G::VROW, b0, b1, vcorr);
+      pv_mmas<D, true>(oacc, v_lane + slot[0] * SB, b0, b1, vcorr);
     } else {
 #pragma unroll
       for (int j = 0; j < NP; j++) {
         // block j's probabilities only: the other blocks' columns are zero
         const uint32_t bj0 = jv == j ? b0 : 0u, bj1 = jv == j ? b1 : 0u;
-        const uint8_t* sv = smem + slot[j] * SB + hl * G::HTILE + G::KTILE + g * G::VB;
-        pv_mmas<D, false>(oacc, sv + (2 * cq) * G::VROW, sv + (2 * cq + 1) * G::VROW, sv + (2 * cq + 8) * G::VROW,
-                          sv + (2 * cq + 9) * G::VROW, bj0, bj1, vcorr);
+        pv_mmas<D, false>(oacc, v_lane + slot[j] * SB, bj0, bj1, vcorr);
       }
 #pragma unroll
       for (int i = 0; i < G::KSTEPS; i++) mma_16816(oacc[i], vcorr, b0, b1);
