@@ -64,6 +64,8 @@ extern "C" {
 #define KV_INT4_DEV_BAD_SEQ 4       /* q_len < 0, q_len > seq_len, seq_len > max_blocks_per_seq * block_size,
                                        or query_start_loc outside [0, num_q_tokens] */
 #define KV_INT4_DEV_BAD_SIGNS 8     /* a sign entry other than +1 / -1 */
+#define KV_INT4_DEV_TIMEOUT 16      /* a wait for staged input exceeded its iteration limit: the kernel
+                                       stopped early and its outputs are incomplete (not expected to occur) */
 
 /*
  * kv_int4_write -- reshape_and_cache_int4: quantise new K/V head vectors into

@@ -46,7 +46,7 @@ _SIGNATURES = {
 OK = 0
 ERR_SCRATCH_LIMIT = 9
 NOALLOC_SCRATCH_BYTES = 64 << 20
-DEV_BAD_SLOT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SIGNS = 1, 2, 4, 8
+DEV_BAD_SLOT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SIGNS, DEV_TIMEOUT = 1, 2, 4, 8, 16
 
 
 class KvInt4Error(RuntimeError):

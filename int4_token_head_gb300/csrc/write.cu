@@ -493,33 +493,30 @@ struct TcGeom {
   static constexpr int NG = D / 16;        // 16-element groups per head vector
   static constexpr int GB = B / 16;        // groups per Hadamard block
   static constexpr int WARPS = 4;
-  static constexpr int MIN_CTAS = 3;       // register budget: three CTAs per SM
   static constexpr int NT = WARPS * 32;
   static constexpr int UT = WARPS * 16;    // head vectors per tile (16 rows per warp)
-  // Staging layout (measured on GB300): for d = 128 rows padded by 16 bytes
-  // with 3 stages are fastest; for the other head sizes unpadded rows whose
-  // 16-byte chunks are XOR-swizzled, with 4 stages.  Both make the ldmatrix
-  // reads of eight rows bank-conflict free.
-  static constexpr bool SWIZZLE = D % 128 != 0;
-  static constexpr int VSTRIDE = SWIZZLE ? 2 * D : 2 * D + 16;
-  static constexpr int STAGE_BYTES = UT * VSTRIDE;
-  static constexpr int STAGES = SWIZZLE ? 4 : 3;
-  static constexpr int CHUNKS = D / 8;
-  static constexpr int OROW = D / 2 + 16;  // output staging row (bytes), padded against bank conflicts
+  static constexpr int ROWB = 2 * D;       // bytes of one bf16 head vector
+  // Staging: a warp's 16 head vectors sit in 8 pairs, each pair contiguous
+  // (one bulk copy fills it when the two vectors are neighbours in memory)
+  // and padded by 16 bytes.  MMA rows g and g + 8 are vectors 2g and 2g + 1,
+  // so the eight rows an ldmatrix reads are first (or second) vectors of
+  // eight pairs, 16 bytes apart modulo 128: no bank conflicts.  Each warp
+  // owns its rows of every stage and waits on its own barrier, so warps never
+  // wait for one another.  Stages and CTAs per SM per head size (measured on
+  // GB300: warps per SM matter more than depth).
+  static constexpr int PSTRIDE = 2 * ROWB + 16;  // bytes per staged pair
+  static constexpr int WSTAGE = 8 * PSTRIDE;     // one warp's rows of one stage
+  static constexpr int STAGES = D == 192 ? 2 : D == 96 ? 4 : 3;
+  static constexpr int MIN_CTAS = D == 192 ? 3 : 4;
+  static constexpr int STAGE_BYTES = WARPS * WSTAGE;
   static constexpr int BFRAG_BYTES = NG * 2 * 32 * 8;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BFRAG_BYTES + WARPS * 16 * OROW;
+  static constexpr int SCALE_TABLE_BYTES = 2 * 128 * 4;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BFRAG_BYTES + SCALE_TABLE_BYTES + WARPS * STAGES * 8;
 };
 
-// Physical 16-byte chunk of logical chunk c in staged row `row`.  Rows that
-// are a multiple of 128 bytes XOR the chunk with row % 8 (eight rows read by
-// one ldmatrix land in eight different bank groups); 192-byte rows (d = 96)
-// alternate bank halves, so XOR with (row / 2) % 4 inside each 64-byte group.
+// byte offset of head vector v (0..15) within a warp's stage rows
 template <int D>
-__device__ __forceinline__ int tc_swz(int row, int c) {
-  if constexpr (!TcGeom<D>::SWIZZLE) return c;
-  else if constexpr ((2 * D) % 128 == 0) return c ^ (row & 7);
-  else return c ^ ((row >> 1) & 3);
-}
+__device__ __forceinline__ int tc_vec_off(int v) { return (v >> 1) * TcGeom<D>::PSTRIDE + (v & 1) * TcGeom<D>::ROWB; }
 
 // output o (0..15) of MMA column n of n-tile t: lane c holds columns 2c, 2c+1,
 // i.e. outputs 4c + 2t and 4c + 2t + 1
@@ -532,18 +529,20 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
                 uint8_t* __restrict__ v_cache, float* __restrict__ k_scale, float* __restrict__ v_scale,
                 int64_t num_slots, int hkv, int tt_per_tile, const int8_t* __restrict__ signs, int32_t* status) {
   using G = TcGeom<D>;
-  constexpr int NG = G::NG, GB = G::GB, UT = G::UT, NT = G::NT;
-  constexpr int CPT = (UT * G::CHUNKS) / NT;  // copy chunks per thread per tile
+  constexpr int NG = G::NG, GB = G::GB, NT = G::NT;
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* stages = smem;
   uint2* sbfrag = reinterpret_cast<uint2*>(smem + G::STAGES * G::STAGE_BYTES);  // [NG][2][32]
-  uint8_t* sout = smem + G::STAGES * G::STAGE_BYTES + G::BFRAG_BYTES;           // [WARPS][16][OROW]
+  uint32_t* stab = reinterpret_cast<uint32_t*>(smem + G::STAGES * G::STAGE_BYTES + G::BFRAG_BYTES);  // [2][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
   const int units_per_token = 2 * hkv;
   const int units = tt_per_tile * units_per_token;  // <= UT
   const int num_tiles = (num_tokens + tt_per_tile - 1) / tt_per_tile;
+  // this warp's stage barriers [STAGES]
+  const uint32_t bars =
+      smem_addr(smem + G::STAGES * G::STAGE_BYTES + G::BFRAG_BYTES + G::SCALE_TABLE_BYTES) + warp * G::STAGES * 8;
 
   // B_q fragments of D_q . H_16 (columns permuted), bf16 +-1
   for (int e = tid; e < NG * 2 * 32; e += NT) {
@@ -566,49 +565,59 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
     }
     sbfrag[e] = make_uint2(w[0], w[1]);
   }
-
-  // copy slots of this thread (tile-invariant): chunk idx = tid + NT * q
-  const uint16_t* c_src[CPT];
-  int c_tok[CPT];  // token offset within the tile | K/V << 16, or -1 if unused
-#pragma unroll
-  for (int q = 0; q < CPT; q++) {
-    const int idx = tid + NT * q;
-    const int uu = idx / G::CHUNKS, c = idx % G::CHUNKS;
-    const int tt = uu / units_per_token, w = uu % units_per_token;
-    const int kv = w >= hkv, h = kv ? w - hkv : w;
-    c_tok[q] = uu < units ? tt | (kv << 16) : -1;
-    c_src[q] = (kv ? v : k) + (int64_t)tt * (kv ? v_stride : k_stride) + h * D + c * 8;
+  // Scale tables.  absmax is a bf16 value (1 + m/128) 2^e, so
+  // s = fp32(absmax / 7) = fp32((1 + m/128) / 7) 2^e and fp32(1 / s) =
+  // fp32(1 / fp32((1 + m/128) / 7)) 2^-e exactly (all normal numbers above
+  // the flush bound): one correctly rounded division and reciprocal per m.
+  if (tid < 128) {
+    const float t7 = __fdiv_rn(1.0f + (float)tid * 0.0078125f, 7.0f);
+    stab[tid] = __float_as_uint(t7);
+    stab[128 + tid] = __float_as_uint(__frcp_rn(t7));
   }
-  const int64_t k_tile_stride = (int64_t)tt_per_tile * k_stride, v_tile_stride = (int64_t)tt_per_tile * v_stride;
-  auto issue = [&](int tile, int stage) {
-    const uint32_t dst0 = smem_addr(stages + stage * G::STAGE_BYTES);
-    const int t0 = tile * tt_per_tile;
-#pragma unroll
-    for (int q = 0; q < CPT; q++) {
-      const int idx = tid + NT * q;
-      const int uu = idx / G::CHUNKS, c = idx % G::CHUNKS;
-      if (c_tok[q] >= 0 && t0 + (c_tok[q] & 0xffff) < num_tokens) {
-        const uint16_t* src = c_src[q] + (int64_t)tile * ((c_tok[q] >> 16) ? v_tile_stride : k_tile_stride);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst0 + uu * G::VSTRIDE + tc_swz<D>(uu, c) * 16),
-                     "l"(src));
-      }
-    }
+  if (lane == 0) {
+    for (int s = 0; s < G::STAGES; s++) mbar_init(bars + 8 * s, 1);
+    fence_mbar_init();
+  }
+
+  // copies: lane cv < 16 owns head vector warp * 16 + cv of every tile.  With
+  // an even head count the two vectors of a pair are neighbouring heads of
+  // one token, so the even lane copies both with one bulk copy.
+  const bool paired = (hkv & 1) == 0;
+  const int cv = lane & 15;
+  const int cu = warp * 16 + cv;
+  const bool c_used = lane < 16 && cu < units && (!paired || (cv & 1) == 0);
+  const int c_tt = cu / units_per_token, c_w = cu % units_per_token;
+  const int c_kv = c_w >= hkv, c_h = c_kv ? c_w - hkv : c_w;
+  const uint16_t* const c_src = (c_kv ? v : k) + (int64_t)c_tt * (c_kv ? v_stride : k_stride) + c_h * D;
+  const int64_t c_tstride = (int64_t)tt_per_tile * (c_kv ? v_stride : k_stride);
+  const uint32_t c_dst = smem_addr(stages + warp * G::WSTAGE + tc_vec_off<D>(cv));
+  const uint32_t c_bytes = paired ? 2 * G::ROWB : G::ROWB;
+  auto issue = [&](int tl, int stage) {
+    const bool go = c_used && tl * tt_per_tile + c_tt < num_tokens;
+    const unsigned m = __ballot_sync(0xffffffffu, go);
+    const uint32_t bar = bars + 8 * stage;
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(m) * c_bytes);
+    __syncwarp();
+    if (go) bulk_g2s(c_dst + stage * G::STAGE_BYTES, c_src + (int64_t)tl * c_tstride, c_bytes, bar);
   };
 
-  // this thread's two rows (head vectors) within the warp's 16: g and g + 8
+  // this thread's two MMA rows g and g + 8 are head vectors 2g and 2g + 1
   int r_tt[2], r_kv[2], r_h[2];
 #pragma unroll
   for (int rr = 0; rr < 2; rr++) {
-    const int uu = warp * 16 + g + 8 * rr;
+    const int uu = warp * 16 + 2 * g + rr;
     r_tt[rr] = uu < units ? uu / units_per_token : -1;
     const int w = uu % units_per_token;
     r_kv[rr] = w >= hkv;
     r_h[rr] = r_kv[rr] ? w - hkv : w;
   }
-  // ldmatrix row for this lane: matrices (rows 0-7|8-15) x (k 0-7|8-15)
-  const int a_row = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  // ldmatrix row for this lane: matrices (rows 0-7|8-15) x (k 0-7|8-15);
+  // MMA row m is vector 2 (m & 7) + (m >> 3)
+  const int a_m = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int a_off = warp * G::WSTAGE + tc_vec_off<D>(2 * (a_m & 7) + (a_m >> 3));
   const int a_half = lane >> 4;  // which 16-byte half of a 16-element group
-  uint8_t* const wout = sout + warp * 16 * G::OROW;
+
+  __syncthreads();  // B fragments, scale tables and barrier initialisation visible
 
   int tile = blockIdx.x;
   const int tstep = gridDim.x;
@@ -616,7 +625,6 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
   for (int s = 0; s < G::STAGES - 1; s++) {
     const int tt = tile + s * tstep;
     if (tt < num_tiles) issue(tt, s);
-    cp_async_commit();
   }
   // slots of this thread's rows, loaded one tile ahead
   auto load_slots = [&](int tl, int64_t (&sl)[2]) {
@@ -628,22 +636,27 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
   };
   int64_t next_slot[2];
   load_slots(tile, next_slot);
-  __syncthreads();  // B fragments visible
 
   int stage = 0;
+  uint32_t phase = 0;  // bit s: parity of stage s's next completion
+  bool stalled = false;
 #pragma unroll 1
   for (; tile < num_tiles; tile += tstep) {
     int64_t r_slot[2] = {next_slot[0], next_slot[1]};
     load_slots(tile + tstep, next_slot);
-    cp_async_wait<G::STAGES - 2>();
-    __syncthreads();  // this tile's copies visible; every warp is past the previous tile's MMAs
     {
+      // refill the stage this warp finished with at its previous tile
       const int tn = tile + (G::STAGES - 1) * tstep;
-      if (tn < num_tiles) issue(tn, (stage + G::STAGES - 1) % G::STAGES);
-      cp_async_commit();
+      if (tn < num_tiles) issue(tn, stage == 0 ? G::STAGES - 1 : stage - 1);
     }
+    if (!mbar_wait_bounded(bars + 8 * stage, (phase >> stage) & 1)) {
+      stalled = true;
+      break;
+    }
+    phase ^= 1u << stage;
 
-    const uint8_t* sa = stages + stage * G::STAGE_BYTES + a_row * G::VSTRIDE;
+    uint8_t* const wbase = stages + stage * G::STAGE_BYTES + warp * G::WSTAGE;
+    const uint8_t* sa = stages + stage * G::STAGE_BYTES + a_off;
     uint32_t pk[2][NG][2];  // [n-tile][group][row g / row g+8]: bf16x2 of outputs (4c+2t, 4c+2t+1)
 #pragma unroll
     for (int t = 0; t < 2; t++) {
@@ -651,7 +664,7 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
 #pragma unroll
       for (int q = 0; q < NG; q++) {
         uint32_t a[4];
-        ldmatrix_x4(a, sa + tc_swz<D>(a_row, 2 * q + a_half) * 16);
+        ldmatrix_x4(a, sa + (2 * q + a_half) * 16);
         const uint2 bf = sbfrag[(q * 2 + t) * 32 + lane];
         mma_16816_bf16_z(cacc[q], a, bf.x, bf.y);
       }
@@ -684,7 +697,8 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
         r_slot[rr] = -1;
       }
     }
-    // per row: absmax over the 4 lanes of the quad, scale, codes
+    // per row: absmax over the 4 lanes of the quad, scale, codes.  The codes
+    // are staged in the row's own (already consumed) input bytes.
 #pragma unroll
     for (int rr = 0; rr < 2; rr++) {
       uint32_t am = 0;
@@ -698,11 +712,18 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
       const float amax = __uint_as_float(a16 << 16);
       float sc = 0.f, r = 0.f;
       if (amax >= kFlushAbsmax) {
-        sc = __fdiv_rn(amax, 7.0f);
-        r = __frcp_rn(sc);
+        if (a16 < 0x7f80u) {
+          const uint32_t m = a16 & 0x7fu;
+          const int e = (int)(a16 >> 7) - 127;
+          sc = __uint_as_float(stab[m] + (uint32_t)(e << 23));
+          r = __uint_as_float(stab[128 + m] - (uint32_t)(e << 23));
+        } else {  // inf / NaN input
+          sc = __fdiv_rn(amax, 7.0f);
+          r = __frcp_rn(sc);
+        }
       }
       const float2 r2 = make_float2(r, r), magic2 = make_float2(kCodeMagic, kCodeMagic);
-      uint8_t* orow = wout + (g + 8 * rr) * G::OROW;
+      uint8_t* orow = wbase + tc_vec_off<D>(2 * g + rr);
 #pragma unroll
       for (int q = 0; q < NG; q++) {
         uint32_t bytes[2];
@@ -726,13 +747,23 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
       uint8_t* dst = (r_kv[rr] ? v_cache : k_cache) + (r_slot[rr] * hkv + r_h[rr]) * (int64_t)(D / 2);
 #pragma unroll
       for (int ch = cq; ch < CPR; ch += 4)
-        *reinterpret_cast<uint4*>(dst + ch * 16) =
-            *reinterpret_cast<const uint4*>(wout + (g + 8 * rr) * G::OROW + ch * 16);
+        *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(wbase + tc_vec_off<D>(2 * g + rr) + ch * 16);
     }
-    __syncwarp();  // the warp's output staging may now be reused
-    stage = (stage + 1) % G::STAGES;
+    // this tile's shared-memory reads and writes come before the bulk copy
+    // that refills the stage at the next tile
+    fence_proxy_async_smem();
+    __syncwarp();
+    stage = stage + 1 == G::STAGES ? 0 : stage + 1;
   }
-  cp_async_wait<0>();
+  if (stalled) {
+    // report, then let the copies this warp still has in flight land (each
+    // wait again bounded) before the CTA's shared memory is released
+    if (lane == 0) flag(status, KV_INT4_DEV_TIMEOUT);
+    for (int j = 0; j < G::STAGES; j++) {  // tiles tile .. tile + (STAGES - 1) * tstep
+      const int sj = (stage + j) % G::STAGES;
+      if (tile + j * tstep < num_tiles && !mbar_wait_bounded(bars + 8 * sj, (phase >> sj) & 1)) break;
+    }
+  }
 }
 
 template <int D, bool PREROT>
