@@ -43,6 +43,7 @@ if ROOT not in sys.path:
 METRIC = "INT4-KV paged decode: KV-read GB/s vs HBM peak, tokens/s; RHT+quant write GB/s"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TC_TFLOPS = 1700.0  # dense bf16, sustained, one earlier GB300 measurement
 WORKLOAD_TEXT = {
     "tiny": "tiny causal: 4 q / 4 kv heads, head 128, block 16, seqs (q,kv) = (4,128),(4,97)",
     "phi3": "Phi-3-mini decode: 32 q / 32 kv heads, head 96 (b=32, n=3), block 16, batch 32 x kv 1024, 1% outlier channels x8",
@@ -106,13 +107,24 @@ def aggregate_throughput(units_per_rank: float, world: int, seconds_max: float) 
 # measurement helpers
 # ---------------------------------------------------------------------------
 def load_peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s sustained, source) from MEASURED_PEAKS.json."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", FALLBACK_TC_TFLOPS)), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_HBM_GBS, FALLBACK_TC_TFLOPS, "fallback"
+
+
+def decode_columns(w) -> int:
+    """Query columns per key block of the decode kernel, as the library picks
+    them: q_len * G of the longest query when every sequence fits in 8 columns,
+    else G (longer queries go to prefill); two blocks share the 8 MMA columns
+    when that count is at most 4."""
+    mq = max(1, w.max_query_len) * w.group
+    cols = mq if mq <= 8 else w.group
+    return 4 if cols <= 4 else 8
 
 
 def source_sha(path: str) -> str:
@@ -403,22 +415,33 @@ def run_ours(args):
         raise RuntimeError(f"device status {pk.status.item()} during the timed region")
 
     # ---- roofline of the dominant kernel ----
-    peak, peak_kind = load_peaks()
+    peak, tc_peak, peak_kind = load_peaks()
     dom = max(("decode", "prefill"), key=lambda k: kern[k][0])
     dom_ms, dom_n, _ = kern[dom]
     d, hkv, hq = w.head_size, w.num_kv_heads, w.num_q_heads
+    dcols = decode_columns(w)
+    is_dec = lambda ql: w.group <= dcols and ql * w.group <= dcols
+    launch_s = dom_ms / dom_n / 1e3 if dom_n else None
     if dom == "decode":
-        seqs = [(ql, kv) for ql, kv in w.seqs if ql * w.group <= 8 and w.group <= 8]
+        seqs = [(ql, kv) for ql, kv in w.seqs if is_dec(ql)]
+        algo = sum(kv * hkv * 2 * (d // 2 + 4) + 4 * ((kv + 15) // 16) + ql * hq * d * 2 for ql, kv in seqs)
+        achieved = algo / launch_s / 1e9 if launch_s else None
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
+                    "traffic": recorded_traffic(dom, args.workload), "kernel": "decode_kernel",
+                    "peak_source": f"{peak_kind} (HBM copy)", "algorithmic_bytes_per_launch": algo}
     else:
-        seqs = [(ql, kv) for ql, kv in w.seqs if not (ql * w.group <= 8 and w.group <= 8)]
-    algo = sum(kv * hkv * 2 * (d // 2 + 4) + 4 * ((kv + 15) // 16) + ql * hq * d * 2 for ql, kv in seqs)
-    achieved = algo / (dom_ms / dom_n / 1e3) / 1e9 if dom_n else None
-    traffic = recorded_traffic(dom, args.workload)
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": peak,
-                "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
-                "traffic": traffic, "kernel": f"{dom}_kernel", "peak_source": f"{peak_kind} (HBM copy)",
-                "algorithmic_bytes_per_launch": algo,
-                "avg_launch_ms": round(dom_ms / dom_n, 5) if dom_n else None}
+        # a dense contraction: QK^T and PV over the visible (query, key) pairs
+        seqs = [(ql, kv) for ql, kv in w.seqs if not is_dec(ql)]
+        pairs = sum((ql * (kv - ql) + ql * (ql + 1) // 2) if w.causal else ql * kv for ql, kv in seqs)
+        flops = 4 * d * hq * pairs
+        achieved = flops / launch_s / 1e12 if launch_s else None
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2) if achieved else None, "peak": tc_peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4) if achieved else None,
+                    "traffic": recorded_traffic(dom, args.workload), "kernel": "prefill_kernel",
+                    "peak_source": f"{peak_kind} bf16 dense, sustained (cuBLAS); f16 has the same nominal rate",
+                    "algorithmic_flops_per_launch": flops}
+    roofline["avg_launch_ms"] = round(dom_ms / dom_n, 5) if dom_n else None
 
     # whole-attention and write throughput
     attn_bytes = pk.kv_bytes_read()
