@@ -35,6 +35,7 @@
 // skipped, and a KV_INT4_DEV_* bit is ORed into the caller's status word.
 
 #include <float.h>
+#include <limits.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -44,10 +45,10 @@ namespace kvint4 {
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PlanView {
-  int32_t* plan;      // [0] n_dseq, [1] n_prefill_items, [2] prefill work counter
+  int32_t* plan;      // [0] n_dseq, [1] n_prefill_items, [2] prefill work counter, [3] n_pseq
   int32_t* dseq;
   int64_t* dprefix;
-  int4* pitems;       // (seq, kv_head, tile, key blocks)
+  int2* ptab;         // prefill sequences in order: (seq id, index of its first item); [n_pseq].y = items
   __half* qrot;
   float* direct_o;
   float* direct_ml;
@@ -61,7 +62,7 @@ static PlanView plan_view(void* ws, const WorkspaceLayout& L) {
   v.plan = reinterpret_cast<int32_t*>(b + L.plan);
   v.dseq = reinterpret_cast<int32_t*>(b + L.dseq);
   v.dprefix = reinterpret_cast<int64_t*>(b + L.dprefix);
-  v.pitems = reinterpret_cast<int4*>(b + L.pitems);
+  v.ptab = reinterpret_cast<int2*>(b + L.pitems);
   v.qrot = reinterpret_cast<__half*>(b + L.qrot);
   v.direct_o = reinterpret_cast<float*>(b + L.direct_o);
   v.direct_ml = reinterpret_cast<float*>(b + L.direct_ml);
@@ -143,8 +144,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
   if (blockIdx.x == 0) {
     __shared__ int32_t s_i32[kPrepThreads / 32];
     __shared__ long long s_i64[kPrepThreads / 32];
-    int n_dseq = 0, n_items = 0;
-    long long dpre = 0;
+    int n_dseq = 0, n_pseq = 0;
+    long long dpre = 0, n_items = 0;
     for (int base = 0; base < c.num_seqs; base += kPrepThreads) {
       const int s = base + threadIdx.x;
       int kind = 0, nblk = 0, ntiles = 0, ql = 0, L = 0;
@@ -162,74 +163,76 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
           if (kind == 2) ntiles = (ql + c.tile_tokens - 1) / c.tile_tokens;
         }
       }
-      int tot_a;
-      long long tot_b;
-      int tot_c;
+      int tot_a, tot_p;
+      long long tot_b, tot_c;
       const int ex_a = block_exclusive_scan<int>(kind == 1, &tot_a, s_i32);
       const long long ex_b = block_exclusive_scan<long long>(kind == 1 ? (nblk + c.np - 1) / c.np : 0, &tot_b, s_i64);
-      const int ex_c = block_exclusive_scan<int>(ntiles, &tot_c, s_i32);
+      const int ex_p = block_exclusive_scan<int>(kind == 2, &tot_p, s_i32);
+      const long long ex_c = block_exclusive_scan<long long>((long long)ntiles * c.hkv, &tot_c, s_i64);
       if (kind == 1) {
         pv.dseq[n_dseq + ex_a] = s;
         pv.dprefix[n_dseq + ex_a] = dpre + ex_b;
       } else if (kind == 2) {
-        const int ctx = L - ql;
-        for (int t = 0; t < ntiles; t++) {
-          int keys = L;
-          if (c.causal) {
-            const int last = min(ql, (t + 1) * c.tile_tokens) - 1;  // last query of the tile
-            keys = ctx + last + 1;
-          }
-          const int nkb = (keys + 15) / 16;
-          // tiles in descending order of work within a sequence
-          const long long slot = (long long)n_items + (long long)(ex_c + (ntiles - 1 - t)) * c.hkv;
-          if (slot + c.hkv > c.max_items) {  // only reachable with inconsistent query_start_loc
-            flag(c.status, KV_INT4_DEV_BAD_SEQ);
-            continue;
-          }
-          for (int h = 0; h < c.hkv; h++) pv.pitems[slot + h] = make_int4(s, h, t, nkb);
-        }
+        // the prefill kernel expands (tile, kv head) items from this table
+        pv.ptab[n_pseq + ex_p] = make_int2(s, (int)min(n_items + ex_c, (long long)INT_MAX));
       }
       n_dseq += tot_a;
       dpre += tot_b;
-      n_items += tot_c * c.hkv;
+      n_pseq += tot_p;
+      n_items += tot_c;
     }
     if (threadIdx.x == 0) {
       pv.dprefix[n_dseq] = dpre;
       pv.plan[0] = n_dseq;
-      // an overflowing list (inconsistent metadata, already flagged) is dropped whole
-      pv.plan[1] = (long long)n_items > c.max_items ? 0 : n_items;
+      // more items than the workspace was sized for only happens with
+      // inconsistent query_start_loc: the prefill part is dropped and flagged
+      const bool over = n_items > c.max_items || n_items > INT_MAX;
+      if (over) flag(c.status, KV_INT4_DEV_BAD_SEQ);
+      pv.ptab[n_pseq] = make_int2(-1, over ? 0 : (int)n_items);
+      pv.plan[1] = over ? 0 : (int)n_items;
       pv.plan[2] = 0;
+      pv.plan[3] = n_pseq;
     }
     return;
   }
 
-  // query rotation: one warp per (token, q head) row
-  __shared__ float srow[kPrepRowsPerCta][D];
+  // query rotation: one warp per (token, q head) row, held in registers
+  // (lane owns elements lane + 32k); butterfly stages h < 32 pair lanes,
+  // stages h >= 32 pair the lane's own registers
   constexpr int B = Head<D>::b;
+  constexpr int PER = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = (long long)(blockIdx.x - 1) * kPrepRowsPerCta + warp;
   if (row >= (long long)c.num_q_tokens * c.hq) return;
   const long long t = row / c.hq;
   const int h = (int)(row - t * c.hq);
   const uint16_t* src = c.q + t * c.q_stride + (long long)h * D;
-  float* r = srow[warp];
-  for (int i = lane; i < D; i += 32) {
-    const float x = __uint_as_float((uint32_t)src[i] << 16);
-    r[i] = c.signs[i] < 0 ? -x : x;
+  float x[PER];
+#pragma unroll
+  for (int k = 0; k < PER; k++) {
+    const float v = __uint_as_float((uint32_t)src[lane + 32 * k] << 16);
+    x[k] = c.signs[lane + 32 * k] < 0 ? -v : v;
   }
-  __syncwarp();
-#pragma unroll 1
-  for (int hh = 1; hh < B; hh <<= 1) {
-    for (int p = lane; p < D / 2; p += 32) {
-      const int i = (p / hh) * 2 * hh + (p % hh);
-      const float a = r[i], b = r[i + hh];
-      r[i] = a + b;
-      r[i + hh] = a - b;
+#pragma unroll
+  for (int hh = 1; hh < B && hh < 32; hh <<= 1) {
+    const float f = (lane & hh) ? -1.f : 1.f;  // upper element: partner - self
+#pragma unroll
+    for (int k = 0; k < PER; k++) x[k] = fmaf(f, x[k], __shfl_xor_sync(0xffffffffu, x[k], hh));
+  }
+#pragma unroll
+  for (int m = 1; 32 * m < B; m <<= 1) {
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+      if ((k & m) == 0) {
+        const float a0 = x[k], b0 = x[k + m];
+        x[k] = a0 + b0;
+        x[k + m] = a0 - b0;
+      }
     }
-    __syncwarp();
   }
   __half* dst = pv.qrot + row * D;
-  for (int i = lane; i < D; i += 32) dst[i] = __float2half_rn(r[i] * c.qscale);
+#pragma unroll
+  for (int k = 0; k < PER; k++) dst[lane + 32 * k] = __float2half_rn(x[k] * c.qscale);
 }
 
 // ---------------------------------------------------------------------------
@@ -781,13 +784,22 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
     }
   };
   merge_slot(pv.direct_o + (long long)seg * kDecodeCols * D, pv.direct_ml + (long long)seg * kDecodeCols * 2);
-  // CTAs whose (non-empty) range starts strictly inside this segment
-  long long w = (sbeg * W) / Tu;
-  while (w < W && wstart(w) <= sbeg) w++;
-  for (; w < W && wstart(w) < send; w++) {
-    if (wstart(w + 1) <= wstart(w)) continue;
+  // the other pieces: CTAs whose non-empty range starts strictly inside the
+  // segment.  Walk the CTAs or the positions, whichever are fewer.
+  auto merge_cta = [&](long long w) {
     const long long slot = w * c.hg + hl;
     merge_slot(pv.warp_o + slot * kDecodeCols * D, pv.warp_ml + slot * kDecodeCols * 2);
+  };
+  const long long w_first = ((sbeg + 1) * W + Tu - 1) / Tu;  // first CTA starting after sbeg
+  const long long w_end = (send * W + Tu - 1) / Tu;          // first CTA starting at or after send
+  if (w_end - w_first <= send - sbeg - 1) {
+    for (long long w = w_first; w < w_end; w++)
+      if (wstart(w + 1) > wstart(w)) merge_cta(w);
+  } else {
+    for (long long p = sbeg + 1; p < send; p++) {
+      const long long w = ((p + 1) * W + Tu - 1) / Tu - 1;  // last CTA starting at or before p
+      if (wstart(w) == p) merge_cta(w);
+    }
   }
   float* r = srow[col];
   const float inv = 1.f / (Lsum * (float)B);
@@ -851,16 +863,34 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
   for (int i = tid; i < D; i += G::THREADS) ssign[i] = c.signs[i] < 0 ? -1.f : 1.f;
-  const int n_items = pv.plan[1];
+  const int n_items = pv.plan[1], n_pseq = pv.plan[3];
 
 #pragma unroll 1
   while (true) {
-    if (tid == 0) sitem[0] = atomicAdd(&pv.plan[2], 1);
+    if (tid == 0) {
+      // next item: (prefill sequence, tile in descending order of work, kv head)
+      const int itn = atomicAdd(&pv.plan[2], 1);
+      int4 it = make_int4(-1, 0, 0, 0);
+      if (itn < n_items) {
+        int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pv.ptab[mid].y <= itn) lo = mid;
+          else hi = mid;
+        }
+        const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
+        const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
+        const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
+        const int t = ntiles - 1 - r / c.hkv;
+        const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
+        it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
+      }
+      sitem[0] = it.x; sitem[1] = it.y; sitem[2] = it.z; sitem[3] = it.w;
+    }
     __syncthreads();
-    const int itn = sitem[0];
+    const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
     __syncthreads();
-    if (itn >= n_items) break;
-    const int4 item = pv.pitems[itn];
+    if (item.x < 0) break;
     const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
     const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
     const int L = c.seq_lens[seq], ctx = L - ql;
