@@ -254,6 +254,35 @@ def bulk_write_bench(w, dev, n_chunks: int, chunk_tokens: int = 65536):
             "tokens_per_chunk": chunk_tokens, "bytes_per_chunk": nbytes}
 
 
+def rht_bench(w, dev, n_chunks: int, chunk_tokens: int = 65536):
+    """Standalone rotation (kv_int4_rht) throughput: n_chunks pre-drawn
+    65,536-token x Hkv-head bf16 K chunks rotated to bf16, back to back;
+    one warm-up pass, then device time of a second pass by CUDA events.
+    Algorithmic bytes: bf16 in + bf16 out."""
+    import torch
+    from int4_token_head_gb300 import _lib
+    hkv, d = w.num_kv_heads, w.head_size
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed * 7 + 5)
+    xs = [torch.randn((chunk_tokens * hkv, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_chunks)]
+    ys = [torch.empty_like(x) for x in xs]
+    signs = w.signs.to(dev)
+    for x, y in zip(xs, ys):
+        _lib.rht(x, signs, out=y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for x, y in zip(xs, ys):
+        _lib.rht(x, signs, out=y)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n_chunks
+    nbytes = chunk_tokens * hkv * d * 2 * 2
+    del xs, ys
+    return {"gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "ms_per_chunk": round(ms, 4), "chunks": n_chunks,
+            "rows_per_chunk": chunk_tokens * hkv, "bytes_per_chunk": nbytes}
+
+
 # ---------------------------------------------------------------------------
 # the oracle on host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -348,6 +377,7 @@ def run_ours(args):
     pk.populate_history(chunk_tokens=65536)
     torch.cuda.synchronize()
     write_info = bulk_write_bench(w, dev, args.write_chunks)
+    rht_info = rht_bench(w, dev, max(1, args.write_chunks))
     q, k_new, v_new, slots = pk.step_inputs()
     out = torch.empty((w.num_q_tokens, w.num_q_heads, w.head_size), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
@@ -448,6 +478,7 @@ def run_ours(args):
     attn_ms = sum(kern[k][0] for k in ("prep", "prefill", "decode", "reduce")) / args.steps
     write_info["frac"] = round(write_info["gbs"] / peak, 4)
     write_info["step_write_us"] = round(kern["write"][0] / max(1, kern["write"][1]) * 1e3, 2)
+    rht_info["frac"] = round(rht_info["gbs"] / peak, 4)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -462,6 +493,7 @@ def run_ours(args):
         "roofline": roofline,
         "kv_read_gbs": round(attn_bytes / (attn_ms / 1e3) / 1e9, 1) if attn_ms else None,
         "write": write_info,
+        "rht": rht_info,
         "kernels_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in kern.items()},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(sum(v[1] for v in kern.values())),

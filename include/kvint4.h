@@ -218,6 +218,42 @@ KVINT4_API int kv_int4_attention_noalloc(const void* q, int64_t q_token_stride,
                                          int32_t* dev_status, void* stream);
 
 /*
+ * kv_int4_rht -- the block-diagonal randomized Hadamard rotation on its own:
+ * the rotation the write path applies to K and V before quantising them (the
+ * pages' single_rht step), and its inverse.
+ *
+ * Defined by: "vLLM -- Attention Kernels & KV Cache Quantization" (PR
+ * #56198), Merged contribution: with b the largest power-of-two divisor of
+ * head_size d and n = d / b, H_b (unnormalised Sylvester Walsh-Hadamard,
+ * H_b H_b^T = b I) acts on each of the n contiguous blocks of b elements;
+ * "Rotate KV into RHT domain in the INT4 unified attn test" (PR #62881),
+ * Details / Root cause: the random +-1 diagonal D is applied first.
+ *
+ *   inverse == 0:  y = (I_n (x) H_b) . D . x
+ *   inverse != 0:  y = D . (I_n (x) H_b) . x / b      (so rht(rht(x), inverse) = x)
+ *
+ * Arithmetic in fp32 (one rounding per butterfly stage); the result is
+ * stored as bf16 (round to nearest even) or, with y_f32 != 0, as fp32.  Any
+ * head_size in [1, 4096] (odd d gives b = 1: y = D x, resp. D y).
+ *
+ * x        device, bf16 [num_rows][head_size], row stride x_row_stride
+ *          elements (>= head_size), 2-byte aligned
+ * y        device, [num_rows][head_size] bf16 (y_f32 == 0) or fp32, row
+ *          stride y_row_stride elements (>= head_size), naturally aligned;
+ *          must not overlap x
+ * signs    device, int8 [head_size], entries +1 / -1 (anything < 0 counts as -1)
+ * stream   a cudaStream_t (NULL: the legacy default stream)
+ *
+ * Returns KV_INT4_OK after enqueueing one kernel (nothing for num_rows == 0),
+ * KV_INT4_ERR_NULL for a NULL x, y or signs with num_rows > 0,
+ * KV_INT4_ERR_HEAD_SIZE for head_size outside [1, 4096], KV_INT4_ERR_ALIGN
+ * for a misaligned pointer or a row stride below head_size, KV_INT4_ERR_SIZE
+ * for num_rows < 0, KV_INT4_ERR_CUDA if the launch failed.
+ */
+KVINT4_API int kv_int4_rht(const void* x, int64_t x_row_stride, void* y, int64_t y_row_stride, int y_f32,
+                           int64_t num_rows, int head_size, const int8_t* signs, int inverse, void* stream);
+
+/*
  * Kernel timing for benchmarks (off by default, per host thread; not part of
  * the method).  While enabled on the calling thread, every kv_int4_write and
  * kv_int4_attention call records a pair of CUDA events on its stream around

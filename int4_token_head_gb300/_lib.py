@@ -37,6 +37,7 @@ _SIGNATURES = {
                                           c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
                                           c_int, c_int, c_int, c_float, c_int, c_void_p, c_void_p, c_int64,
                                           c_void_p, c_void_p]),
+    "kv_int4_rht": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_int, c_int64, c_int, c_void_p, c_int, c_void_p]),
     "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
     "kv_int4_timing_enable": (c_int, [c_int]),
     "kv_int4_timing_collect": (c_int, [c_void_p, c_void_p, c_void_p]),
@@ -144,6 +145,33 @@ def write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, signs,
                                  _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                  nb, bs, hkv, d, _ptr(signs), _ptr(dev_status), _stream(stream))
         _raise(code, "kv_int4_write")
+
+
+def rht(x, signs, inverse: bool = False, out: Optional[torch.Tensor] = None,
+        out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """The block-diagonal randomized Hadamard rotation through kv_int4_rht.
+
+    x: bf16 [..., d] with a contiguous last dimension (rows may be strided);
+    forward y = (I_n (x) H_b) D x, inverse y = D (I_n (x) H_b) x / b.  The
+    result (bf16 or float32, shape of x) is written to `out` if given."""
+    _check(x.dtype == torch.bfloat16, "x must be bfloat16")
+    _check(x.dim() >= 1 and x.stride(-1) == 1, "x must have a contiguous last dimension")
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    x2 = x.reshape(rows, d) if x.dim() != 2 else x
+    _check(signs.dtype == torch.int8 and signs.numel() == d and signs.is_contiguous(), "signs must be int8 [d]")
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    _check(out.dtype in (torch.bfloat16, torch.float32), "out must be bfloat16 or float32")
+    _check(tuple(out.shape) == tuple(x.shape) and out.stride(-1) == 1, "out must match x's shape, last dim contiguous")
+    o2 = out.reshape(rows, d) if out.dim() != 2 else out
+    _check(o2.data_ptr() == out.data_ptr(), "out must be viewable as rows")
+    xs = x2.stride(0) if rows > 1 else d
+    ys = o2.stride(0) if rows > 1 else d
+    code = load().kv_int4_rht(_ptr(x2), xs, _ptr(o2), ys, int(out.dtype == torch.float32), rows, d, _ptr(signs),
+                              int(bool(inverse)), _stream(stream))
+    _raise(code, "kv_int4_rht")
+    return out
 
 
 TIMED_KINDS = ("write", "prep", "prefill", "decode", "reduce")

@@ -130,3 +130,20 @@ def test_attention_validation(lib):
     assert _attn(lib, ws=ctypes.c_void_p(0x10010)) == D["KV_INT4_ERR_ALIGN"]
     assert _attn(lib, qs=32 * 128 + 2) == D["KV_INT4_ERR_ALIGN"]
     assert _attn(lib, ns=-3) == D["KV_INT4_ERR_SIZE"]
+
+
+def test_rht_validation(lib):
+    def rht(x=FAKE, xs=128, y=FAKE, ys=128, f32=0, rows=4, d=128, signs=FAKE, inv=0):
+        return lib.kv_int4_rht(x, xs, y, ys, f32, rows, d, signs, inv, None)
+    assert rht(rows=0) == D["KV_INT4_OK"]              # nothing to do, nothing touched
+    assert rht(rows=0, x=None, y=None, signs=None) == D["KV_INT4_OK"]
+    assert rht(rows=-1) == D["KV_INT4_ERR_SIZE"]
+    assert rht(d=0) == D["KV_INT4_ERR_HEAD_SIZE"]
+    assert rht(d=4097) == D["KV_INT4_ERR_HEAD_SIZE"]
+    assert rht(x=None) == D["KV_INT4_ERR_NULL"]
+    assert rht(y=None) == D["KV_INT4_ERR_NULL"]
+    assert rht(signs=None) == D["KV_INT4_ERR_NULL"]
+    assert rht(x=ctypes.c_void_p(0x10001)) == D["KV_INT4_ERR_ALIGN"]
+    assert rht(y=ctypes.c_void_p(0x10002), f32=1) == D["KV_INT4_ERR_ALIGN"]
+    assert rht(xs=127) == D["KV_INT4_ERR_ALIGN"]
+    assert rht(ys=100) == D["KV_INT4_ERR_ALIGN"]

@@ -74,6 +74,40 @@ def test_prerotated_codes_and_scales_bit_exact(d):
             assert np.array_equal(a, b), name
 
 
+@pytest.mark.parametrize("d", [64, 96, 128, 192])
+def test_write_scale_and_codes_exact_over_all_absmax_mantissas(d):
+    """Head vectors with a single nonzero entry c: every rotated element is
+    +-c exactly (on both sides), so the absmax is |c| and the scale must be
+    fp32(|c| / 7) bit for bit, with codes +-7.  c sweeps all 128 bf16
+    mantissas over exponents from below the flush bound (2^-120) to 2^126."""
+    hkv = 4
+    exps = [-121, -120, -119, -100, -30, -1, 0, 1, 7, 40, 100, 126]
+    vals = np.array([(1 + m / 128) * 2.0 ** e * (1 if (m + e) % 2 else -1) for e in exps for m in range(128)])
+    n = len(vals)
+    T = (n + hkv - 1) // hkv
+    g = torch.Generator().manual_seed(d)
+    k = torch.zeros((T, hkv, d), dtype=torch.float64)
+    v = torch.zeros((T, hkv, d), dtype=torch.float64)
+    perm = torch.randperm(n, generator=g).numpy()
+    for u in range(T * hkv):
+        t, h = divmod(u, hkv)
+        k[t, h, (7 * u + 3) % d] = float(vals[u % n])
+        v[t, h, (5 * u + 1) % d] = float(vals[perm[u % n]])
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    assert np.array_equal(k.double().numpy().sum(axis=2).ravel()[:n], vals)  # every c is a bf16 value
+    nb = (T + 15) // 16 + 3
+    slots = torch.randperm(nb * 16, generator=g)[:T].to(torch.int64)
+    signs = _signs(d, 5)
+    got, status = _run_gpu_write(k, v, slots, nb, signs)
+    ref = _oracle_write(k, v, slots, nb, signs)
+    assert status == 0
+    for a, b, name in zip(got, ref, ["k_cache", "v_cache", "k_scale", "v_scale"]):
+        if a.dtype == np.float32:
+            assert np.array_equal(f32_bits(a), f32_bits(b)), name
+        else:
+            assert np.array_equal(a, b), name
+
+
 @pytest.mark.parametrize("d", HEADS)
 def test_write_end_to_end_within_one_code(d):
     """Raw bf16 K/V -> rotation in fp32 on the GPU vs fp64 in the oracle:
