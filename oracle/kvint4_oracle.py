@@ -239,19 +239,24 @@ def dequantize_original(codes, scales, signs) -> np.ndarray:
     return rht_inverse(rot, signs)
 
 
-def attention_head(q_rows, k_hat, v_hat, ctx, softmax_scale, causal):
+def attention_head(q_rows, k_hat, v_hat, ctx, softmax_scale, causal, sliding_window=0):
     """softmax(scale * q k^T + mask) v for one q head of one sequence, fp64.
 
     q_rows [q_len, d]; k_hat, v_hat [L, d]; query j sits at position ctx + j
-    and, when causal, sees keys 0..ctx+j; otherwise all L keys.
+    and, when causal, sees keys 0..ctx+j; otherwise all L keys.  A sliding
+    window W > 0 also hides every key t with (ctx + j) - t >= W, i.e. the
+    query keeps the W positions ending at its own (the "added window" of the
+    Triton INT4 PR, read with vLLM's window rule).
     """
     q = np.asarray(q_rows, dtype=np.float64)
     scores = softmax_scale * (q @ k_hat.T)
     L = k_hat.shape[0]
+    j = np.arange(q.shape[0])[:, None]
+    t = np.arange(L)[None, :]
     if causal:
-        j = np.arange(q.shape[0])[:, None]
-        t = np.arange(L)[None, :]
         scores = np.where(t <= ctx + j, scores, -np.inf)
+    if sliding_window > 0:
+        scores = np.where((ctx + j) - t < sliding_window, scores, -np.inf)
     m = np.max(scores, axis=1, keepdims=True)
     p = np.exp(scores - m)
     p /= np.sum(p, axis=1, keepdims=True)
@@ -260,7 +265,7 @@ def attention_head(q_rows, k_hat, v_hat, ctx, softmax_scale, causal):
 
 def attention_seq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                   query_start_loc, seq, num_kv_heads, block_size, softmax_scale,
-                  causal, signs, q_heads=None):
+                  causal, signs, q_heads=None, sliding_window=0):
     """Output rows [q_len, Hq, d] (fp64) of one sequence; optionally only some q heads.
 
     q is [num_q_tokens, Hq, d]; q head h uses kv head h // (Hq / Hkv).
@@ -283,12 +288,14 @@ def attention_seq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
             cache_rows[kvh] = (dequantize_original(kc, ks, signs),
                                dequantize_original(vc, vs, signs))
         k_hat, v_hat = cache_rows[kvh]
-        out[:, h, :] = attention_head(q[q0:q1, h, :], k_hat, v_hat, ctx, softmax_scale, causal)
+        out[:, h, :] = attention_head(q[q0:q1, h, :], k_hat, v_hat, ctx, softmax_scale, causal,
+                                      sliding_window)
     return out
 
 
 def attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
-              query_start_loc, num_kv_heads, block_size, softmax_scale, causal, signs):
+              query_start_loc, num_kv_heads, block_size, softmax_scale, causal, signs,
+              sliding_window=0):
     """Full attention output [num_q_tokens, Hq, d] in fp64, streamed per sequence."""
     q = np.asarray(q)
     out = np.zeros(q.shape, dtype=np.float64)
@@ -298,7 +305,7 @@ def attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
             continue
         out[q0:q1] = attention_seq(q, k_cache, v_cache, k_scale, v_scale, block_table,
                                    seq_lens, query_start_loc, s, num_kv_heads, block_size,
-                                   softmax_scale, causal, signs)
+                                   softmax_scale, causal, signs, sliding_window=sliding_window)
     return out
 
 

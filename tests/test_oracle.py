@@ -332,8 +332,12 @@ def _random_cache(rng, nb, bs, hkv, d):
     return kc, vc, ks, vs
 
 
-def test_attention_brute_force_loops_gqa_paged_causal():
-    """Literal per-element loops over a tiny paged, GQA, mixed batch."""
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 1), (True, 3), (True, 5), (False, 2), (False, 4),
+                                           (True, 100)])
+def test_attention_brute_force_loops_gqa_paged_causal(causal, window):
+    """Literal per-element loops over a tiny paged, GQA, mixed batch; the
+    mask is written out per key (causal: t <= ctx + j; sliding window W > 0:
+    (ctx + j) - t < W)."""
     rng = np.random.default_rng(0)
     d, bs, hkv, hq, nb = 6, 4, 2, 4, 6
     kc, vc, ks, vs = _random_cache(rng, nb, bs, hkv, d)
@@ -343,7 +347,8 @@ def test_attention_brute_force_loops_gqa_paged_causal():
     qsl = [0, 3, 4, 6]
     q = _bf16_values((6, hq, d), 9)
     scale = 0.37
-    out = O.attention(q, kc, vc, ks, vs, table, [kv for _, kv in seqs], qsl, hkv, bs, scale, True, signs)
+    out = O.attention(q, kc, vc, ks, vs, table, [kv for _, kv in seqs], qsl, hkv, bs, scale, causal, signs,
+                      sliding_window=window)
     H = scipy.linalg.hadamard(2)  # b = 2, n = 3
     for s, (ql, L) in enumerate(seqs):
         ctx = L - ql
@@ -368,7 +373,11 @@ def test_attention_brute_force_loops_gqa_paged_causal():
                         return orig
                     keys.append(deq(kc, ks))
                     vals.append(deq(vc, vs))
-                sc = [scale * sum(q[tok, h, i] * keys[t][i] for i in range(d)) if t <= ctx + j else -math.inf
+                def visible(t):
+                    if causal and t > ctx + j:
+                        return False
+                    return not (window > 0 and (ctx + j) - t >= window)
+                sc = [scale * sum(q[tok, h, i] * keys[t][i] for i in range(d)) if visible(t) else -math.inf
                       for t in range(L)]
                 m = max(sc)
                 w = [math.exp(x - m) for x in sc]
@@ -415,6 +424,48 @@ def test_attention_noncausal_sees_all_keys():
     n = O.attention(q, kc, vc, ks, vs, np.array([[1, 0]]), [20], [0, 2], 1, 16, 0.2, False, s)
     assert np.allclose(c[1], n[1], atol=1e-12)      # last query sees everything anyway
     assert not np.allclose(c[0], n[0], atol=1e-6)   # first query is masked when causal
+
+
+def test_attention_window_of_one_returns_own_value():
+    """Causal with W = 1: every query sees only the key at its own position,
+    so the output is that key's dequantised value (softmax of one score)."""
+    rng = np.random.default_rng(8)
+    d, L, ql = 128, 40, 5
+    kc, vc, ks, vs = _random_cache(rng, 3, 16, 1, d)
+    s = _signs(d, 8)
+    q = _bf16_values((ql, 1, d), 8)
+    table = np.array([[2, 0, 1]])
+    out = O.attention(q, kc, vc, ks, vs, table, [L], [0, ql], 1, 16, 0.3, True, s, sliding_window=1)
+    for j in range(ql):
+        t = L - ql + j
+        blk, off = table[0][t // 16], t % 16
+        v_hat = O.dequantize_original(O.unpack_codes(vc[blk, off, 0])[None], np.array([vs[blk, off, 0]]), s)[0]
+        assert np.allclose(out[j, 0], v_hat, atol=1e-12)
+
+
+def test_attention_window_equals_attention_over_the_last_keys():
+    """A decode query with window W sees exactly the last W keys: the same as
+    unwindowed attention over a sequence holding only those keys; W >= L is
+    no window at all."""
+    rng = np.random.default_rng(9)
+    d, L = 96, 50
+    kc, vc, ks, vs = _random_cache(rng, 4, 16, 2, d)
+    s = _signs(d, 9)
+    q = _bf16_values((1, 4, d), 9)
+    table = np.array([[3, 1, 0, 2]])
+    for W in (1, 7, 16, 33):
+        win = O.attention(q, kc, vc, ks, vs, table, [L], [0, 1], 2, 16, 0.2, True, s, sliding_window=W)
+        for h in range(4):
+            kvh = h // 2
+            kc_s, ks_s = O.gather_sequence(kc, ks, table[0], L, kvh, 16)
+            vc_s, vs_s = O.gather_sequence(vc, vs, table[0], L, kvh, 16)
+            k_hat = O.dequantize_original(kc_s, ks_s, s)[L - W:]
+            v_hat = O.dequantize_original(vc_s, vs_s, s)[L - W:]
+            ref = O.attention_head(q[0:1, h, :], k_hat, v_hat, W - 1, 0.2, True)
+            assert np.allclose(win[0, h], ref[0], atol=1e-12)
+    full = O.attention(q, kc, vc, ks, vs, table, [L], [0, 1], 2, 16, 0.2, True, s)
+    assert np.array_equal(O.attention(q, kc, vc, ks, vs, table, [L], [0, 1], 2, 16, 0.2, True, s,
+                                      sliding_window=L), full)
 
 
 def test_end_to_end_attention_close_to_unquantised():
