@@ -283,6 +283,38 @@ def rht_bench(w, dev, n_chunks: int, chunk_tokens: int = 65536):
             "rows_per_chunk": chunk_tokens * hkv, "bytes_per_chunk": nbytes}
 
 
+def window_bench(pk, q, out, window: int, iters: int):
+    """Sliding-window attention over the resident cache: device time of
+    `iters` back-to-back kv_int4_attention calls with the window, and the
+    algorithmic bytes the window keeps (the last min(L, W + q_len - 1) keys
+    of each sequence, their scales, q and the block table entries)."""
+    import torch
+    w = pk.w
+    saved = w.sliding_window
+    w.sliding_window = window
+    try:
+        pk.attend(q, out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            pk.attend(q, out)
+        e1.record()
+        torch.cuda.synchronize()
+        if pk.status.item() != 0:
+            raise RuntimeError(f"device status {pk.status.item()} in the windowed attention")
+    finally:
+        w.sliding_window = saved
+    ms = e0.elapsed_time(e1) / iters
+    d, hkv, hq = w.head_size, w.num_kv_heads, w.num_q_heads
+    nbytes = 0
+    for ql, L in w.seqs:
+        keys = min(L, window + ql - 1)
+        nbytes += keys * hkv * 2 * (d // 2 + 4) + 4 * ((keys + 15) // 16) + ql * hq * d * 2
+    return {"window": window, "ms": round(ms, 5), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+            "algorithmic_bytes": nbytes}
+
+
 # ---------------------------------------------------------------------------
 # the oracle on host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -443,6 +475,7 @@ def run_ours(args):
     e2e_value = aggregate_throughput(w.num_q_tokens * args.steps, world, e2e_ms / 1e3)
     if pk.status.item() != 0:
         raise RuntimeError(f"device status {pk.status.item()} during the timed region")
+    window_info = window_bench(pk, q, out, 4096, max(10, min(200, args.steps)))
 
     # ---- roofline of the dominant kernel ----
     peak, tc_peak, peak_kind = load_peaks()
@@ -479,6 +512,7 @@ def run_ours(args):
     write_info["frac"] = round(write_info["gbs"] / peak, 4)
     write_info["step_write_us"] = round(kern["write"][0] / max(1, kern["write"][1]) * 1e3, 2)
     rht_info["frac"] = round(rht_info["gbs"] / peak, 4)
+    window_info["frac"] = round(window_info["gbs"] / peak, 4)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -494,6 +528,7 @@ def run_ours(args):
         "kv_read_gbs": round(attn_bytes / (attn_ms / 1e3) / 1e9, 1) if attn_ms else None,
         "write": write_info,
         "rht": rht_info,
+        "sliding_window": window_info,
         "kernels_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in kern.items()},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(sum(v[1] for v in kern.values())),

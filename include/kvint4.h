@@ -143,7 +143,12 @@ KVINT4_API size_t kv_int4_attention_workspace_size(int num_seqs, int num_q_token
  * kv length seq_lens[i] (including those tokens, whose K/V must already be in
  * the cache).  Its queries are its last q_len positions: query j sits at
  * position seq_lens[i] - q_len + j and, when `causal` != 0, sees keys
- * 0 .. that position; otherwise all seq_lens[i] keys.  Key position p of
+ * 0 .. that position; otherwise all seq_lens[i] keys.  With sliding_window
+ * W > 0 a query at position p also sees no key at a position <= p - W (it
+ * keeps the W positions ending at its own; the "added window" of the Triton
+ * INT4 PR, with vLLM's window rule); W = 0 means no window and W < 0 is
+ * KV_INT4_ERR_SIZE.  Blocks wholly before a sequence's window are never
+ * read.  Key position p of
  * sequence i is in block block_table[i*max_blocks_per_seq + p/block_size],
  * offset p % block_size.  q head hq uses kv head hq / (num_q_heads/num_kv_heads).
  *
@@ -172,7 +177,7 @@ KVINT4_API int kv_int4_attention(const void* q, int64_t q_token_stride,
                       int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len,
                       int num_q_heads, int num_kv_heads, int head_size,
                       int block_size, int num_blocks, float softmax_scale, int causal,
-                      const int8_t* signs, void* out, int64_t out_token_stride,
+                      int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
                       void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
 
@@ -214,8 +219,8 @@ KVINT4_API int kv_int4_attention_noalloc(const void* q, int64_t q_token_stride,
                                          int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len,
                                          int num_q_heads, int num_kv_heads, int head_size,
                                          int block_size, int num_blocks, float softmax_scale, int causal,
-                                         const int8_t* signs, void* out, int64_t out_token_stride,
-                                         int32_t* dev_status, void* stream);
+                                         int sliding_window, const int8_t* signs, void* out,
+                                         int64_t out_token_stride, int32_t* dev_status, void* stream);
 
 /*
  * kv_int4_rht -- the block-diagonal randomized Hadamard rotation on its own:
@@ -276,7 +281,8 @@ KVINT4_API int kv_int4_timing_collect(double* ms, int* launches, int* dropped);
 /* kv_int4_status_string -- a static, human-readable name for a KV_INT4_* code. */
 KVINT4_API const char* kv_int4_status_string(int status);
 
-/* kv_int4_version -- the library's ABI version (currently 1). */
+/* kv_int4_version -- the library's ABI version: 2 (kv_int4_rht added; the attention entry points
+ * take sliding_window). */
 KVINT4_API int kv_int4_version(void);
 
 #ifdef __cplusplus

@@ -31,11 +31,11 @@ _SIGNATURES = {
     "kv_int4_attention_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "kv_int4_attention": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                                   c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
-                                  c_int, c_float, c_int, c_void_p, c_void_p, c_int64, c_void_p, c_size_t,
+                                  c_int, c_float, c_int, c_int, c_void_p, c_void_p, c_int64, c_void_p, c_size_t,
                                   c_void_p, c_void_p]),
     "kv_int4_attention_noalloc": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                           c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
-                                          c_int, c_int, c_int, c_float, c_int, c_void_p, c_void_p, c_int64,
+                                          c_int, c_int, c_int, c_float, c_int, c_int, c_void_p, c_void_p, c_int64,
                                           c_void_p, c_void_p]),
     "kv_int4_rht": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_int, c_int64, c_int, c_void_p, c_int, c_void_p]),
     "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
@@ -198,8 +198,9 @@ def attention_workspace_size(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, 
 
 def attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, query_start_loc,
               max_query_len, max_seq_len, softmax_scale, causal, signs, out, workspace,
-              dev_status: Optional[torch.Tensor] = None, stream=None):
-    """unified_attention_int4 through kv_int4_attention; writes ``out`` in place."""
+              dev_status: Optional[torch.Tensor] = None, stream=None, sliding_window: int = 0):
+    """unified_attention_int4 through kv_int4_attention; writes ``out`` in place.
+    ``sliding_window`` W > 0 hides keys at positions <= p - W from the query at p."""
     nb, bs, hkv, d = _cache_dims(k_cache, v_cache, k_scale, v_scale)
     _check(q.dim() == 3 and q.shape[2] == d, "q must be [tokens, q_heads, d]")
     hq = q.shape[1]
@@ -218,14 +219,15 @@ def attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, quer
                                  _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
                                  _ptr(query_start_loc), int(num_seqs), int(q.shape[0]), int(max_query_len),
                                  int(max_seq_len), int(hq), int(hkv), int(d), int(bs), int(nb),
-                                 float(softmax_scale), int(bool(causal)), _ptr(signs), _ptr(out), os_,
-                                 _ptr(workspace), int(workspace.numel()), _ptr(dev_status), _stream(stream))
+                                 float(softmax_scale), int(bool(causal)), int(sliding_window), _ptr(signs),
+                                 _ptr(out), os_, _ptr(workspace), int(workspace.numel()), _ptr(dev_status),
+                                 _stream(stream))
     _raise(code, "kv_int4_attention")
 
 
 def attention_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, query_start_loc,
                       max_query_len, max_seq_len, softmax_scale, causal, signs, out,
-                      dev_status: Optional[torch.Tensor] = None, stream=None):
+                      dev_status: Optional[torch.Tensor] = None, stream=None, sliding_window: int = 0):
     """kv_int4_attention_noalloc: attention whose workspace is the library's
     static device scratch (for callers that cannot allocate device memory).
 
@@ -251,6 +253,6 @@ def attention_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
                                          _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
                                          _ptr(query_start_loc), int(num_seqs), int(q.shape[0]), int(max_query_len),
                                          int(max_seq_len), int(hq), int(hkv), int(d), int(bs), int(nb),
-                                         float(softmax_scale), int(bool(causal)), _ptr(signs), _ptr(out), os_,
-                                         _ptr(dev_status), _stream(stream))
+                                         float(softmax_scale), int(bool(causal)), int(sliding_window),
+                                         _ptr(signs), _ptr(out), os_, _ptr(dev_status), _stream(stream))
     _raise(code, "kv_int4_attention_noalloc")

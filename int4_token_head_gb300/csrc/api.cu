@@ -70,7 +70,7 @@ using namespace kvint4;
 
 extern "C" {
 
-int kv_int4_version(void) { return 1; }
+int kv_int4_version(void) { return 2; }
 
 const char* kv_int4_status_string(int status) {
   switch (status) {
@@ -147,10 +147,10 @@ int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_ca
                       int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc,
                       int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
                       int num_kv_heads, int head_size, int block_size, int num_blocks, float softmax_scale,
-                      int causal, const int8_t* signs, void* out, int64_t out_token_stride, void* workspace,
-                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                      int causal, int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (num_seqs < 0 || num_q_tokens < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0 ||
-      max_blocks_per_seq < 0)
+      max_blocks_per_seq < 0 || sliding_window < 0)
     return KV_INT4_ERR_SIZE;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return KV_INT4_ERR_HEADS;
   if (!head_size_ok(head_size)) return KV_INT4_ERR_HEAD_SIZE;
@@ -170,7 +170,8 @@ int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_ca
   if (current_device() < 0) return KV_INT4_ERR_CUDA;
   AttnArgs a{q, q_token_stride, k_cache, v_cache, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
              seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len, max_seq_len, num_q_heads,
-             num_kv_heads, head_size, block_size, num_blocks, softmax_scale, causal, signs, out, out_token_stride,
+             num_kv_heads, head_size, block_size, num_blocks, softmax_scale, causal, sliding_window, signs, out,
+             out_token_stride,
              workspace, workspace_bytes, dev_status};
   return launch_attention(a, static_cast<cudaStream_t>(stream));
 }

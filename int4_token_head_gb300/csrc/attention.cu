@@ -89,6 +89,7 @@ struct Common {
   int group;
   int num_blocks;
   int causal;
+  int window;    // sliding window (0: none): the query at position p sees no key at p - window or before
   float qscale;  // softmax_scale * log2(e) / b
   const int8_t* signs;
   uint16_t* out;
@@ -101,6 +102,14 @@ struct Common {
   int dcols;        // decode: query columns per block (8 / np); longer queries go to prefill
   long long max_items;  // capacity of the prefill item list
 };
+
+// first key position visible to the query at position qpos
+__device__ __forceinline__ int window_lo(const Common& c, int qpos) {
+  return c.window > 0 ? max(0, qpos - c.window + 1) : 0;
+}
+// first 16-key block a sequence's attention reads: blocks wholly before the
+// window of its earliest query (position L - q_len) are never visible
+__device__ __forceinline__ int first_block(const Common& c, int L, int ql) { return window_lo(c, L - ql) >> 4; }
 
 __device__ __forceinline__ bool is_decode_kind(int qlen, const Common& c) {
   return c.group <= c.dcols && qlen * c.group <= c.dcols;
@@ -166,7 +175,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
       int tot_a, tot_p;
       long long tot_b, tot_c;
       const int ex_a = block_exclusive_scan<int>(kind == 1, &tot_a, s_i32);
-      const long long ex_b = block_exclusive_scan<long long>(kind == 1 ? (nblk + c.np - 1) / c.np : 0, &tot_b, s_i64);
+      const int npos = kind == 1 ? (nblk - first_block(c, L, ql) + c.np - 1) / c.np : 0;
+      const long long ex_b = block_exclusive_scan<long long>(npos, &tot_b, s_i64);
       const int ex_p = block_exclusive_scan<int>(kind == 2, &tot_p, s_i32);
       const long long ex_c = block_exclusive_scan<long long>((long long)ntiles * c.hkv, &tot_c, s_i64);
       if (kind == 1) {
@@ -276,14 +286,17 @@ struct DecWalk {
   int kp;     // position within the sequence
   int npos;   // positions of the sequence
   int nblk;   // 16-key blocks of the sequence
+  int fb;     // first block read (the sliding window's)
   int seq;    // sequence id
 };
 
 template <int NP>
 __device__ __forceinline__ void walk_load(DecWalk& w, const Common& c, const PlanView& pv) {
   w.seq = pv.dseq[w.i];
-  w.nblk = (c.seq_lens[w.seq] + 15) / 16;
-  w.npos = (w.nblk + NP - 1) / NP;
+  const int L = c.seq_lens[w.seq];
+  w.nblk = (L + 15) / 16;
+  w.fb = first_block(c, L, c.qsl[w.seq + 1] - c.qsl[w.seq]);
+  w.npos = (w.nblk - w.fb + NP - 1) / NP;
 }
 template <int NP>
 __device__ __forceinline__ void walk_next(DecWalk& w, const Common& c, const PlanView& pv) {
@@ -458,7 +471,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   // block j of a position, or kAbsent past the end of the sequence (NP > 1)
   constexpr int kAbsent = -0x7fffffff - 1;
   auto block_at = [&](const DecWalk& w, int j) {
-    const int kb = w.kp * NP + j;
+    const int kb = w.fb + w.kp * NP + j;
     return kb < w.nblk ? c.block_table[(long long)w.seq * c.max_blocks + kb] : kAbsent;
   };
   auto issue = [&](int blk, int grp, int slot) {
@@ -504,8 +517,10 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   uint32_t qb[G::KSTEPS][2];
   float oacc[G::KSTEPS][4];
   float m0, m1, l0, l1, bias0, bias1;
-  int lim0, lim1;  // keys visible to columns 2cq, 2cq+1
+  int lim0, lim1;  // keys visible to columns 2cq, 2cq+1: positions [lo, lim)
+  int lo0, lo1;
   int lim_warp;    // smallest of all columns' limits
+  int lo_warp;     // largest of all columns' first visible positions
   bool first_piece = cw.kp == 0;
 
   auto begin_segment = [&]() {
@@ -543,9 +558,15 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const int j0 = min(col0 / c.group, max(ql - 1, 0)), j1 = min(col1 / c.group, max(ql - 1, 0));
     lim0 = c.causal ? min(L, ctx + j0 + 1) : L;
     lim1 = c.causal ? min(L, ctx + j1 + 1) : L;
+    lo0 = window_lo(c, ctx + j0);
+    lo1 = window_lo(c, ctx + j1);
     lim_warp = min(lim0, lim1);
+    lo_warp = max(lo0, lo1);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) lim_warp = min(lim_warp, __shfl_xor_sync(0xffffffffu, lim_warp, o));
+    for (int o = 1; o < 32; o <<= 1) {
+      lim_warp = min(lim_warp, __shfl_xor_sync(0xffffffffu, lim_warp, o));
+      lo_warp = max(lo_warp, __shfl_xor_sync(0xffffffffu, lo_warp, o));
+    }
 #pragma unroll
     for (int i = 0; i < G::KSTEPS; i++) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
     m0 = m1 = -INFINITY;
@@ -645,19 +666,20 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
 #pragma unroll
       for (int e = 0; e < 4; e++) sa[e] = jb == j ? sacc[j][e] : sa[e];
 
-    const int kb0 = cw.kp * NP;
+    const int kb0 = cw.fb + cw.kp * NP;
     const int pos0 = (kb0 + jb) * 16 + g, pos1 = pos0 + 8;
     const float ks0 = sks[g] * 0.0625f, ks1 = sks[g + 8] * 0.0625f;
     float s00 = (sa[0] - bias0) * ks0, s01 = (sa[1] - bias1) * ks0;
     float s10 = (sa[2] - bias0) * ks1, s11 = (sa[3] - bias1) * ks1;
-    // keys past a column's visible length (or in an invalid or absent block)
-    // only occur in positions that reach past the warp's smallest limit
-    const bool full = allok && (kb0 + NP) * 16 <= lim_warp;
+    // keys outside a column's visible range [lo, lim) (or in an invalid or
+    // absent block) only occur in positions that reach past the warp's
+    // smallest limit or start before its largest window start
+    const bool full = allok && (kb0 + NP) * 16 <= lim_warp && kb0 * 16 >= lo_warp;
     if (!full) {
-      s00 = (bok && pos0 < lim0) ? s00 : -INFINITY;
-      s01 = (bok && pos0 < lim1) ? s01 : -INFINITY;
-      s10 = (bok && pos1 < lim0) ? s10 : -INFINITY;
-      s11 = (bok && pos1 < lim1) ? s11 : -INFINITY;
+      s00 = (bok && pos0 < lim0 && pos0 >= lo0) ? s00 : -INFINITY;
+      s01 = (bok && pos0 < lim1 && pos0 >= lo1) ? s01 : -INFINITY;
+      s10 = (bok && pos1 < lim0 && pos1 >= lo0) ? s10 : -INFINITY;
+      s11 = (bok && pos1 < lim1 && pos1 >= lo1) ? s11 : -INFINITY;
     }
     float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
     // exact running max: reduce across the key lanes only when some lane
@@ -755,7 +777,7 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (col >= ql * c.group) return;  // ql * group <= dcols
   const int nblk = (c.seq_lens[seq] + 15) / 16;
-  const int npos = (nblk + c.np - 1) / c.np;
+  const int npos = (nblk - first_block(c, c.seq_lens[seq], ql) + c.np - 1) / c.np;
   const int grp = h / c.hg, hl = h - grp * c.hg;
   const long long Tu = pv.dprefix[n_dseq] * c.ng;
   const long long sbeg = pv.dprefix[i] * c.ng + (long long)grp * npos, send = sbeg + npos;
@@ -928,8 +950,10 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
       }
     };
 
+    // blocks wholly before the window of the tile's earliest query are skipped
+    const int kb0 = window_lo(c, ctx + tok0) >> 4;
     for (int s = 0; s < G::STAGES - 1; s++) {
-      if (s < nkb) issue(s, s);
+      if (kb0 + s < nkb) issue(kb0 + s, s);
       cp_async_commit();
     }
 
@@ -942,11 +966,12 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
     const int qp1 = ctx + tok0 + (r1 < nrows ? r1 / c.group : 0);
     const int lim0 = c.causal ? min(L, qp0 + 1) : L;
     const int lim1 = c.causal ? min(L, qp1 + 1) : L;
+    const int lo0 = window_lo(c, qp0), lo1 = window_lo(c, qp1);
 
 #pragma unroll 1
-    for (int kb = 0; kb < nkb; kb++) {
-      const int stage = kb % G::STAGES;
-      if (kb + G::STAGES - 1 < nkb) issue(kb + G::STAGES - 1, (kb + G::STAGES - 1) % G::STAGES);
+    for (int kb = kb0; kb < nkb; kb++) {
+      const int stage = (kb - kb0) % G::STAGES;
+      if (kb + G::STAGES - 1 < nkb) issue(kb + G::STAGES - 1, (kb - kb0 + G::STAGES - 1) % G::STAGES);
       cp_async_commit();
       cp_async_wait<G::STAGES - 1>();
       __syncthreads();
@@ -998,8 +1023,8 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
           const int key = nt * 8 + 2 * cq + e;
           const int pos = kb * 16 + key;
           const float ks = sks[key];
-          sv[nt][e] = (bok && pos < lim0) ? sacc[nt][e] * ks : -INFINITY;
-          sv[nt][2 + e] = (bok && pos < lim1) ? sacc[nt][2 + e] * ks : -INFINITY;
+          sv[nt][e] = (bok && pos < lim0 && pos >= lo0) ? sacc[nt][e] * ks : -INFINITY;
+          sv[nt][2 + e] = (bok && pos < lim1 && pos >= lo1) ? sacc[nt][2 + e] * ks : -INFINITY;
           mx0 = fmaxf(mx0, sv[nt][e]);
           mx1 = fmaxf(mx1, sv[nt][2 + e]);
         }
@@ -1160,6 +1185,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.group = a.num_q_heads / a.num_kv_heads;
   c.num_blocks = a.num_blocks;
   c.causal = a.causal;
+  c.window = a.sliding_window;
   c.qscale = a.softmax_scale * kLog2e / (float)Head<D>::b;
   c.signs = a.signs;
   c.out = static_cast<uint16_t*>(a.out);

@@ -58,6 +58,7 @@ struct AttnArgs {
   int num_blocks;
   float softmax_scale;
   int causal;
+  int sliding_window;  // 0: none
   const int8_t* signs;
   void* out;
   int64_t out_stride;
@@ -71,11 +72,11 @@ struct WorkspaceLayout {
   size_t plan;          // int32 counters + per-seq schedule
   size_t dseq;          // int32 [num_seqs] decode-sequence list
   size_t dprefix;       // int64 [num_seqs + 1] block prefix over decode sequences
-  size_t pitems;        // int4 [max_prefill_items] prefill work list
+  size_t pitems;        // int2 [num_seqs + 1] prefill sequence table (region sized for max_prefill_items int4)
   size_t qrot;          // f16 [num_q_tokens][Hq][d] rotated, pre-scaled queries
   size_t direct_o;      // f32 [num_seqs][Hkv][8][d]
   size_t direct_ml;     // f32 [num_seqs][Hkv][8][2]
-  size_t warp_o;        // f32 [kMaxDecodeWarps][8][d]
+  size_t warp_o;        // f32 [kMaxDecodeWarps][8][d] (one slot per (decode CTA, head of its group))
   size_t warp_ml;       // f32 [kMaxDecodeWarps][8][2]
   size_t total;
   int64_t max_prefill_items;

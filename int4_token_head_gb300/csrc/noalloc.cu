@@ -60,8 +60,8 @@ extern "C" int kv_int4_attention_noalloc(
     const float* k_scale_cache, const float* v_scale_cache, const int32_t* block_table, int max_blocks_per_seq,
     const int32_t* seq_lens, const int32_t* query_start_loc, int num_seqs, int num_q_tokens, int max_query_len,
     int max_seq_len, int num_q_heads, int num_kv_heads, int head_size, int block_size, int num_blocks,
-    float softmax_scale, int causal, const int8_t* signs, void* out, int64_t out_token_stride, int32_t* dev_status,
-    void* stream) {
+    float softmax_scale, int causal, int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
+    int32_t* dev_status, void* stream) {
   const size_t need =
       kv_int4_attention_workspace_size(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_size);
   if (need > KV_INT4_NOALLOC_SCRATCH_BYTES) return KV_INT4_ERR_SCRATCH_LIMIT;
@@ -71,7 +71,8 @@ extern "C" int kv_int4_attention_noalloc(
     return kv_int4_attention(q, q_token_stride, k_cache, v_cache, k_scale_cache, v_scale_cache, block_table,
                              max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len,
                              max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
-                             softmax_scale, causal, signs, out, out_token_stride, nullptr, 0, dev_status, stream);
+                             softmax_scale, causal, sliding_window, signs, out, out_token_stride, nullptr, 0,
+                             dev_status, stream);
   }
   const int dev = kvint4::current_device();
   if (dev < 0) return KV_INT4_ERR_CUDA;
@@ -81,6 +82,6 @@ extern "C" int kv_int4_attention_noalloc(
   return kv_int4_attention(q, q_token_stride, k_cache, v_cache, k_scale_cache, v_scale_cache, block_table,
                            max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len,
                            max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-                           causal, signs, out, out_token_stride, scratch, KV_INT4_NOALLOC_SCRATCH_BYTES, dev_status,
-                           stream);
+                           causal, sliding_window, signs, out, out_token_stride, scratch,
+                           KV_INT4_NOALLOC_SCRATCH_BYTES, dev_status, stream);
 }

@@ -91,7 +91,7 @@ class PagedKV:
         _lib.attention(q, self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.block_table,
                        self.seq_lens, self.query_start_loc, w.max_query_len, w.max_seq_len,
                        self.softmax_scale, w.causal, self.signs, out, self.workspace,
-                       dev_status=self.status, stream=stream)
+                       dev_status=self.status, stream=stream, sliding_window=w.sliding_window)
 
     def step(self, q, k_new, v_new, slots, out, stream=None):
         self.write(k_new, v_new, slots, stream=stream)

@@ -50,6 +50,7 @@ class Workload:
     block_table: torch.Tensor    # int32 [num_seqs, max_blocks_per_seq], -1 padded
     outlier_channels: Optional[torch.Tensor]  # int64 [n] flat (kv_head*d + ch)
     outlier_scale: float
+    sliding_window: int = 0      # 0: none; else a query at p sees no key at p - W or before
 
     @property
     def num_seqs(self) -> int:
@@ -263,7 +264,7 @@ def make_workload(name: str, seed: Optional[int] = None, **overrides) -> Workloa
 
 def custom_workload(num_q_heads: int, num_kv_heads: int, head_size: int,
                     seqs: List[Tuple[int, int]], seed: int = 7, spare: int = 3,
-                    block_size: int = 16, causal: bool = True) -> Workload:
+                    block_size: int = 16, causal: bool = True, sliding_window: int = 0) -> Workload:
     """A workload with explicit shapes, for parity sweeps and edge cases."""
     g = torch.Generator("cpu")
     g.manual_seed(seed)
@@ -280,7 +281,7 @@ def custom_workload(num_q_heads: int, num_kv_heads: int, head_size: int,
     return Workload(name="custom", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                     head_size=head_size, block_size=block_size, causal=causal, seed=seed,
                     seqs=list(seqs), num_blocks=num_blocks, signs=signs, block_table=table,
-                    outlier_channels=None, outlier_scale=1.0)
+                    outlier_channels=None, outlier_scale=1.0, sliding_window=sliding_window)
 
 
 def describe(w: Workload) -> Dict:

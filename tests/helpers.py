@@ -32,11 +32,11 @@ def oracle_attention(w, q, caches, seqs=None, heads=None):
     scale = 1.0 / math.sqrt(w.head_size)
     if seqs is None:
         return O.attention(qn, kc, vc, ks, vs, bt, sl, qsl, w.num_kv_heads, w.block_size, scale, w.causal,
-                           w.signs.numpy())
+                           w.signs.numpy(), sliding_window=w.sliding_window)
     out = {}
     for s in seqs:
         out[s] = O.attention_seq(qn, kc, vc, ks, vs, bt, sl, qsl, s, w.num_kv_heads, w.block_size, scale,
-                                 w.causal, w.signs.numpy(), q_heads=heads)
+                                 w.causal, w.signs.numpy(), q_heads=heads, sliding_window=w.sliding_window)
     return out
 
 

@@ -55,7 +55,7 @@ def test_status_strings_and_version(lib):
             s = lib.kv_int4_status_string(code).decode()
             assert s and s != "unknown status"
     assert lib.kv_int4_status_string(999).decode() == "unknown status"
-    assert lib.kv_int4_version() == 1
+    assert lib.kv_int4_version() == 2
 
 
 def test_workspace_size_is_host_only_and_monotone(lib):
@@ -106,12 +106,12 @@ def test_write_validation(lib):
 def _attn(lib, **kw):
     ws = lib.kv_int4_attention_workspace_size(2, 8, 32, 8, 128)
     a = dict(q=FAKE, qs=32 * 128, kc=FAKE, vc=FAKE, ksc=FAKE, vsc=FAKE, bt=FAKE, maxb=8, sl=FAKE, qsl=FAKE,
-             ns=2, nq=8, mq=4, ms=128, hq=32, hkv=8, d=128, bs=16, nb=16, scale=0.1, causal=1, signs=FAKE,
+             ns=2, nq=8, mq=4, ms=128, hq=32, hkv=8, d=128, bs=16, nb=16, scale=0.1, causal=1, win=0, signs=FAKE,
              out=FAKE, os=32 * 128, ws=FAKE, wsb=ws, status=None, stream=None)
     a.update(kw)
     return lib.kv_int4_attention(a["q"], a["qs"], a["kc"], a["vc"], a["ksc"], a["vsc"], a["bt"], a["maxb"],
                                  a["sl"], a["qsl"], a["ns"], a["nq"], a["mq"], a["ms"], a["hq"], a["hkv"],
-                                 a["d"], a["bs"], a["nb"], a["scale"], a["causal"], a["signs"], a["out"],
+                                 a["d"], a["bs"], a["nb"], a["scale"], a["causal"], a["win"], a["signs"], a["out"],
                                  a["os"], a["ws"], a["wsb"], a["status"], a["stream"])
 
 
@@ -130,6 +130,8 @@ def test_attention_validation(lib):
     assert _attn(lib, ws=ctypes.c_void_p(0x10010)) == D["KV_INT4_ERR_ALIGN"]
     assert _attn(lib, qs=32 * 128 + 2) == D["KV_INT4_ERR_ALIGN"]
     assert _attn(lib, ns=-3) == D["KV_INT4_ERR_SIZE"]
+    assert _attn(lib, win=-1) == D["KV_INT4_ERR_SIZE"]
+    assert _attn(lib, ns=0, win=4096) == D["KV_INT4_OK"]
 
 
 def test_rht_validation(lib):

@@ -70,6 +70,67 @@ def test_attention_on_oracle_cache(case):
     assert_close_attention(got, ref, what=name)
 
 
+WINDOW_CASES = [
+    # (name, Hq, Hkv, d, [(q_len, kv_len), ...], causal, sliding_window)
+    ("win64_decode_d128_g4", 32, 8, 128, [(1, 300), (1, 37), (1, 16), (1, 1), (1, 129)], True, 64),
+    ("win37_decode_d96_g1", 8, 8, 96, [(1, 200), (1, 33), (1, 64)], True, 37),
+    ("win1_decode_d128_g4", 16, 4, 128, [(1, 90), (1, 5)], True, 1),
+    ("win_ge_len_decode_d192", 16, 4, 192, [(1, 500), (1, 17)], True, 1000),
+    ("win5_spec_q2_decode_path", 8, 2, 128, [(2, 50), (2, 2), (1, 40)], True, 5),
+    ("win24_prefill_d128_g4", 16, 4, 128, [(40, 40), (70, 100), (5, 5)], True, 24),
+    ("win100_prefill_d64_g16", 32, 2, 64, [(130, 300), (3, 40)], True, 100),
+    ("win50_mixed_d192", 16, 4, 192, [(1, 300), (60, 60), (1, 45), (25, 200), (1, 1)], True, 50),
+    ("win10_noncausal_prefill", 8, 2, 128, [(20, 60), (7, 7)], False, 10),
+    ("win20_decode_g16_prefill_kernel", 32, 2, 128, [(1, 100), (1, 33)], True, 20),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=lambda c: c[0])
+def test_attention_sliding_window_on_oracle_cache(case):
+    name, hq, hkv, d, seqs, causal, win = case
+    w = synthetic.custom_workload(hq, hkv, d, seqs, seed=13, causal=causal, sliding_window=win)
+    got, ref, status = _attend_on_oracle_cache(w)
+    assert status == 0
+    assert_close_attention(got, ref, what=name)
+
+
+def test_sliding_window_blocks_before_the_window_are_never_read():
+    """Blocks wholly before every query's window may hold anything (here
+    NaN-payload scales and garbage codes): the output must not change."""
+    w = synthetic.custom_workload(16, 4, 128, [(1, 400), (3, 260)], seed=17, sliding_window=48)
+    caches = oracle_write_history_and_step(w)
+    pk = PagedKV(w)
+    _upload(pk, caches)
+    q = w.queries("cpu").cuda()
+    out_a = torch.empty((w.num_q_tokens, w.num_q_heads, w.head_size), dtype=torch.bfloat16, device="cuda")
+    pk.attend(q, out_a)
+    for s, (ql, L) in enumerate(w.seqs):
+        first = (L - ql - 48 + 1) // 16
+        for blk in w.block_table[s, :max(0, first)].tolist():
+            pk.k_cache[blk].fill_(0x77)
+            pk.v_cache[blk].fill_(0x77)
+            pk.k_scale[blk].fill_(float("nan"))
+            pk.v_scale[blk].fill_(float("nan"))
+    out_b = torch.empty_like(out_a)
+    pk.attend(q, out_b)
+    torch.cuda.synchronize()
+    assert pk.status.item() == 0
+    assert torch.equal(out_a, out_b)
+
+
+def test_full_size_gqa_with_sliding_window_sampled():
+    w = synthetic.make_workload("gqa")
+    w.sliding_window = 1000
+    pk = PagedKV(w)
+    pk.populate_history()
+    q, k, v, slots = pk.step_inputs()
+    out = torch.empty((w.num_q_tokens, w.num_q_heads, w.head_size), dtype=torch.bfloat16, device="cuda")
+    pk.step(q, k, v, slots, out)
+    torch.cuda.synchronize()
+    assert pk.status.item() == 0
+    _check_sampled(w, q, out, seqs=[0, w.num_seqs // 2, w.num_seqs - 1], heads=[0, w.num_q_heads - 1])
+
+
 @pytest.mark.parametrize("name", ["tiny"])
 def test_attention_tiny_end_to_end(name):
     w = synthetic.make_workload(name)
@@ -164,7 +225,7 @@ def _check_sampled(w, q, out, seqs, heads):
             vc, vsc = O.quantize(O.rotate_for_cache(v[:, kvh], signs))
             k_hat = O.dequantize_original(kc, ksc, signs)
             v_hat = O.dequantize_original(vc, vsc, signs)
-            ref = O.attention_head(qn[q0:q0 + ql, h], k_hat, v_hat, L - ql, scale, w.causal)
+            ref = O.attention_head(qn[q0:q0 + ql, h], k_hat, v_hat, L - ql, scale, w.causal, w.sliding_window)
             got = out[q0:q0 + ql, h].float().cpu().numpy()
             assert_close_attention(got, ref, min_corr=0.999 if got.size < 256 else 0.9999,
                                    what=f"{w.name} seq {s} head {h}")

@@ -65,6 +65,6 @@ def test_noalloc_rejects_sizes_beyond_the_scratch():
     assert need > _lib.NOALLOC_SCRATCH_BYTES
     fake = __import__("ctypes").c_void_p(0x10000)
     rc = lib.kv_int4_attention_noalloc(fake, 64 * 256, fake, fake, fake, fake, fake, 8, fake, fake, 100000, 100000,
-                                       1, 128, 64, 8, 256, 16, 16, 0.1, 1, fake, fake, 64 * 256, None, None)
+                                       1, 128, 64, 8, 256, 16, 16, 0.1, 1, 0, fake, fake, 64 * 256, None, None)
     assert rc == _lib.ERR_SCRATCH_LIMIT
     assert "no-allocation scratch" in _lib.status_string(rc)
