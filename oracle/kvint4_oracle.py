@@ -320,3 +320,91 @@ def rotated_domain_scores(q_rows, codes, scales, signs, softmax_scale):
     qr = rht_forward(q_rows, signs)
     rot = np.asarray(codes, dtype=np.float64) * np.asarray(scales, dtype=np.float64)[..., None]
     return (softmax_scale / b) * (qr @ rot.T)
+
+
+# ---------------------------------------------------------------------------
+# Sibling mode: int8_per_token_head ("[Feature] Triton INT4 per-token-head KV
+# cache quantization", PR #40835, review thread: the int8 cache dtype, the
+# raw-cache "round reference" test, the 0.1 dequantisation tolerance;
+# "vLLM -- Attention Kernels & KV Cache Quantization", Merged contribution:
+# int8_per_token_head never uses the transform).  Readings: scale =
+# fp32(absmax / 127) (symmetric, codes in [-127, 127], clamp to [-128, 127]
+# as a guard), code = round-half-even(x * r) with r = fp32(1 / s) and the
+# product exact, the same evaluation as the INT4 mode; vectors with absmax
+# below 2^-119 (where absmax / 127 would leave the fp32 normal range) are
+# stored as scale 0 and zero codes.  Caches: int8 [NB, bs, Hkv, d], scales
+# float32 [NB, bs, Hkv].
+# ---------------------------------------------------------------------------
+
+FLUSH_ABSMAX_INT8 = 2.0 ** -119
+
+
+def quantize_int8(x_bf16):
+    """Per-vector absmax INT8 quantisation over the last axis, no rotation.
+
+    Returns (codes int8 [..., d] in [-128, 127], scale float32 [...]).
+      a = max_i |x_i|;  s = fp32(a / 127);  r = fp32(1 / s)
+      c = clamp(round_half_even(x * r), -128, 127), x*r exact in fp64
+    with s = 0, c = 0 when a < 2^-119.
+    """
+    x = np.asarray(x_bf16, dtype=np.float64)
+    a = np.max(np.abs(x), axis=-1)
+    a32 = a.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        s = (a32 / np.float32(127.0)).astype(np.float32)
+        r = (np.float32(1.0) / s).astype(np.float32)
+    flush = a < FLUSH_ABSMAX_INT8
+    s = np.where(flush, np.float32(0.0), s).astype(np.float32)
+    r = np.where(flush, np.float32(0.0), r).astype(np.float32)
+    prod = x * r.astype(np.float64)[..., None]
+    c = np.clip(np.rint(prod), -128, 127).astype(np.int8)
+    return c, s
+
+
+def write_cache_int8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, block_size):
+    """Quantise new K/V head vectors (no rotation) into the int8 paged cache.
+
+    k, v: [T, Hkv, d]; k_cache/v_cache int8 [NB, bs, Hkv, d], scales float32
+    [NB, bs, Hkv], updated in place; slot < 0 skipped; returns the slots that
+    were outside [0, NB*bs) (and skipped)."""
+    kc, ks = quantize_int8(k)
+    vc, vs = quantize_int8(v)
+    nb = k_cache.shape[0]
+    bad = []
+    for t, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if slot < 0:
+            continue
+        if slot >= nb * block_size:
+            bad.append(int(slot))
+            continue
+        blk, off = divmod(int(slot), block_size)
+        k_cache[blk, off] = kc[t]
+        v_cache[blk, off] = vc[t]
+        k_scale[blk, off] = ks[t]
+        v_scale[blk, off] = vs[t]
+    return bad
+
+
+def attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, query_start_loc,
+                   num_kv_heads, block_size, softmax_scale, causal, sliding_window=0):
+    """Attention over the int8 cache: k_hat = c * s (no rotation), then the
+    same softmax(scale * q k_hat^T + mask) v_hat per q head as the INT4 mode."""
+    q = np.asarray(q, dtype=np.float64)
+    hq = q.shape[1]
+    group = hq // num_kv_heads
+    out = np.zeros(q.shape, dtype=np.float64)
+    for s in range(len(seq_lens)):
+        q0, q1 = int(query_start_loc[s]), int(query_start_loc[s + 1])
+        if q1 == q0:
+            continue
+        L = int(seq_lens[s])
+        pos = np.arange(L)
+        blk = np.asarray(block_table[s], dtype=np.int64)[pos // block_size]
+        off = pos % block_size
+        for h in range(hq):
+            kvh = h // group
+            k_hat = k_cache[blk, off, kvh].astype(np.float64) * k_scale[blk, off, kvh].astype(np.float64)[:, None]
+            v_hat = v_cache[blk, off, kvh].astype(np.float64) * v_scale[blk, off, kvh].astype(np.float64)[:, None]
+            out[q0:q1, h] = attention_head(q[q0:q1, h], k_hat, v_hat, L - (q1 - q0), softmax_scale, causal,
+                                           sliding_window)
+    return out

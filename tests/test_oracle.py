@@ -499,3 +499,113 @@ def test_end_to_end_attention_close_to_unquantised():
             corr = np.corrcoef(out[q0:q0 + ql, h].ravel(), ref.ravel())[0, 1]
             assert corr > 0.95
         q0 += ql
+
+
+# ---------------------------------------------------------------------------
+# int8_per_token_head sibling mode
+# ---------------------------------------------------------------------------
+
+def test_int8_quantizer_hand_examples():
+    """Worked by hand: absmax 127 gives s = 1, r = 1 and codes = rint(x) with
+    ties to even; absmax 63.5 gives s = 0.5, r = 2."""
+    x = np.array([[127.0, -3.5, 2.5, 0.5, -0.5, 1.5, -127.0, 0.0]])
+    c, s = O.quantize_int8(x)
+    assert s[0] == np.float32(1.0)
+    assert c[0].tolist() == [127, -4, 2, 0, 0, 2, -127, 0]
+    x = np.array([[63.5, 0.25, -0.75, 0.125]])
+    c, s = O.quantize_int8(x)
+    assert s[0] == np.float32(0.5)
+    assert c[0].tolist() == [127, 0, -2, 0]
+
+
+def test_int8_quantizer_invariants_and_flush():
+    rng = np.random.default_rng(21)
+    x = torch.from_numpy(rng.standard_normal((2000, 128)) * np.exp(rng.uniform(-6, 6, (2000, 1)))).to(
+        torch.bfloat16).double().numpy()
+    c, s = O.quantize_int8(x)
+    a = np.abs(x).max(axis=1)
+    assert np.all(np.abs(c.astype(np.int64)) <= 127)
+    idx = np.abs(x).argmax(axis=1)
+    assert np.all(np.abs(c[np.arange(len(x)), idx]) == 127)            # absmax -> +-127
+    # r = fp32(1/s) is off by at most 2^-24 relative, so x*r is within 127.5 * 2^-24 of x/s
+    sd = s.astype(np.float64)[:, None]
+    assert np.all(np.abs(x - c * sd) <= sd * (0.5 + 127.5 * 2.0 ** -24))
+    assert np.array_equal(s, (a.astype(np.float32) / np.float32(127)).astype(np.float32))
+    # multiples of the scale come back exactly
+    k = rng.integers(-127, 128, (50, 64)).astype(np.float64)
+    k[:, 0] = 127
+    c, s = O.quantize_int8(k * 0.25)
+    assert np.array_equal(c, k.astype(np.int8)) and np.all(s == np.float32(0.25))
+    # flush bound: below 2^-119 -> scale 0, zero codes; at it -> a normal scale
+    tiny = np.full((1, 8), 2.0 ** -119)
+    c, s = O.quantize_int8(tiny * (1 - 2.0 ** -8))
+    assert s[0] == 0 and not c.any()
+    c, s = O.quantize_int8(tiny)
+    assert s[0] > np.finfo(np.float32).tiny and np.all(c == 127)
+
+
+def test_int8_dequant_within_the_pages_tolerance():
+    """The int8 path's dequantisation tolerance on the pages is 0.1 / 0.1."""
+    rng = np.random.default_rng(22)
+    x = torch.from_numpy(rng.standard_normal((4096, 128))).to(torch.bfloat16).double().numpy()
+    c, s = O.quantize_int8(x)
+    deq = c * s.astype(np.float64)[:, None]
+    assert np.all(np.abs(deq - x) <= 0.1 + 0.1 * np.abs(x))
+
+
+def test_int8_attention_brute_force_loops():
+    """Literal per-element loops over a tiny paged GQA batch of the int8 cache."""
+    rng = np.random.default_rng(23)
+    d, bs, hkv, hq, nb = 6, 4, 2, 4, 6
+    kc = rng.integers(-128, 128, (nb, bs, hkv, d)).astype(np.int8)
+    vc = rng.integers(-128, 128, (nb, bs, hkv, d)).astype(np.int8)
+    ks = rng.uniform(0.001, 0.02, (nb, bs, hkv)).astype(np.float32)
+    vs = rng.uniform(0.001, 0.02, (nb, bs, hkv)).astype(np.float32)
+    seqs = [(3, 7), (1, 5), (2, 2)]
+    table = np.array([[4, 1], [0, 5], [3, 2]])
+    qsl = [0, 3, 4, 6]
+    q = _bf16_values((6, hq, d), 24)
+    for causal, window in ((True, 0), (True, 2), (False, 0)):
+        out = O.attention_int8(q, kc, vc, ks, vs, table, [kv for _, kv in seqs], qsl, hkv, bs, 0.5, causal,
+                               sliding_window=window)
+        for s, (ql, L) in enumerate(seqs):
+            ctx = L - ql
+            for j in range(ql):
+                tok = qsl[s] + j
+                for h in range(hq):
+                    kvh = h // (hq // hkv)
+                    sc, vals = [], []
+                    for t in range(L):
+                        blk, off = table[s][t // bs], t % bs
+                        key = [int(kc[blk, off, kvh, i]) * float(ks[blk, off, kvh]) for i in range(d)]
+                        vals.append([int(vc[blk, off, kvh, i]) * float(vs[blk, off, kvh]) for i in range(d)])
+                        vis = (not causal or t <= ctx + j) and not (window > 0 and ctx + j - t >= window)
+                        sc.append(0.5 * sum(q[tok, h, i] * key[i] for i in range(d)) if vis else -math.inf)
+                    m = max(sc)
+                    wts = [math.exp(x - m) for x in sc]
+                    z = sum(wts)
+                    for i in range(d):
+                        ref = sum(wts[t] * vals[t][i] for t in range(len(sc))) / z
+                        assert abs(out[tok, h, i] - ref) < 1e-12
+
+
+def test_int8_write_scatter_and_skips():
+    rng = np.random.default_rng(25)
+    T, hkv, d, nb = 10, 2, 16, 3
+    k = torch.from_numpy(rng.standard_normal((T, hkv, d))).to(torch.bfloat16).double().numpy()
+    v = torch.from_numpy(rng.standard_normal((T, hkv, d))).to(torch.bfloat16).double().numpy()
+    kc = np.full((nb, 16, hkv, d), 0x5A, np.int8)
+    vc = kc.copy()
+    ks = np.full((nb, 16, hkv), 9.0, np.float32)
+    vs = ks.copy()
+    slots = np.array([5, -1, 47, 0, 48, 16, 3, -7, 20, 33])
+    bad = O.write_cache_int8(k, v, slots, kc, vc, ks, vs, 16)
+    assert bad == [48]
+    ck, sk = O.quantize_int8(k)
+    for t, slot in enumerate(slots):
+        if 0 <= slot < nb * 16:
+            assert np.array_equal(kc[slot // 16, slot % 16], ck[t]) and np.array_equal(ks[slot // 16, slot % 16], sk[t])
+    written = {int(x) for x in slots if 0 <= x < nb * 16}
+    for slot in range(nb * 16):
+        if slot not in written:
+            assert np.all(kc[slot // 16, slot % 16] == 0x5A) and np.all(ks[slot // 16, slot % 16] == 9.0)
