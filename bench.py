@@ -218,12 +218,13 @@ def gpu_id_for_smi(dev_index: int) -> str:
         return str(dev_index)
 
 
-def bulk_write_bench(w, dev, n_chunks: int, chunk_tokens: int = 65536):
+def bulk_write_bench(w, dev, n_chunks: int, chunk_tokens: int = 65536, fmt: str = "int4"):
     """RHT + quantise write throughput: n_chunks pre-drawn 65,536-token chunks of
     this workload's shape (bf16 K and V, random slots of a scratch cache; the
     inputs, 2 x 65,536 x Hkv x d x 2 bytes per chunk, exceed L2) written back
     to back; one warm-up pass, then device time of a second pass by CUDA
-    events.  Algorithmic bytes: bf16 K,V in + codes and scales out + slots."""
+    events.  Algorithmic bytes: bf16 K,V in + codes and scales out + slots.
+    fmt "int8": the int8_per_token_head write (no rotation, d code bytes)."""
     import torch
     from int4_token_head_gb300 import _lib
     hkv, d, bs = w.num_kv_heads, w.head_size, w.block_size
@@ -233,22 +234,29 @@ def bulk_write_bench(w, dev, n_chunks: int, chunk_tokens: int = 65536):
     ks = [torch.randn((chunk_tokens, hkv, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_chunks)]
     vs = [torch.randn((chunk_tokens, hkv, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_chunks)]
     slots = [torch.randperm(nb * bs, generator=g, device=dev) for _ in range(n_chunks)]
-    kc = torch.empty((nb, bs, hkv, d // 2), dtype=torch.uint8, device=dev)
+    cb = d if fmt == "int8" else d // 2
+    kc = torch.empty((nb, bs, hkv, cb), dtype=torch.int8 if fmt == "int8" else torch.uint8, device=dev)
     vc = torch.empty_like(kc)
     ksc = torch.empty((nb, bs, hkv), dtype=torch.float32, device=dev)
     vsc = torch.empty_like(ksc)
     signs = w.signs.to(dev)
+
+    def one(i):
+        if fmt == "int8":
+            _lib.write_int8(ks[i], vs[i], slots[i], kc, vc, ksc, vsc)
+        else:
+            _lib.write(ks[i], vs[i], slots[i], kc, vc, ksc, vsc, signs)
     for i in range(n_chunks):
-        _lib.write(ks[i], vs[i], slots[i], kc, vc, ksc, vsc, signs)
+        one(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(n_chunks):
-        _lib.write(ks[i], vs[i], slots[i], kc, vc, ksc, vsc, signs)
+        one(i)
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n_chunks
-    nbytes = chunk_tokens * (2 * hkv * d * 2 + 2 * hkv * (d // 2 + 4) + 8)
+    nbytes = chunk_tokens * (2 * hkv * d * 2 + 2 * hkv * (cb + 4) + 8)
     del ks, vs, slots, kc, vc, ksc, vsc
     return {"gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "ms_per_chunk": round(ms, 4), "chunks": n_chunks,
             "tokens_per_chunk": chunk_tokens, "bytes_per_chunk": nbytes}
@@ -313,6 +321,43 @@ def window_bench(pk, q, out, window: int, iters: int):
         nbytes += keys * hkv * 2 * (d // 2 + 4) + 4 * ((keys + 15) // 16) + ql * hq * d * 2
     return {"window": window, "ms": round(ms, 5), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
             "algorithmic_bytes": nbytes}
+
+
+def int8_decode_bench(w, dev, iters: int):
+    """The int8_per_token_head mode on this workload: a second cache (int8
+    codes, no rotation) populated through kv_int8_write, then `iters`
+    attention calls; decode kernel time from the library's timer.
+    Algorithmic bytes as for INT4 with d code bytes per head vector."""
+    import torch
+    from int4_token_head_gb300 import _lib
+    from int4_token_head_gb300.paged import PagedKV
+    pk = PagedKV(w, device=str(dev), fmt="int8")
+    pk.populate_history(chunk_tokens=65536)
+    q, k_new, v_new, slots = pk.step_inputs()
+    out = torch.empty((w.num_q_tokens, w.num_q_heads, w.head_size), dtype=torch.bfloat16, device=dev)
+    pk.step(q, k_new, v_new, slots, out)
+    for _ in range(3):
+        pk.attend(q, out)
+    torch.cuda.synchronize()
+    _lib.timing_collect()
+    _lib.timing_enable(True)
+    for _ in range(iters):
+        pk.attend(q, out)
+    torch.cuda.synchronize()
+    kern = _lib.timing_collect()
+    _lib.timing_enable(False)
+    if pk.status.item() != 0:
+        raise RuntimeError(f"device status {pk.status.item()} in the int8 attention")
+    d, hkv, hq = w.head_size, w.num_kv_heads, w.num_q_heads
+    dom = "decode" if kern["decode"][0] >= kern["prefill"][0] else "prefill"
+    ms = kern[dom][0] / max(1, kern[dom][1])
+    nbytes = sum(kv * hkv * 2 * (d + 4) + 4 * ((kv + 15) // 16) + ql * hq * d * 2 for ql, kv in w.seqs)
+    step_ms = sum(kern[k][0] for k in ("prep", "prefill", "decode", "reduce")) / iters
+    del pk
+    torch.cuda.empty_cache()
+    return {"kernel": f"{dom}_kernel", "ms": round(ms, 5), "attention_ms": round(step_ms, 5),
+            "gbs": round(nbytes / (ms / 1e3) / 1e9, 1) if dom == "decode" else None,
+            "cache_bytes_read": nbytes}
 
 
 # ---------------------------------------------------------------------------
@@ -476,6 +521,8 @@ def run_ours(args):
     if pk.status.item() != 0:
         raise RuntimeError(f"device status {pk.status.item()} during the timed region")
     window_info = window_bench(pk, q, out, 4096, max(10, min(200, args.steps)))
+    int8_info = {"write": bulk_write_bench(w, dev, max(1, args.write_chunks), fmt="int8")}
+    int8_info.update(int8_decode_bench(w, dev, max(10, min(200, args.steps))))
 
     # ---- roofline of the dominant kernel ----
     peak, tc_peak, peak_kind = load_peaks()
@@ -513,6 +560,9 @@ def run_ours(args):
     write_info["step_write_us"] = round(kern["write"][0] / max(1, kern["write"][1]) * 1e3, 2)
     rht_info["frac"] = round(rht_info["gbs"] / peak, 4)
     window_info["frac"] = round(window_info["gbs"] / peak, 4)
+    int8_info["write"]["frac"] = round(int8_info["write"]["gbs"] / peak, 4)
+    if int8_info["gbs"]:
+        int8_info["frac"] = round(int8_info["gbs"] / peak, 4)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -529,6 +579,7 @@ def run_ours(args):
         "write": write_info,
         "rht": rht_info,
         "sliding_window": window_info,
+        "int8_per_token_head": int8_info,
         "kernels_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in kern.items()},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(sum(v[1] for v in kern.values())),

@@ -117,6 +117,30 @@ KVINT4_API int kv_int4_write_prerotated(const void* k, int64_t k_token_stride,
                              int32_t* dev_status, void* stream);
 
 /*
+ * kv_int8_write -- the int8_per_token_head sibling mode's write: quantise new
+ * K/V head vectors, without rotation, into a paged int8 cache.
+ *
+ * Defined by: "[Feature] Triton INT4 per-token-head KV cache quantization"
+ * (vLLM PR #40835), review thread (the int8 cache dtype of the per-token-head
+ * modes; the raw int8 cache compared with a round reference); "vLLM --
+ * Attention Kernels & KV Cache Quantization" (PR #56198), Merged
+ * contribution (int8_per_token_head never uses the transform).  Per (token t,
+ * kv head h) vector x of K and of V:
+ *   a = max |x_i|,  s = fp32(a / 127),  c_i = rne(x_i * fp32(1 / s))  (|c_i| <= 127)
+ * with s = 0 and c = 0 when a < 2^-119; c goes to cache[slot][h][:] (int8,
+ * one code per element) and s to scale[slot][h].
+ *
+ * Arguments, ownership, slot conventions and errors are those of
+ * kv_int4_write, except: k_cache / v_cache are int8 [num_blocks][block_size]
+ * [num_kv_heads][head_size] (16-byte aligned), there are no signs, and
+ * head_size is one of 64, 96, 128, 192, 256.
+ */
+KVINT4_API int kv_int8_write(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                             const int64_t* slot_mapping, int num_tokens, int8_t* k_cache, int8_t* v_cache,
+                             float* k_scale_cache, float* v_scale_cache, int num_blocks, int block_size,
+                             int num_kv_heads, int head_size, int32_t* dev_status, void* stream);
+
+/*
  * kv_int4_attention_workspace_size -- bytes of device workspace that
  * kv_int4_attention needs for these sizes (a pure host computation).  The
  * workspace holds the device-built schedule, the rotated queries and the
@@ -180,6 +204,35 @@ KVINT4_API int kv_int4_attention(const void* q, int64_t q_token_stride,
                       int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
                       void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
+
+/*
+ * kv_int8_attention -- attention over the int8_per_token_head cache written
+ * by kv_int8_write (the sibling mode: int8 codes of the unrotated vectors).
+ *
+ * Defined by: "[Feature] Triton INT4 per-token-head KV cache quantization"
+ * (vLLM PR #40835), review thread (the per-token-head modes share one
+ * unified attention; int8 caches); "vLLM -- Attention Kernels & KV Cache
+ * Quantization" (PR #56198), Merged contribution (this mode never uses the
+ * transform):
+ *   out[t][hq][:] = sum_p softmax_p(softmax_scale * q[t][hq] . k_hat_p) v_hat_p,
+ *   k_hat_p = c_p * s_p, v_hat_p likewise.
+ * Arguments, layouts, masks (causal, sliding_window), workspace
+ * (kv_int4_attention_workspace_size), device status bits and errors are
+ * those of kv_int4_attention, except: k_cache / v_cache are int8
+ * [num_blocks][block_size][num_kv_heads][head_size] (16-byte aligned) and
+ * there are no signs.
+ */
+KVINT4_API int kv_int8_attention(const void* q, int64_t q_token_stride,
+                                 const int8_t* k_cache, const int8_t* v_cache,
+                                 const float* k_scale_cache, const float* v_scale_cache,
+                                 const int32_t* block_table, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, const int32_t* query_start_loc,
+                                 int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len,
+                                 int num_q_heads, int num_kv_heads, int head_size,
+                                 int block_size, int num_blocks, float softmax_scale, int causal,
+                                 int sliding_window, void* out, int64_t out_token_stride,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, void* stream);
 
 /*
  * kv_int4_attention_noalloc -- kv_int4_attention without a caller-provided
@@ -281,8 +334,8 @@ KVINT4_API int kv_int4_timing_collect(double* ms, int* launches, int* dropped);
 /* kv_int4_status_string -- a static, human-readable name for a KV_INT4_* code. */
 KVINT4_API const char* kv_int4_status_string(int status);
 
-/* kv_int4_version -- the library's ABI version: 2 (kv_int4_rht added; the attention entry points
- * take sliding_window). */
+/* kv_int4_version -- the library's ABI version: 2 (kv_int4_rht and the int8_per_token_head entry
+ * points kv_int8_write / kv_int8_attention added; the attention entry points take sliding_window). */
 KVINT4_API int kv_int4_version(void);
 
 #ifdef __cplusplus

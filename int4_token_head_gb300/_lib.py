@@ -28,6 +28,8 @@ _SIGNATURES = {
     "kv_int4_write_prerotated": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p,
                                          c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                                          c_void_p]),
+    "kv_int8_write": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p, c_void_p,
+                              c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "kv_int4_attention_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "kv_int4_attention": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                                   c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
@@ -38,6 +40,10 @@ _SIGNATURES = {
                                           c_int, c_int, c_int, c_float, c_int, c_int, c_void_p, c_void_p, c_int64,
                                           c_void_p, c_void_p]),
     "kv_int4_rht": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_int, c_int64, c_int, c_void_p, c_int, c_void_p]),
+    "kv_int8_attention": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                  c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                  c_int, c_float, c_int, c_int, c_void_p, c_int64, c_void_p, c_size_t,
+                                  c_void_p, c_void_p]),
     "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
     "kv_int4_timing_enable": (c_int, [c_int]),
     "kv_int4_timing_collect": (c_int, [c_void_p, c_void_p, c_void_p]),
@@ -174,6 +180,31 @@ def rht(x, signs, inverse: bool = False, out: Optional[torch.Tensor] = None,
     return out
 
 
+def _cache_dims_int8(k_cache, v_cache, k_scale, v_scale):
+    _check(k_cache.dtype == torch.int8 and v_cache.dtype == torch.int8, "int8 caches must be int8")
+    _check(k_cache.dim() == 4 and k_cache.shape == v_cache.shape, "caches must be [blocks, block_size, heads, d]")
+    _check(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
+    nb, bs, hkv, d = k_cache.shape
+    for s in (k_scale, v_scale):
+        _check(s.dtype == torch.float32 and tuple(s.shape) == (nb, bs, hkv) and s.is_contiguous(),
+               "scale caches must be contiguous float32 [blocks, block_size, heads]")
+    return nb, bs, hkv, d
+
+
+def write_int8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+               dev_status: Optional[torch.Tensor] = None, stream=None):
+    """The int8_per_token_head write (no rotation) through kv_int8_write."""
+    nb, bs, hkv, d = _cache_dims_int8(k_cache, v_cache, k_scale, v_scale)
+    ks = _token_major(k, "k", hkv, d)
+    vs = _token_major(v, "v", hkv, d)
+    _check(k.shape[0] == v.shape[0] == slot_mapping.shape[0], "k, v and slot_mapping disagree on tokens")
+    _check(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), "slot_mapping must be contiguous int64")
+    code = load().kv_int8_write(_ptr(k), ks, _ptr(v), vs, _ptr(slot_mapping), int(k.shape[0]), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), nb, bs, hkv, d, _ptr(dev_status),
+                                _stream(stream))
+    _raise(code, "kv_int8_write")
+
+
 TIMED_KINDS = ("write", "prep", "prefill", "decode", "reduce")
 
 
@@ -256,3 +287,28 @@ def attention_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
                                          float(softmax_scale), int(bool(causal)), int(sliding_window),
                                          _ptr(signs), _ptr(out), os_, _ptr(dev_status), _stream(stream))
     _raise(code, "kv_int4_attention_noalloc")
+
+
+def attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, query_start_loc,
+                   max_query_len, max_seq_len, softmax_scale, causal, out, workspace,
+                   dev_status: Optional[torch.Tensor] = None, stream=None, sliding_window: int = 0):
+    """Attention over the int8_per_token_head cache through kv_int8_attention."""
+    nb, bs, hkv, d = _cache_dims_int8(k_cache, v_cache, k_scale, v_scale)
+    _check(q.dim() == 3 and q.shape[2] == d, "q must be [tokens, q_heads, d]")
+    hq = q.shape[1]
+    qs = _token_major(q, "q", hq, d)
+    os_ = _token_major(out, "out", hq, d)
+    _check(out.shape[0] == q.shape[0], "out must match q")
+    _check(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous(),
+           "block_table must be contiguous int32 [seqs, max_blocks]")
+    _check(seq_lens.dtype == torch.int32 and query_start_loc.dtype == torch.int32, "seq_lens/query_start_loc int32")
+    num_seqs = seq_lens.shape[0]
+    _check(query_start_loc.shape[0] == num_seqs + 1 and block_table.shape[0] == num_seqs, "metadata shapes")
+    _check(workspace.dtype == torch.uint8 and workspace.is_contiguous(), "workspace must be contiguous uint8")
+    code = load().kv_int8_attention(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                    _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+                                    _ptr(query_start_loc), int(num_seqs), int(q.shape[0]), int(max_query_len),
+                                    int(max_seq_len), int(hq), int(hkv), int(d), int(bs), int(nb),
+                                    float(softmax_scale), int(bool(causal)), int(sliding_window), _ptr(out), os_,
+                                    _ptr(workspace), int(workspace.numel()), _ptr(dev_status), _stream(stream))
+    _raise(code, "kv_int8_attention")

@@ -126,6 +126,23 @@ int kv_int4_write(const void* k, int64_t k_token_stride, const void* v, int64_t 
                   v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, signs, dev_status, stream, false);
 }
 
+int kv_int8_write(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                  const int64_t* slot_mapping, int num_tokens, int8_t* k_cache, int8_t* v_cache, float* k_scale_cache,
+                  float* v_scale_cache, int num_blocks, int block_size, int num_kv_heads, int head_size,
+                  int32_t* dev_status, void* stream) {
+  int e = validate_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens,
+                         reinterpret_cast<const uint8_t*>(k_cache), reinterpret_cast<const uint8_t*>(v_cache),
+                         k_scale_cache, v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, nullptr,
+                         false);
+  if (e != KV_INT4_OK || num_tokens == 0) return e;
+  if ((int64_t)num_blocks * block_size * num_kv_heads * head_size >= (1ll << 62)) return KV_INT4_ERR_SIZE;
+  if (current_device() < 0) return KV_INT4_ERR_CUDA;
+  WriteArgs a{k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, reinterpret_cast<uint8_t*>(k_cache),
+              reinterpret_cast<uint8_t*>(v_cache), k_scale_cache, v_scale_cache, num_blocks, block_size,
+              num_kv_heads, head_size, nullptr, dev_status};
+  return launch_write_int8(a, static_cast<cudaStream_t>(stream));
+}
+
 int kv_int4_write_prerotated(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
                              const int64_t* slot_mapping, int num_tokens, uint8_t* k_cache, uint8_t* v_cache,
                              float* k_scale_cache, float* v_scale_cache, int num_blocks, int block_size,
@@ -142,13 +159,13 @@ size_t kv_int4_attention_workspace_size(int num_seqs, int num_q_tokens, int num_
   return L.total;
 }
 
-int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_cache, const uint8_t* v_cache,
-                      const float* k_scale_cache, const float* v_scale_cache, const int32_t* block_table,
-                      int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc,
-                      int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
-                      int num_kv_heads, int head_size, int block_size, int num_blocks, float softmax_scale,
-                      int causal, int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
-                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+static int do_attention(const void* q, int64_t q_token_stride, const uint8_t* k_cache, const uint8_t* v_cache,
+                        const float* k_scale_cache, const float* v_scale_cache, const int32_t* block_table,
+                        int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc,
+                        int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
+                        int num_kv_heads, int head_size, int block_size, int num_blocks, float softmax_scale,
+                        int causal, int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream, bool int8) {
   if (num_seqs < 0 || num_q_tokens < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0 ||
       max_blocks_per_seq < 0 || sliding_window < 0)
     return KV_INT4_ERR_SIZE;
@@ -157,7 +174,7 @@ int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_ca
   if (block_size != 16) return KV_INT4_ERR_BLOCK_SIZE;
   if (num_seqs == 0 || num_q_tokens == 0) return KV_INT4_OK;
   if (!q || !k_cache || !v_cache || !k_scale_cache || !v_scale_cache || !block_table || !seq_lens ||
-      !query_start_loc || !signs || !out || !workspace)
+      !query_start_loc || (!int8 && !signs) || !out || !workspace)
     return !workspace ? KV_INT4_ERR_WORKSPACE : KV_INT4_ERR_NULL;
   if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || (q_token_stride % 8) ||
       (out_token_stride % 8) || q_token_stride < 0 || out_token_stride < 0 || ((uintptr_t)workspace & 255u))
@@ -171,9 +188,37 @@ int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_ca
   AttnArgs a{q, q_token_stride, k_cache, v_cache, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
              seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len, max_seq_len, num_q_heads,
              num_kv_heads, head_size, block_size, num_blocks, softmax_scale, causal, sliding_window, signs, out,
-             out_token_stride,
-             workspace, workspace_bytes, dev_status};
+             out_token_stride, workspace, workspace_bytes, dev_status, int8};
   return launch_attention(a, static_cast<cudaStream_t>(stream));
+}
+
+int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_cache, const uint8_t* v_cache,
+                      const float* k_scale_cache, const float* v_scale_cache, const int32_t* block_table,
+                      int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc,
+                      int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
+                      int num_kv_heads, int head_size, int block_size, int num_blocks, float softmax_scale,
+                      int causal, int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return do_attention(q, q_token_stride, k_cache, v_cache, k_scale_cache, v_scale_cache, block_table,
+                      max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len,
+                      max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
+                      causal, sliding_window, signs, out, out_token_stride, workspace, workspace_bytes, dev_status,
+                      stream, false);
+}
+
+int kv_int8_attention(const void* q, int64_t q_token_stride, const int8_t* k_cache, const int8_t* v_cache,
+                      const float* k_scale_cache, const float* v_scale_cache, const int32_t* block_table,
+                      int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc,
+                      int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
+                      int num_kv_heads, int head_size, int block_size, int num_blocks, float softmax_scale,
+                      int causal, int sliding_window, void* out, int64_t out_token_stride, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return do_attention(q, q_token_stride, reinterpret_cast<const uint8_t*>(k_cache),
+                      reinterpret_cast<const uint8_t*>(v_cache), k_scale_cache, v_scale_cache, block_table,
+                      max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len,
+                      max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
+                      causal, sliding_window, nullptr, out, out_token_stride, workspace, workspace_bytes, dev_status,
+                      stream, true);
 }
 
 }  // extern "C"

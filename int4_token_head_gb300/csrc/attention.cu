@@ -71,6 +71,11 @@ static PlanView plan_view(void* ws, const WorkspaceLayout& L) {
   return v;
 }
 
+// KV cache formats: INT4 codes of the rotated vectors, two per byte (the
+// method), or int8 codes of the unrotated vectors (the int8_per_token_head
+// sibling mode).
+enum KvFmt { kFmtInt4 = 0, kFmtInt8 = 1 };
+
 struct Common {
   const uint16_t* q;
   int64_t q_stride;
@@ -148,7 +153,7 @@ __device__ T block_exclusive_scan(T v, T* total, T* sbuf /*[kPrepThreads/32]*/) 
   return before + x - v;
 }
 
-template <int D>
+template <int D, bool ROT>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView pv) {
   if (blockIdx.x == 0) {
     __shared__ int32_t s_i32[kPrepThreads / 32];
@@ -221,8 +226,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
 #pragma unroll
   for (int k = 0; k < PER; k++) {
     const float v = __uint_as_float((uint32_t)src[lane + 32 * k] << 16);
-    x[k] = c.signs[lane + 32 * k] < 0 ? -v : v;
+    x[k] = (ROT && c.signs[lane + 32 * k] < 0) ? -v : v;
   }
+  if constexpr (ROT) {
 #pragma unroll
   for (int hh = 1; hh < B && hh < 32; hh <<= 1) {
     const float f = (lane & hh) ? -1.f : 1.f;  // upper element: partner - self
@@ -240,6 +246,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
       }
     }
   }
+  }
   __half* dst = pv.qrot + row * D;
 #pragma unroll
   for (int k = 0; k < PER; k++) dst[lane + 32 * k] = __float2half_rn(x[k] * c.qscale);
@@ -254,24 +261,25 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
 // one softmax pass, one barrier and one V offset correction serve NP blocks.
 // Each column keeps its own running (m, l, o'); the reduce kernel merges the
 // NP columns of a query with the log-sum-exp rule like any other split.
-template <int D, int NP>
+template <int D, int NP, int FMT>
 struct DecGeom {
   static constexpr int COLS = kDecodeCols / NP;  // query columns per block
   // ring of single-block slots: NP consumed per iteration, the rest in flight
   static constexpr int NS = NP == 1 ? 4 : 2 * NP + 1;
   static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
-  static constexpr int KROW = D / 2;        // K tile row stride (bytes)
+  static constexpr int CB = FMT == kFmtInt8 ? D : D / 2;  // code bytes per head vector
+  static constexpr int KROW = CB;           // K tile row stride (bytes)
   // V tile row stride: an odd multiple of 16 bytes, so that the 8 rows of
   // an ldmatrix piece fall in distinct bank groups
-  static constexpr int VROW = (D / 32) % 2 ? D / 2 : D / 2 + 16;
+  static constexpr int VROW = (CB / 16) % 2 ? CB : CB + 16;
   static constexpr int KTILE = 16 * KROW;
   static constexpr int VTILE = 16 * VROW;
   // one head's K and V codes of one block, padded to 64 mod 128 bytes so that
   // the copies of neighbouring heads' rows fall in different bank halves
   static constexpr int HTILE = ((KTILE + VTILE + 63) / 128) * 128 + 64;
-  static constexpr int KW = D / 32;     // K words per row per thread (quarter row)
-  static constexpr int KSTEPS = D / 16;
-  static constexpr int CHR = D / 32;    // 16-byte chunks per code row
+  static constexpr int KW = CB / 16;    // K words per row per thread (quarter row)
+  static constexpr int KSTEPS = D / 16; // MMA k-steps of a block's K (and m-tiles of its V)
+  static constexpr int CHR = CB / 16;   // 16-byte chunks per code row
   // per slot: hg head tiles, then scales [K/V][hg][16]
   __host__ __device__ static constexpr int slot_bytes(int hg) { return hg * (HTILE + 128); }
   __host__ __device__ static constexpr int smem_bytes(int hg) { return NS * slot_bytes(hg) + 32; }
@@ -333,45 +341,58 @@ __device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint8_t* p) {
 
 // O'^T += V^T P'^T.  ldmatrix.trans of an 8-key x 16-byte piece of the V
 // tile gives each lane one word holding bytes (2g, 2g+1) of keys 2cq and
-// 2cq+1, so one lop3 yields an A-fragment register (two keys, one head
+// 2cq+1.
+// INT4: one lop3 yields an A-fragment register (two keys, one head
 // dimension) and a shift by 8 exposes the second byte.  Chunk ch (bytes
 // [16 ch, 16 ch + 16) of each V row) feeds m-tiles 2 ch and 2 ch + 1, whose
 // rows g and g + 8 are head dimensions 32 ch + 4g + 2e and 32 ch + 4g + 2e + 1
-// (e = 0, 1; the odd ones carry the factor 16 of the high nibble).  With CORR
-// the block's offset correction follows every m-tile's MMA.
-template <int D, bool CORR>
+// (e = 0, 1; the odd ones carry the factor 16 of the high nibble).
+// int8: the word, made offset-binary by an xor, gives its two head
+// dimensions' registers by one byte permute each (0x64nn is 1024 + nn):
+// chunk ch feeds m-tile ch, rows g and g + 8 being dimensions 16 ch + 2g and
+// 16 ch + 2g + 1.  With CORR the block's offset correction follows every
+// m-tile's MMA.
+template <int D, bool CORR, int FMT>
 __device__ __forceinline__ void pv_mma_chunk(float (&oacc)[D / 16][4], int ch, uint32_t r_lo, uint32_t r_hi,
                                              uint32_t b0, uint32_t b1, const uint32_t (&vcorr)[4]) {
-  const uint32_t s_lo = r_lo >> 8, s_hi = r_hi >> 8;
-  const uint32_t a0[4] = {nib_lo(r_lo), nib_hi(r_lo), nib_lo(r_hi), nib_hi(r_hi)};
-  mma_16816(oacc[2 * ch], a0, b0, b1);
-  if constexpr (CORR) mma_16816(oacc[2 * ch], vcorr, b0, b1);
-  const uint32_t a1[4] = {nib_lo(s_lo), nib_hi(s_lo), nib_lo(s_hi), nib_hi(s_hi)};
-  mma_16816(oacc[2 * ch + 1], a1, b0, b1);
-  if constexpr (CORR) mma_16816(oacc[2 * ch + 1], vcorr, b0, b1);
+  if constexpr (FMT == kFmtInt4) {
+    const uint32_t s_lo = r_lo >> 8, s_hi = r_hi >> 8;
+    const uint32_t a0[4] = {nib_lo(r_lo), nib_hi(r_lo), nib_lo(r_hi), nib_hi(r_hi)};
+    mma_16816(oacc[2 * ch], a0, b0, b1);
+    if constexpr (CORR) mma_16816(oacc[2 * ch], vcorr, b0, b1);
+    const uint32_t a1[4] = {nib_lo(s_lo), nib_hi(s_lo), nib_lo(s_hi), nib_hi(s_hi)};
+    mma_16816(oacc[2 * ch + 1], a1, b0, b1);
+    if constexpr (CORR) mma_16816(oacc[2 * ch + 1], vcorr, b0, b1);
+  } else {
+    const uint32_t lo = r_lo ^ 0x80808080u, hi = r_hi ^ 0x80808080u;
+    const uint32_t a[4] = {__byte_perm(lo, kBytes64, 0x4240), __byte_perm(lo, kBytes64, 0x4341),
+                           __byte_perm(hi, kBytes64, 0x4240), __byte_perm(hi, kBytes64, 0x4341)};
+    mma_16816(oacc[ch], a, b0, b1);
+    if constexpr (CORR) mma_16816(oacc[ch], vcorr, b0, b1);
+  }
 }
 
 // vaddr: shared address of this lane's ldmatrix row in chunk pair 0 (lane l
 // addresses key 8 ((l >> 3) & 1) + (l & 7) of chunk (l >> 4))
-template <int D, bool CORR>
+template <int D, bool CORR, int FMT>
 __device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], uint32_t vaddr, uint32_t b0, uint32_t b1,
                                         const uint32_t (&vcorr)[4]) {
-  constexpr int CH = D / 32;  // 16-byte chunks per V row
+  constexpr int CH = (FMT == kFmtInt8 ? D : D / 2) / 16;  // 16-byte chunks per V row
 #pragma unroll
   for (int p = 0; p < CH / 2; p++) {
     uint32_t r[4];
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(vaddr + p * 32));
-    pv_mma_chunk<D, CORR>(oacc, 2 * p, r[0], r[1], b0, b1, vcorr);
-    pv_mma_chunk<D, CORR>(oacc, 2 * p + 1, r[2], r[3], b0, b1, vcorr);
+    pv_mma_chunk<D, CORR, FMT>(oacc, 2 * p, r[0], r[1], b0, b1, vcorr);
+    pv_mma_chunk<D, CORR, FMT>(oacc, 2 * p + 1, r[2], r[3], b0, b1, vcorr);
   }
   if constexpr (CH % 2) {
     uint32_t r[2];
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
                  : "=r"(r[0]), "=r"(r[1])
                  : "r"(vaddr + (CH / 2) * 32));
-    pv_mma_chunk<D, CORR>(oacc, CH - 1, r[0], r[1], b0, b1, vcorr);
+    pv_mma_chunk<D, CORR, FMT>(oacc, CH - 1, r[0], r[1], b0, b1, vcorr);
   }
 }
 
@@ -401,9 +422,10 @@ struct DecParams {
 // removes that position's offset, so the running accumulator only ever holds
 // one block's worth of offset per column (accumulating the offset over
 // thousands of keys would cost the fp32 accumulator the signal's low bits).
-template <int D, int NP>
+template <int D, int NP, int FMT>
 __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
-  using G = DecGeom<D, NP>;
+  using G = DecGeom<D, NP, FMT>;
+  constexpr bool I8 = FMT == kFmtInt8;
   const Common& c = prm.c;
   const PlanView& pv = prm.pv;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -458,14 +480,14 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const int kvr = rest / HG;
     const int kv = kvr / 16, r = kvr % 16;
     c_saddr[j] = smem_addr(smem) + h * G::HTILE + (kv ? G::KTILE + r * G::VROW : r * G::KROW) + col * 16;
-    c_src[j] = (kv ? c.v_cache : c.k_cache) + ((long long)r * c.hkv + h) * (D / 2) + col * 16;
+    c_src[j] = (kv ? c.v_cache : c.k_cache) + ((long long)r * c.hkv + h) * G::CB + col * 16;
   }
   // one 4-byte scale per thread: [K/V][row][h]
   const int s_kv = tid / (16 * HG), s_rem = tid % (16 * HG);
   const int s_r = s_rem / HG, s_h = s_rem % HG;
   const uint32_t s_saddr = smem_addr(smem) + HG * G::HTILE + (s_kv * HG + s_h) * 64 + s_r * 4;
   const float* s_src = (s_kv ? c.v_scale : c.k_scale) + (long long)s_r * c.hkv + s_h;
-  const uint32_t blk_bytes = 16u * c.hkv * (D / 2);  // < 2^32 (host-checked head counts)
+  const uint32_t blk_bytes = 16u * c.hkv * G::CB;  // < 2^32 (host-checked head counts)
   const uint32_t blk_scales = 16u * c.hkv;
 
   // block j of a position, or kAbsent past the end of the sequence (NP > 1)
@@ -478,7 +500,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const bool ok = blk >= 0 && blk < c.num_blocks;
     if (ok) {
       const uint32_t soff = (uint32_t)(slot * SB);
-      const uint32_t goff = (uint32_t)(grp * HG * (D / 2));
+      const uint32_t goff = (uint32_t)(grp * HG * G::CB);
 #pragma unroll
       for (int j = 0; j < G::CHR; j++) {
         const uint8_t* src = c_src[j] + (uint64_t)(uint32_t)blk * blk_bytes + goff;
@@ -535,21 +557,33 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const bool colok = n < ql * c.group;
     const int j = n / c.group, jj = n - j * c.group;
     const __half* qrow = pv.qrot + ((long long)(q0 + (colok ? j : 0)) * c.hq + head * c.group + (colok ? jj : 0)) * D;
-    const __half2 x16 = __float2half2_rn(16.f);
+    if constexpr (!I8) {
+      const __half2 x16 = __float2half2_rn(16.f);
 #pragma unroll
-    for (int w = 0; w < G::KW; w++) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (colok) v = *reinterpret_cast<const uint4*>(qrow + 8 * (cq * G::KW + w));
-      uint32_t lo0 = __byte_perm(v.x, v.z, 0x5410), lo1 = __byte_perm(v.y, v.w, 0x5410);
-      __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&lo0), x16);
-      __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&lo1), x16);
-      qb[2 * w][0] = *reinterpret_cast<uint32_t*>(&h0);
-      qb[2 * w][1] = __byte_perm(v.x, v.z, 0x7632);
-      qb[2 * w + 1][0] = *reinterpret_cast<uint32_t*>(&h1);
-      qb[2 * w + 1][1] = __byte_perm(v.y, v.w, 0x7632);
+      for (int w = 0; w < G::KW; w++) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (colok) v = *reinterpret_cast<const uint4*>(qrow + 8 * (cq * G::KW + w));
+        uint32_t lo0 = __byte_perm(v.x, v.z, 0x5410), lo1 = __byte_perm(v.y, v.w, 0x5410);
+        __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&lo0), x16);
+        __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&lo1), x16);
+        qb[2 * w][0] = *reinterpret_cast<uint32_t*>(&h0);
+        qb[2 * w][1] = __byte_perm(v.x, v.z, 0x7632);
+        qb[2 * w + 1][0] = *reinterpret_cast<uint32_t*>(&h1);
+        qb[2 * w + 1][1] = __byte_perm(v.y, v.w, 0x7632);
+      }
+    } else {
+      // k-step s of this lane's quarter: dimensions cq D/4 + 4s + {0, 1} and + {2, 3}
+#pragma unroll
+      for (int w = 0; w < G::KW; w++) {
+        uint2 v = make_uint2(0, 0);
+        if (colok) v = *reinterpret_cast<const uint2*>(qrow + cq * (D / 4) + 4 * w);
+        qb[w][0] = v.x;
+        qb[w][1] = v.y;
+      }
     }
     float bacc[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t abias[4] = {kF16x2_1032, kF16x2_1032, kF16x2_1152, kF16x2_1152};
+    const uint32_t abias[4] = {I8 ? kF16x2_1152 : kF16x2_1032, I8 ? kF16x2_1152 : kF16x2_1032, kF16x2_1152,
+                               kF16x2_1152};
 #pragma unroll
     for (int s = 0; s < G::KSTEPS; s++) mma_16816(bacc, abias, qb[s][0], qb[s][1]);
     bias0 = bacc[0];
@@ -591,15 +625,26 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
       dst_o = pv.warp_o + slot * kDecodeCols * D;
       dst_ml = pv.warp_ml + slot * kDecodeCols * 2;
     }
-    // m-tiles 2ch, 2ch+1 hold d = 32 ch + 4g + {0, 1, 2, 3} (odd d scaled by 16)
-    float* o0 = dst_o + (2 * cq) * D + 4 * g;
-    float* o1 = dst_o + (2 * cq + 1) * D + 4 * g;
+    if constexpr (!I8) {
+      // m-tiles 2ch, 2ch+1 hold d = 32 ch + 4g + {0, 1, 2, 3} (odd d scaled by 16)
+      float* o0 = dst_o + (2 * cq) * D + 4 * g;
+      float* o1 = dst_o + (2 * cq + 1) * D + 4 * g;
 #pragma unroll
-    for (int i = 0; i < G::KSTEPS; i += 2) {
-      *reinterpret_cast<float4*>(o0 + 16 * i) =
-          make_float4(oacc[i][0], oacc[i][2] * 0.0625f, oacc[i + 1][0], oacc[i + 1][2] * 0.0625f);
-      *reinterpret_cast<float4*>(o1 + 16 * i) =
-          make_float4(oacc[i][1], oacc[i][3] * 0.0625f, oacc[i + 1][1], oacc[i + 1][3] * 0.0625f);
+      for (int i = 0; i < G::KSTEPS; i += 2) {
+        *reinterpret_cast<float4*>(o0 + 16 * i) =
+            make_float4(oacc[i][0], oacc[i][2] * 0.0625f, oacc[i + 1][0], oacc[i + 1][2] * 0.0625f);
+        *reinterpret_cast<float4*>(o1 + 16 * i) =
+            make_float4(oacc[i][1], oacc[i][3] * 0.0625f, oacc[i + 1][1], oacc[i + 1][3] * 0.0625f);
+      }
+    } else {
+      // m-tile t holds d = 16 t + 2g (row g) and 16 t + 2g + 1 (row g + 8)
+      float* o0 = dst_o + (2 * cq) * D + 2 * g;
+      float* o1 = dst_o + (2 * cq + 1) * D + 2 * g;
+#pragma unroll
+      for (int i = 0; i < G::KSTEPS; i++) {
+        *reinterpret_cast<float2*>(o0 + 16 * i) = make_float2(oacc[i][0], oacc[i][2]);
+        *reinterpret_cast<float2*>(o1 + 16 * i) = make_float2(oacc[i][1], oacc[i][3]);
+      }
     }
     if (g == 0) {
       dst_ml[(2 * cq) * 2 + 0] = m0;
@@ -617,8 +662,9 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
                           (((lane >> 3) & 1) * 8 + (lane & 7)) * G::VROW + (lane >> 4) * 16;
   int cs = 0;                     // slot of the iteration's first block
   const int nunits = (int)(P1 - P0);
-  // rows g (even d: offset 1032) and g + 8 (odd d: offset 1152)
-  const uint32_t vcorr[4] = {kF16x2_M1032, kF16x2_M1152, kF16x2_M1032, kF16x2_M1152};
+  // INT4: rows g (even d: offset 1032) and g + 8 (odd d: offset 1152); int8: 1152
+  const uint32_t vcorr[4] = {I8 ? kF16x2_M1152 : kF16x2_M1032, kF16x2_M1152, I8 ? kF16x2_M1152 : kF16x2_M1032,
+                             kF16x2_M1152};
 #pragma unroll 1
   for (int it = 0; it < nunits; it++) {
     cp_async_wait<G::WAIT>();
@@ -649,15 +695,23 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
       sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
       const uint8_t* st = smem + slot[j] * SB + hl * G::HTILE;
       uint32_t xk[G::KW], yk[G::KW];
-      lds_words<G::KW, D / 8>(xk, st + g * G::KROW + cq * (D / 8));
-      lds_words<G::KW, D / 8>(yk, st + (g + 8) * G::KROW + cq * (D / 8));
+      lds_words<G::KW, G::CB / 4>(xk, st + g * G::KROW + cq * (G::CB / 4));
+      lds_words<G::KW, G::CB / 4>(yk, st + (g + 8) * G::KROW + cq * (G::CB / 4));
 #pragma unroll
       for (int w = 0; w < G::KW; w++) {
-        const uint32_t x = xk[w], y = yk[w], x8 = x >> 8, y8 = y >> 8;
-        const uint32_t a0[4] = {nib_lo(x), nib_lo(y), nib_hi(x), nib_hi(y)};
-        mma_16816(sacc[j], a0, qb[2 * w][0], qb[2 * w][1]);
-        const uint32_t a1[4] = {nib_lo(x8), nib_lo(y8), nib_hi(x8), nib_hi(y8)};
-        mma_16816(sacc[j], a1, qb[2 * w + 1][0], qb[2 * w + 1][1]);
+        if constexpr (!I8) {
+          const uint32_t x = xk[w], y = yk[w], x8 = x >> 8, y8 = y >> 8;
+          const uint32_t a0[4] = {nib_lo(x), nib_lo(y), nib_hi(x), nib_hi(y)};
+          mma_16816(sacc[j], a0, qb[2 * w][0], qb[2 * w][1]);
+          const uint32_t a1[4] = {nib_lo(x8), nib_lo(y8), nib_hi(x8), nib_hi(y8)};
+          mma_16816(sacc[j], a1, qb[2 * w + 1][0], qb[2 * w + 1][1]);
+        } else {
+          // four int8 codes of key g (x) and key g + 8 (y): 1152 + c per f16
+          const uint32_t x = xk[w] ^ 0x80808080u, y = yk[w] ^ 0x80808080u;
+          const uint32_t a[4] = {__byte_perm(x, kBytes64, 0x4140), __byte_perm(y, kBytes64, 0x4140),
+                                 __byte_perm(x, kBytes64, 0x4342), __byte_perm(y, kBytes64, 0x4342)};
+          mma_16816(sacc[j], a, qb[w][0], qb[w][1]);
+        }
       }
     }
     float sa[4] = {sacc[0][0], sacc[0][1], sacc[0][2], sacc[0][3]};
@@ -668,7 +722,8 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
 
     const int kb0 = cw.fb + cw.kp * NP;
     const int pos0 = (kb0 + jb) * 16 + g, pos1 = pos0 + 8;
-    const float ks0 = sks[g] * 0.0625f, ks1 = sks[g + 8] * 0.0625f;
+    // INT4 scores carry the factor 16 of q' at the low-nibble positions
+    const float ks0 = sks[g] * (I8 ? 1.f : 0.0625f), ks1 = sks[g + 8] * (I8 ? 1.f : 0.0625f);
     float s00 = (sa[0] - bias0) * ks0, s01 = (sa[1] - bias1) * ks0;
     float s10 = (sa[2] - bias0) * ks1, s11 = (sa[3] - bias1) * ks1;
     // keys outside a column's visible range [lo, lim) (or in an invalid or
@@ -725,13 +780,13 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
 
     // ---- O'^T += V^T P'^T (offset removed per position) ----
     if constexpr (NP == 1) {
-      pv_mmas<D, true>(oacc, v_lane + slot[0] * SB, b0, b1, vcorr);
+      pv_mmas<D, true, FMT>(oacc, v_lane + slot[0] * SB, b0, b1, vcorr);
     } else {
 #pragma unroll
       for (int j = 0; j < NP; j++) {
         // block j's probabilities only: the other blocks' columns are zero
         const uint32_t bj0 = jv == j ? b0 : 0u, bj1 = jv == j ? b1 : 0u;
-        pv_mmas<D, false>(oacc, v_lane + slot[j] * SB, bj0, bj1, vcorr);
+        pv_mmas<D, false, FMT>(oacc, v_lane + slot[j] * SB, bj0, bj1, vcorr);
       }
 #pragma unroll
       for (int i = 0; i < G::KSTEPS; i++) mma_16816(oacc[i], vcorr, b0, b1);
@@ -762,7 +817,7 @@ struct RedParams {
   int num_ctas;
 };
 
-template <int D>
+template <int D, bool ROT>
 __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm) {
   const Common& c = prm.c;
   const PlanView& pv = prm.pv;
@@ -824,25 +879,27 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
     }
   }
   float* r = srow[col];
-  const float inv = 1.f / (Lsum * (float)B);
+  const float inv = 1.f / (Lsum * (ROT ? (float)B : 1.f));
 #pragma unroll
   for (int k = 0; k < PER; k++) r[lane + 32 * k] = acc[k] * inv;
   __syncwarp();
+  if constexpr (ROT) {
 #pragma unroll 1
-  for (int hh = 1; hh < B; hh <<= 1) {
-    for (int p = lane; p < D / 2; p += 32) {
-      const int ii = (p / hh) * 2 * hh + (p % hh);
-      const float a = r[ii], b = r[ii + hh];
-      r[ii] = a + b;
-      r[ii + hh] = a - b;
+    for (int hh = 1; hh < B; hh <<= 1) {
+      for (int p = lane; p < D / 2; p += 32) {
+        const int ii = (p / hh) * 2 * hh + (p % hh);
+        const float a = r[ii], b = r[ii + hh];
+        r[ii] = a + b;
+        r[ii + hh] = a - b;
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
   const int j = col / c.group, jj = col - j * c.group;
   uint16_t* dst = c.out + (long long)(q0 + j) * c.out_stride + (long long)(h * c.group + jj) * D;
   for (int p = lane; p < D / 2; p += 32) {
-    const float x0 = c.signs[2 * p] < 0 ? -r[2 * p] : r[2 * p];
-    const float x1 = c.signs[2 * p + 1] < 0 ? -r[2 * p + 1] : r[2 * p + 1];
+    const float x0 = (ROT && c.signs[2 * p] < 0) ? -r[2 * p] : r[2 * p];
+    const float x1 = (ROT && c.signs[2 * p + 1] < 0) ? -r[2 * p + 1] : r[2 * p + 1];
     reinterpret_cast<uint32_t*>(dst)[p] = pack_bf16x2_rn(x0, x1);
   }
 }
@@ -850,13 +907,14 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
 // ---------------------------------------------------------------------------
 // 2. prefill: FA2-style, 64 query rows x 16 keys per step, mma.sync
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, int FMT>
 struct PreGeom {
   static constexpr int WARPS = 4;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int ROWS = kPrefillRows;  // 16 per warp
   static constexpr int STAGES = 3;
-  static constexpr int TILE = 16 * D / 2;
+  static constexpr int CB = FMT == kFmtInt8 ? D : D / 2;  // code bytes per head vector
+  static constexpr int TILE = 16 * CB;
   static constexpr int STAGE = 2 * TILE + 2 * 16 * 4;
   static constexpr int HSTRIDE = D + 8;  // halves per row of the f16 tiles (odd multiple of 16 B)
   static constexpr int SMEM = STAGES * STAGE + ROWS * HSTRIDE * 2 + 2 * 16 * HSTRIDE * 2 + D * 4 + 64;
@@ -867,9 +925,10 @@ struct PreParams {
   PlanView pv;
 };
 
-template <int D>
-__global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams prm) {
-  using G = PreGeom<D>;
+template <int D, int FMT>
+__global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PreParams prm) {
+  using G = PreGeom<D, FMT>;
+  constexpr bool ROT = FMT == kFmtInt4;
   constexpr int B = Head<D>::b;
   constexpr int NT = D / 8;  // n-tiles of the output
   const Common& c = prm.c;
@@ -884,7 +943,7 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
-  for (int i = tid; i < D; i += G::THREADS) ssign[i] = c.signs[i] < 0 ? -1.f : 1.f;
+  for (int i = tid; i < D; i += G::THREADS) ssign[i] = (ROT && c.signs[i] < 0) ? -1.f : 1.f;
   const int n_items = pv.plan[1], n_pseq = pv.plan[3];
 
 #pragma unroll 1
@@ -936,11 +995,11 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
       const int blk = c.block_table[(long long)seq * c.max_blocks + kb];
       if (blk < 0 || blk >= c.num_blocks) return;  // reported and masked by the consumer
       const long long row0 = (long long)blk * 16;
-      for (int q = tid; q < D / 2; q += G::THREADS) {
-        const int r = q / (D / 32), col = q - r * (D / 32);
-        const long long goff = ((row0 + r) * c.hkv + h) * (D / 2) + col * 16;
-        cp_async16(st + r * (D / 2) + col * 16, c.k_cache + goff);
-        cp_async16(st + G::TILE + r * (D / 2) + col * 16, c.v_cache + goff);
+      for (int q = tid; q < G::CB; q += G::THREADS) {  // 16 rows x CB/16 chunks
+        const int r = q / (G::CB / 16), col = q - r * (G::CB / 16);
+        const long long goff = ((row0 + r) * c.hkv + h) * G::CB + col * 16;
+        cp_async16(st + r * G::CB + col * 16, c.k_cache + goff);
+        cp_async16(st + G::TILE + r * G::CB + col * 16, c.v_cache + goff);
       }
       if (tid < 32) {
         const int r = tid & 15;
@@ -980,21 +1039,34 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
       if (!bok && tid == 0) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
       const uint8_t* st = stages + stage * G::STAGE;
       // dequantise K and V codes of this block into f16 rows (natural order)
-      for (int q = tid; q < 2 * 16 * (D / 8); q += G::THREADS) {
-        const int which = q / (16 * (D / 8));
-        const int rem = q - which * 16 * (D / 8);
-        const int r = rem / (D / 8), w = rem - r * (D / 8);
-        const uint32_t x = bok ? reinterpret_cast<const uint32_t*>(st + which * G::TILE + r * (D / 2))[w] : 0x88888888u;
-        const uint32_t p0 = nib_to_f16x2(x), p1 = nib_to_f16x2(x >> 4), p2 = nib_to_f16x2(x >> 8),
-                       p3 = nib_to_f16x2(x >> 12);
-        // p_k = (element k, element k+4) -> natural order 0..7
-        uint4 o;
-        o.x = __byte_perm(p0, p1, 0x5410);
-        o.y = __byte_perm(p2, p3, 0x5410);
-        o.z = __byte_perm(p0, p1, 0x7632);
-        o.w = __byte_perm(p2, p3, 0x7632);
-        __half* dst = (which ? sV : sK) + r * G::HSTRIDE + w * 8;
-        *reinterpret_cast<uint4*>(dst) = o;
+      constexpr int WPR = G::CB / 4;  // code words per row
+      for (int q = tid; q < 2 * 16 * WPR; q += G::THREADS) {
+        const int which = q / (16 * WPR);
+        const int rem = q - which * 16 * WPR;
+        const int r = rem / WPR, w = rem - r * WPR;
+        const uint32_t x0 = bok ? reinterpret_cast<const uint32_t*>(st + which * G::TILE + r * G::CB)[w] : 0u;
+        __half* dst = (which ? sV : sK) + r * G::HSTRIDE;
+        if constexpr (ROT) {
+          const uint32_t x = bok ? x0 : 0x88888888u;
+          const uint32_t p0 = nib_to_f16x2(x), p1 = nib_to_f16x2(x >> 4), p2 = nib_to_f16x2(x >> 8),
+                         p3 = nib_to_f16x2(x >> 12);
+          // p_k = (element k, element k+4) -> natural order 0..7
+          uint4 o;
+          o.x = __byte_perm(p0, p1, 0x5410);
+          o.y = __byte_perm(p2, p3, 0x5410);
+          o.z = __byte_perm(p0, p1, 0x7632);
+          o.w = __byte_perm(p2, p3, 0x7632);
+          *reinterpret_cast<uint4*>(dst + w * 8) = o;
+        } else {
+          // four int8 codes: 0x64uu (u = c + 128) is 1024 + u, minus 1152 is c, exactly
+          const uint32_t x = x0 ^ 0x80808080u;
+          const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6480),
+                                             __ushort_as_half((unsigned short)0x6480));  // 1152
+          uint32_t h01 = __byte_perm(x, kBytes64, 0x4140), h23 = __byte_perm(x, kBytes64, 0x4342);
+          __half2 a = __hsub2(*reinterpret_cast<__half2*>(&h01), off), b = __hsub2(*reinterpret_cast<__half2*>(&h23), off);
+          *reinterpret_cast<uint2*>(dst + w * 4) =
+              make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+        }
       }
       __syncthreads();
       const float* sks = reinterpret_cast<const float*>(st + 2 * G::TILE);
@@ -1081,8 +1153,10 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
       lr0 += __shfl_xor_sync(0xffffffffu, lr0, o);
       lr1 += __shfl_xor_sync(0xffffffffu, lr1, o);
     }
-    const float inv0 = 1.f / (lr0 * (float)B), inv1 = 1.f / (lr1 * (float)B);
+    const float bn = ROT ? (float)B : 1.f;
+    const float inv0 = 1.f / (lr0 * bn), inv1 = 1.f / (lr1 * bn);
     // thread values: row r0 -> oacc[t][0..1] (d = 8t + 2cq + e), row r1 -> oacc[t][2..3]
+    if constexpr (ROT) {
 #pragma unroll
     for (int t = 0; t < NT; t++) {  // stage h = 1
       float a = oacc[t][0], b = oacc[t][1];
@@ -1119,6 +1193,7 @@ __global__ void __launch_bounds__(PreGeom<D>::THREADS) prefill_kernel(PreParams 
         }
       }
     }
+    }  // ROT
     if (r0 < nrows) {
       const int j = r0 / c.group, jj = r0 - j * c.group;
       uint16_t* dst = c.out + (long long)(q0 + tok0 + j) * c.out_stride + (long long)(h * c.group + jj) * D;
@@ -1160,7 +1235,7 @@ static bool configure(K kern, int smem, int threads, int* occ_out, bool* done, i
   return true;
 }
 
-template <int D>
+template <int D, int FMT>
 static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   WorkspaceLayout L;
   workspace_layout(a.num_seqs, a.num_q_tokens, a.num_q_heads, a.num_kv_heads, a.head_size, &L);
@@ -1186,15 +1261,21 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.num_blocks = a.num_blocks;
   c.causal = a.causal;
   c.window = a.sliding_window;
-  c.qscale = a.softmax_scale * kLog2e / (float)Head<D>::b;
+  constexpr bool ROT = FMT == kFmtInt4;
+  c.qscale = a.softmax_scale * kLog2e / (ROT ? (float)Head<D>::b : 1.f);
   c.signs = a.signs;
   c.out = static_cast<uint16_t*>(a.out);
   c.out_stride = a.out_stride;
   c.status = a.dev_status;
   c.tile_tokens = kPrefillRows / c.group > 0 ? kPrefillRows / c.group : 1;
   c.max_items = L.max_prefill_items;
+  // kv heads per decode CTA: the largest divisor of Hkv up to 8 whose
+  // staging ring fits in shared memory (int8 tiles are twice as large)
+  constexpr int kMaxSmem = 227 * 1024;
+  int hg_cap = 8;
+  while (hg_cap > 1 && DecGeom<D, 1, FMT>::smem_bytes(hg_cap) > kMaxSmem) hg_cap--;
   c.hg = 1;
-  for (int h = 8; h >= 1; h--)
+  for (int h = hg_cap; h >= 1; h--)
     if (a.num_kv_heads % h == 0) {
       c.hg = h;
       break;
@@ -1212,8 +1293,11 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     static bool attr_done[kMaxDevices][2] = {};
     static int occ_cache[kMaxDevices][2][9] = {};
     auto occupancy = [&](auto kern, int np, int smem_max, int smem) -> int {
+      if (smem > kMaxSmem) return 0;  // this ring does not fit
       if (!attr_done[dev][np - 1]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess) return 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, min(smem_max, kMaxSmem)) !=
+            cudaSuccess)
+          return 0;
         attr_done[dev][np - 1] = true;
       }
       if (!occ_cache[dev][np - 1][c.hg]) {
@@ -1223,7 +1307,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
       }
       return occ_cache[dev][np - 1][c.hg];
     };
-    const int occ1 = occupancy(decode_kernel<D, 1>, 1, DecGeom<D, 1>::smem_bytes(8), DecGeom<D, 1>::smem_bytes(c.hg));
+    const int occ1 = occupancy(decode_kernel<D, 1, FMT>, 1, DecGeom<D, 1, FMT>::smem_bytes(8), DecGeom<D, 1, FMT>::smem_bytes(c.hg));
     if (occ1 < 1) return KV_INT4_ERR_CUDA;
     const long long mq = (long long)(a.max_query_len > 0 ? a.max_query_len : 1) * c.group;
     const long long cols = mq <= kDecodeCols ? mq : c.group;
@@ -1231,9 +1315,8 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     dec_occ = occ1;
     if (cols <= kDecodeCols / 2) {
       const int occ2 =
-          occupancy(decode_kernel<D, 2>, 2, DecGeom<D, 2>::smem_bytes(8), DecGeom<D, 2>::smem_bytes(c.hg));
-      if (occ2 < 1) return KV_INT4_ERR_CUDA;
-      if (occ2 >= occ1) {
+          occupancy(decode_kernel<D, 2, FMT>, 2, DecGeom<D, 2, FMT>::smem_bytes(8), DecGeom<D, 2, FMT>::smem_bytes(c.hg));
+      if (occ2 >= 1 && occ2 >= occ1) {  // 0: the paired ring does not fit
         c.np = 2;
         dec_occ = occ2;
       }
@@ -1249,23 +1332,23 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     const long long grid = 1 + (rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta;
     if (grid > 0x7fffffff) return KV_INT4_ERR_SIZE;
     timing_begin(kTimedPrep, stream);
-    prep_kernel<D><<<(unsigned)grid, kPrepThreads, 0, stream>>>(c, pv);
+    prep_kernel<D, ROT><<<(unsigned)grid, kPrepThreads, 0, stream>>>(c, pv);
     timing_end(kTimedPrep, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   // 2. prefill
   const bool may_prefill = c.group > c.dcols || (long long)a.max_query_len * c.group > c.dcols;
   if (may_prefill) {
-    using G = PreGeom<D>;
+    using G = PreGeom<D, FMT>;
     static bool done[kMaxDevices] = {};
     static int occ_c[kMaxDevices] = {};
     int occ = 0;
-    if (!configure(prefill_kernel<D>, G::SMEM, G::THREADS, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
+    if (!configure(prefill_kernel<D, FMT>, G::SMEM, G::THREADS, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
     long long grid = (long long)sms * occ;
     if (grid > L.max_prefill_items) grid = L.max_prefill_items;
     if (grid < 1) grid = 1;
     timing_begin(kTimedPrefill, stream);
-    prefill_kernel<D><<<(unsigned)grid, G::THREADS, G::SMEM, stream>>>(PreParams{c, pv});
+    prefill_kernel<D, FMT><<<(unsigned)grid, G::THREADS, G::SMEM, stream>>>(PreParams{c, pv});
     timing_end(kTimedPrefill, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
@@ -1277,32 +1360,37 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     const int threads = c.hg * 32;
     timing_begin(kTimedDecode, stream);
     if (c.np == 2)
-      decode_kernel<D, 2><<<(unsigned)grid, threads, DecGeom<D, 2>::smem_bytes(c.hg), stream>>>(
+      decode_kernel<D, 2, FMT><<<(unsigned)grid, threads, DecGeom<D, 2, FMT>::smem_bytes(c.hg), stream>>>(
           DecParams{c, pv, num_ctas});
     else
-      decode_kernel<D, 1><<<(unsigned)grid, threads, DecGeom<D, 1>::smem_bytes(c.hg), stream>>>(
+      decode_kernel<D, 1, FMT><<<(unsigned)grid, threads, DecGeom<D, 1, FMT>::smem_bytes(c.hg), stream>>>(
           DecParams{c, pv, num_ctas});
     timing_end(kTimedDecode, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
     const long long rgrid = (long long)a.num_seqs * a.num_kv_heads;
     if (rgrid > 0x7fffffff) return KV_INT4_ERR_SIZE;
     timing_begin(kTimedReduce, stream);
-    reduce_kernel<D><<<(unsigned)rgrid, kDecodeCols * 32, 0, stream>>>(RedParams{c, pv, num_ctas});
+    reduce_kernel<D, ROT><<<(unsigned)rgrid, kDecodeCols * 32, 0, stream>>>(RedParams{c, pv, num_ctas});
     timing_end(kTimedReduce, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   return KV_INT4_OK;
 }
 
-int launch_attention(const AttnArgs& a, cudaStream_t stream) {
+template <int FMT>
+static int launch_fmt(const AttnArgs& a, cudaStream_t stream) {
   switch (a.head_size) {
-    case 64: return launch_attention_t<64>(a, stream);
-    case 96: return launch_attention_t<96>(a, stream);
-    case 128: return launch_attention_t<128>(a, stream);
-    case 192: return launch_attention_t<192>(a, stream);
-    case 256: return launch_attention_t<256>(a, stream);
+    case 64: return launch_attention_t<64, FMT>(a, stream);
+    case 96: return launch_attention_t<96, FMT>(a, stream);
+    case 128: return launch_attention_t<128, FMT>(a, stream);
+    case 192: return launch_attention_t<192, FMT>(a, stream);
+    case 256: return launch_attention_t<256, FMT>(a, stream);
     default: return KV_INT4_ERR_HEAD_SIZE;
   }
+}
+
+int launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  return a.int8 ? launch_fmt<kFmtInt8>(a, stream) : launch_fmt<kFmtInt4>(a, stream);
 }
 
 }  // namespace kvint4

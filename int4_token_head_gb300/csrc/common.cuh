@@ -26,6 +26,22 @@ __device__ __forceinline__ void flag(int32_t* status, int bit) {
   if (status) atomicOr(status, bit);
 }
 
+// n / d for 0 <= n < 2^31 by a precomputed multiplier (round-up method of
+// Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with s = ceil(log2 d) and m' = 2^32 + m =
+// ceil(2^(32+s) / d), floor(n / d) = floor(n * m' / 2^(32+s)).
+struct FastDiv {
+  uint32_t d, m, s;
+  __host__ FastDiv(uint32_t d_) : d(d_) {
+    s = 0;
+    while ((1ull << s) < d) s++;
+    m = (uint32_t)((((1ull << 32) * ((1ull << s) - d)) / d) + 1);
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    return (uint32_t)(((uint64_t)__umulhi(n, m) + n) >> s);
+  }
+};
+
 // ---------------------------------------------------------------------------
 // cp.async (LDGSTS) staging
 // ---------------------------------------------------------------------------
@@ -146,6 +162,9 @@ constexpr uint32_t kF16x2_ONE = 0x3c003c00u;   // (1, 1)
 constexpr uint32_t kF16x2_M1032 = 0xe408e408u; // (-1032, -1032)
 constexpr uint32_t kF16x2_M1152 = 0xe480e480u; // (-1152, -1152)
 constexpr uint32_t kF16x2_16 = 0x4c004c00u;    // (16, 16)
+// byte_perm source whose every byte is 0x64: pairing a code byte u with it
+// gives the f16 pattern 0x64uu = 1024 + u
+constexpr uint32_t kBytes64 = 0x64646464u;
 
 // ---------------------------------------------------------------------------
 // packed fp32 pairs: two IEEE single-precision operations per instruction,

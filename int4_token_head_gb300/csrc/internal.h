@@ -35,6 +35,8 @@ struct WriteArgs {
 };
 
 int launch_write(const WriteArgs& a, bool prerotated, cudaStream_t stream);
+// int8_per_token_head write (write_int8.cu): caches of d bytes per head vector
+int launch_write_int8(const WriteArgs& a, cudaStream_t stream);
 
 struct AttnArgs {
   const void* q;
@@ -65,6 +67,7 @@ struct AttnArgs {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  bool int8;  // int8_per_token_head cache (int8 codes, no rotation, no signs)
 };
 
 // Workspace layout, shared by the size query and the launcher.

@@ -33,22 +33,6 @@
 
 namespace kvint4 {
 
-// n / d for 0 <= n < 2^31 by a precomputed multiplier (round-up method of
-// Granlund and Montgomery, "Division by invariant integers using
-// multiplication", 1994): with s = ceil(log2 d) and m' = 2^32 + m =
-// ceil(2^(32+s) / d), floor(n / d) = floor(n * m' / 2^(32+s)).
-struct FastDiv {
-  uint32_t d, m, s;
-  __host__ FastDiv(uint32_t d_) : d(d_) {
-    s = 0;
-    while ((1ull << s) < d) s++;
-    m = (uint32_t)((((1ull << 32) * ((1ull << s) - d)) / d) + 1);
-  }
-  __device__ __forceinline__ uint32_t div(uint32_t n) const {
-    return (uint32_t)(((uint64_t)__umulhi(n, m) + n) >> s);
-  }
-};
-
 template <int D>
 struct WriteGeom {
   static constexpr int B = Head<D>::b;

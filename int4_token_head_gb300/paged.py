@@ -1,4 +1,5 @@
-"""Device-side state of a paged INT4 KV cache for one synthetic workload.
+"""Device-side state of a paged INT4 (or int8_per_token_head) KV cache for
+one synthetic workload.
 
 Allocates the sentinel-filled caches and metadata on the GPU, populates each
 sequence's history through the library's write path, and runs the step
@@ -18,10 +19,14 @@ from .synthetic import Workload
 
 
 class PagedKV:
-    def __init__(self, w: Workload, device: str = "cuda"):
+    def __init__(self, w: Workload, device: str = "cuda", fmt: str = "int4"):
+        if fmt not in ("int4", "int8"):
+            raise ValueError(f"unknown cache format {fmt!r}")
         self.w = w
         self.device = device
-        self.k_cache, self.v_cache, self.k_scale, self.v_scale = w.empty_cache(device)
+        self.fmt = fmt
+        caches = w.empty_cache(device) if fmt == "int4" else w.empty_cache_int8(device)
+        self.k_cache, self.v_cache, self.k_scale, self.v_scale = caches
         self.signs = w.signs.to(device)
         self.block_table = w.block_table.to(device)
         self.seq_lens = w.seq_lens.to(device)
@@ -33,6 +38,12 @@ class PagedKV:
 
     # -------------------------------------------------------------------
     def write(self, k, v, slots, stream=None, prerotated=False):
+        if self.fmt == "int8":
+            if prerotated:
+                raise ValueError("the int8 cache stores unrotated vectors")
+            _lib.write_int8(k, v, slots, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                            dev_status=self.status, stream=stream)
+            return
         _lib.write(k, v, slots, self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.signs,
                    dev_status=self.status, stream=stream, prerotated=prerotated)
 
@@ -88,6 +99,12 @@ class PagedKV:
 
     def attend(self, q, out, stream=None):
         w = self.w
+        if self.fmt == "int8":
+            _lib.attention_int8(q, self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.block_table,
+                                self.seq_lens, self.query_start_loc, w.max_query_len, w.max_seq_len,
+                                self.softmax_scale, w.causal, out, self.workspace, dev_status=self.status,
+                                stream=stream, sliding_window=w.sliding_window)
+            return
         _lib.attention(q, self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.block_table,
                        self.seq_lens, self.query_start_loc, w.max_query_len, w.max_seq_len,
                        self.softmax_scale, w.causal, self.signs, out, self.workspace,

@@ -116,6 +116,14 @@ class Workload:
         vs = ks.clone()
         return kc, vc, ks, vs
 
+    def empty_cache_int8(self, device="cpu"):
+        """Sentinel-filled int8_per_token_head caches: codes 0xA5, scales a NaN payload."""
+        nb, bs, h, d = self.num_blocks, self.block_size, self.num_kv_heads, self.head_size
+        kc = torch.full((nb, bs, h, d), SENTINEL_CODE_BYTE, dtype=torch.uint8, device=device).view(torch.int8)
+        vc = kc.clone()
+        ks = torch.full((nb, bs, h), SENTINEL_SCALE_BITS, dtype=torch.int32, device=device).view(torch.float32)
+        return kc, vc, ks, ks.clone()
+
     # ---- token values -------------------------------------------------
     def seq_kv(self, seq: int, device="cpu", positions: Optional[Tuple[int, int]] = None):
         """bf16 K and V [kv_len, Hkv, d] of every position of sequence ``seq``.

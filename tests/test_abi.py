@@ -18,7 +18,7 @@ HEADER = os.path.join(ROOT, "include", "kvint4.h")
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kv_int4_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(kv_int[48]_\w+)\s*\(", text)))
 
 
 def _defines():
@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
         assert n in exported, n
         assert hasattr(lib, n)
     # nothing but the ABI is exported from our own code
-    ours = {e for e in exported if e.startswith("kv_int4") or "kvint4" in e}
+    ours = {e for e in exported if e.startswith(("kv_int4", "kv_int8")) or "kvint4" in e}
     assert ours == set(names)
 
 
@@ -149,3 +149,24 @@ def test_rht_validation(lib):
     assert rht(y=ctypes.c_void_p(0x10002), f32=1) == D["KV_INT4_ERR_ALIGN"]
     assert rht(xs=127) == D["KV_INT4_ERR_ALIGN"]
     assert rht(ys=100) == D["KV_INT4_ERR_ALIGN"]
+
+
+def test_int8_entry_points_validation(lib):
+    w = lambda **kw: lib.kv_int8_write(
+        kw.get("k", FAKE), 8 * 128, FAKE, 8 * 128, FAKE, kw.get("nt", 4), kw.get("kc", FAKE), FAKE, FAKE, FAKE, 4,
+        kw.get("bs", 16), 8, kw.get("d", 128), None, None)
+    assert w(nt=0) == D["KV_INT4_OK"]
+    assert w(k=None) == D["KV_INT4_ERR_NULL"]
+    assert w(d=100) == D["KV_INT4_ERR_HEAD_SIZE"]
+    assert w(bs=8) == D["KV_INT4_ERR_BLOCK_SIZE"]
+    assert w(kc=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
+    ws = lib.kv_int4_attention_workspace_size(2, 8, 32, 8, 128)
+
+    def a(**kw):
+        return lib.kv_int8_attention(FAKE, 32 * 128, kw.get("kc", FAKE), FAKE, FAKE, FAKE, FAKE, 8, FAKE, FAKE,
+                                     kw.get("ns", 2), 8, 4, 128, 32, 8, 128, 16, 16, 0.1, 1, kw.get("win", 0),
+                                     kw.get("out", FAKE), 32 * 128, FAKE, ws, None, None)
+    assert a(ns=0) == D["KV_INT4_OK"]
+    assert a(out=None) == D["KV_INT4_ERR_NULL"]
+    assert a(kc=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
+    assert a(win=-2) == D["KV_INT4_ERR_SIZE"]
