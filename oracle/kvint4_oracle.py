@@ -408,3 +408,46 @@ def attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
             out[q0:q1, h] = attention_head(q[q0:q1, h], k_hat, v_hat, L - (q1 - q0), softmax_scale, causal,
                                            sliding_window)
     return out
+
+
+# ---------------------------------------------------------------------------
+# In-slot scale layout ("[Feature] Triton INT4 per-token-head KV cache
+# quantization", PR #40835, review thread: a block holds a K half then a V
+# half, each (token, head) slot padded_hs wide with the f32 scale at offset hs
+# inside it; #62113 per "Rotate KV into RHT domain in the INT4 unified attn
+# test", Validation: 16-byte-aligned slots).  Reading: slot bytes P =
+# round_up(CB + 4, 16) with CB code bytes per head vector; codes at [0, CB),
+# the scale at [CB, CB + 4), padding after; cache uint8 [NB, 2, bs, Hkv, P].
+# A re-arrangement only: the values are those of the separate caches.
+# ---------------------------------------------------------------------------
+
+def inslot_slot_bytes(code_bytes: int) -> int:
+    return (code_bytes + 4 + 15) // 16 * 16
+
+
+def to_inslot(k_cache, v_cache, k_scale, v_scale, fill=0):
+    """The combined in-slot cache holding the given separate caches' codes and
+    scales (padding bytes = fill)."""
+    kc = np.asarray(k_cache).view(np.uint8)
+    vc = np.asarray(v_cache).view(np.uint8)
+    nb, bs, hkv, cb = kc.shape
+    P = inslot_slot_bytes(cb)
+    out = np.full((nb, 2, bs, hkv, P), fill, dtype=np.uint8)
+    out[:, 0, :, :, :cb] = kc
+    out[:, 1, :, :, :cb] = vc
+    out[:, 0, :, :, cb:cb + 4] = np.ascontiguousarray(np.asarray(k_scale, np.float32)).view(np.uint8).reshape(
+        nb, bs, hkv, 4)
+    out[:, 1, :, :, cb:cb + 4] = np.ascontiguousarray(np.asarray(v_scale, np.float32)).view(np.uint8).reshape(
+        nb, bs, hkv, 4)
+    return out
+
+
+def from_inslot(cache, code_bytes):
+    """Separate (k_cache, v_cache, k_scale, v_scale) views of an in-slot cache."""
+    c = np.asarray(cache, dtype=np.uint8)
+    cb = code_bytes
+    kc = np.ascontiguousarray(c[:, 0, :, :, :cb])
+    vc = np.ascontiguousarray(c[:, 1, :, :, :cb])
+    ks = np.ascontiguousarray(c[:, 0, :, :, cb:cb + 4]).view(np.float32)[..., 0]
+    vs = np.ascontiguousarray(c[:, 1, :, :, cb:cb + 4]).view(np.float32)[..., 0]
+    return kc, vc, ks, vs

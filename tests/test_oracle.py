@@ -8,6 +8,7 @@ loops, and the error bounds the pages publish.
 
 import json
 import math
+import struct
 import os
 
 import numpy as np
@@ -609,3 +610,34 @@ def test_int8_write_scatter_and_skips():
     for slot in range(nb * 16):
         if slot not in written:
             assert np.all(kc[slot // 16, slot % 16] == 0x5A) and np.all(ks[slot // 16, slot % 16] == 9.0)
+
+
+# ---------------------------------------------------------------------------
+# in-slot scale layout
+# ---------------------------------------------------------------------------
+
+def test_inslot_slot_bytes_and_offsets():
+    """P = round_up(CB + 4, 16) for every cache head size of both formats, and
+    to_inslot puts slot s / head h / half kv at byte
+    (((s // 16) * 2 + kv) * 16 + s % 16) * Hkv * P + h * P, scale CB bytes on."""
+    expect = {32: 48, 48: 64, 64: 80, 96: 112, 128: 144, 192: 208, 256: 272}
+    for cb, p in expect.items():
+        assert O.inslot_slot_bytes(cb) == p and p % 16 == 0
+    rng = np.random.default_rng(40)
+    nb, hkv, cb = 3, 2, 48
+    kc = rng.integers(0, 256, (nb, 16, hkv, cb)).astype(np.uint8)
+    vc = rng.integers(0, 256, (nb, 16, hkv, cb)).astype(np.uint8)
+    ks = rng.standard_normal((nb, 16, hkv)).astype(np.float32)
+    vs = rng.standard_normal((nb, 16, hkv)).astype(np.float32)
+    flat = O.to_inslot(kc, vc, ks, vs, fill=0xEE).reshape(-1)
+    P = 64
+    for s in range(nb * 16):
+        for h in range(hkv):
+            for kv, (codes, sc) in enumerate(((kc, ks), (vc, vs))):
+                off = (((s // 16) * 2 + kv) * 16 + s % 16) * hkv * P + h * P
+                assert bytes(flat[off:off + cb]) == bytes(codes[s // 16, s % 16, h])
+                assert struct.unpack("<f", bytes(flat[off + cb:off + cb + 4]))[0] == sc[s // 16, s % 16, h]
+                assert all(b == 0xEE for b in flat[off + cb + 4:off + P])
+    back = O.from_inslot(O.to_inslot(kc, vc, ks, vs), cb)
+    for a, b in zip(back, (kc, vc, ks, vs)):
+        assert np.array_equal(a, b)
