@@ -360,6 +360,72 @@ def int8_decode_bench(w, dev, iters: int):
             "cache_bytes_read": nbytes}
 
 
+def inslot_bench(w, dev, pk, q, out, n_chunks: int, iters: int, chunk_tokens: int = 65536):
+    """The in-slot scale layout (uint8 [blocks][2][16][Hkv][P], the scale
+    inside every P-byte slot) for the INT4 format: bulk writes into an in-slot
+    scratch cache, and decode over the resident cache repacked into that
+    layout on the device (untimed).  Algorithmic bytes are the method's (the
+    same as for the separate layout); the padding to P bytes is layout
+    overhead, reported as slot_bytes."""
+    import torch
+    from int4_token_head_gb300 import _lib
+    hkv, d, bs = w.num_kv_heads, w.head_size, w.block_size
+    cb, P = d // 2, _lib.inslot_slot_bytes(d)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed * 7 + 9)
+    nb = chunk_tokens // bs
+    ks = [torch.randn((chunk_tokens, hkv, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_chunks)]
+    vs = [torch.randn((chunk_tokens, hkv, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_chunks)]
+    slots = [torch.randperm(nb * bs, generator=g, device=dev) for _ in range(n_chunks)]
+    scratch = torch.zeros((nb, 2, bs, hkv, P), dtype=torch.uint8, device=dev)
+    signs = w.signs.to(dev)
+    for i in range(n_chunks):
+        _lib.write_inslot(ks[i], vs[i], slots[i], scratch, signs=signs)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n_chunks):
+        _lib.write_inslot(ks[i], vs[i], slots[i], scratch, signs=signs)
+    e1.record()
+    torch.cuda.synchronize()
+    wms = e0.elapsed_time(e1) / n_chunks
+    wbytes = chunk_tokens * (2 * hkv * d * 2 + 2 * hkv * (cb + 4) + 8)
+    del ks, vs, slots, scratch
+    # decode over the repacked resident cache
+    NB = pk.k_cache.shape[0]
+    ins = torch.zeros((NB, 2, bs, hkv, P), dtype=torch.uint8, device=dev)
+    ins[:, 0, :, :, :cb] = pk.k_cache
+    ins[:, 1, :, :, :cb] = pk.v_cache
+    ins[:, 0, :, :, cb:cb + 4] = pk.k_scale.view(torch.uint8).view(NB, bs, hkv, 4)
+    ins[:, 1, :, :, cb:cb + 4] = pk.v_scale.view(torch.uint8).view(NB, bs, hkv, 4)
+
+    def attend():
+        _lib.attention_inslot(q, ins, pk.block_table, pk.seq_lens, pk.query_start_loc, w.max_query_len,
+                              w.max_seq_len, pk.softmax_scale, w.causal, out, pk.workspace, signs=pk.signs,
+                              dev_status=pk.status, sliding_window=w.sliding_window)
+    for _ in range(3):
+        attend()
+    torch.cuda.synchronize()
+    _lib.timing_collect()
+    _lib.timing_enable(True)
+    for _ in range(iters):
+        attend()
+    torch.cuda.synchronize()
+    kern = _lib.timing_collect()
+    _lib.timing_enable(False)
+    if pk.status.item() != 0:
+        raise RuntimeError(f"device status {pk.status.item()} in the in-slot attention")
+    del ins
+    torch.cuda.empty_cache()
+    res = {"slot_bytes": P, "write": {"gbs": round(wbytes / (wms / 1e3) / 1e9, 1), "ms_per_chunk": round(wms, 4)}}
+    if kern["decode"][0] >= kern["prefill"][0] and kern["decode"][1]:
+        dms = kern["decode"][0] / kern["decode"][1]
+        dbytes = sum(kv * hkv * 2 * (cb + 4) + 4 * ((kv + 15) // 16) + ql * w.num_q_heads * d * 2
+                     for ql, kv in w.seqs)
+        res["decode"] = {"ms": round(dms, 5), "gbs": round(dbytes / (dms / 1e3) / 1e9, 1)}
+    return res
+
+
 # ---------------------------------------------------------------------------
 # the oracle on host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -521,6 +587,7 @@ def run_ours(args):
     if pk.status.item() != 0:
         raise RuntimeError(f"device status {pk.status.item()} during the timed region")
     window_info = window_bench(pk, q, out, 4096, max(10, min(200, args.steps)))
+    inslot_info = inslot_bench(w, dev, pk, q, out, max(1, args.write_chunks), max(10, min(200, args.steps)))
     int8_info = {"write": bulk_write_bench(w, dev, max(1, args.write_chunks), fmt="int8")}
     int8_info.update(int8_decode_bench(w, dev, max(10, min(200, args.steps))))
 
@@ -561,6 +628,9 @@ def run_ours(args):
     rht_info["frac"] = round(rht_info["gbs"] / peak, 4)
     window_info["frac"] = round(window_info["gbs"] / peak, 4)
     int8_info["write"]["frac"] = round(int8_info["write"]["gbs"] / peak, 4)
+    inslot_info["write"]["frac"] = round(inslot_info["write"]["gbs"] / peak, 4)
+    if "decode" in inslot_info:
+        inslot_info["decode"]["frac"] = round(inslot_info["decode"]["gbs"] / peak, 4)
     if int8_info["gbs"]:
         int8_info["frac"] = round(int8_info["gbs"] / peak, 4)
 
@@ -580,6 +650,7 @@ def run_ours(args):
         "rht": rht_info,
         "sliding_window": window_info,
         "int8_per_token_head": int8_info,
+        "inslot_scales": inslot_info,
         "kernels_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in kern.items()},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(sum(v[1] for v in kern.values())),

@@ -276,6 +276,55 @@ KVINT4_API int kv_int4_attention_noalloc(const void* q, int64_t q_token_stride,
                                          int64_t out_token_stride, int32_t* dev_status, void* stream);
 
 /*
+ * In-slot scale layout: K, V, codes and scales in one cache tensor.
+ *
+ * Defined by: "[Feature] Triton INT4 per-token-head KV cache quantization"
+ * (vLLM PR #40835), review thread (the cache-layout diff: a block holds a K
+ * half then a V half; every (token, head) slot is padded_hs wide with the f32
+ * scale at offset hs inside it) and "Rotate KV into RHT domain in the INT4
+ * unified attn test" (PR #62881), Validation (#62113: 16-byte-aligned
+ * per-token-head KV slots).  Reading taken: with CB code bytes per head
+ * vector (head_size / 2 for INT4, head_size for int8) a slot is
+ *   P = kv_int4_inslot_slot_bytes(head_size, int8) = round_up(CB + 4, 16) bytes:
+ * codes at [0, CB), the f32 scale at [CB, CB + 4), padding after (never read
+ * or written); the cache is uint8 [num_blocks][2 (K, V)][block_size]
+ * [num_kv_heads][P], 16-byte aligned: the codes of token slot s, kv head h,
+ * half kv (0: K, 1: V) start at byte
+ *   (((s / 16) * 2 + kv) * 16 + s % 16) * num_kv_heads * P + h * P
+ * and its scale CB bytes further on.
+ *
+ * The writes and attentions below are kv_int4_write / kv_int8_write and
+ * kv_int4_attention / kv_int8_attention with the four cache and scale
+ * pointers replaced by that one tensor; everything else is identical.
+ * kv_int4_inslot_slot_bytes returns 0 for an unsupported head size.
+ */
+KVINT4_API int kv_int4_inslot_slot_bytes(int head_size, int int8);
+KVINT4_API int kv_int4_write_inslot(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                                    const int64_t* slot_mapping, int num_tokens, uint8_t* kv_cache, int num_blocks,
+                                    int block_size, int num_kv_heads, int head_size, const int8_t* signs,
+                                    int32_t* dev_status, void* stream);
+KVINT4_API int kv_int8_write_inslot(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                                    const int64_t* slot_mapping, int num_tokens, uint8_t* kv_cache, int num_blocks,
+                                    int block_size, int num_kv_heads, int head_size, int32_t* dev_status,
+                                    void* stream);
+KVINT4_API int kv_int4_attention_inslot(const void* q, int64_t q_token_stride, const uint8_t* kv_cache,
+                                        const int32_t* block_table, int max_blocks_per_seq,
+                                        const int32_t* seq_lens, const int32_t* query_start_loc, int num_seqs,
+                                        int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
+                                        int num_kv_heads, int head_size, int block_size, int num_blocks,
+                                        float softmax_scale, int causal, int sliding_window, const int8_t* signs,
+                                        void* out, int64_t out_token_stride, void* workspace,
+                                        size_t workspace_bytes, int32_t* dev_status, void* stream);
+KVINT4_API int kv_int8_attention_inslot(const void* q, int64_t q_token_stride, const uint8_t* kv_cache,
+                                        const int32_t* block_table, int max_blocks_per_seq,
+                                        const int32_t* seq_lens, const int32_t* query_start_loc, int num_seqs,
+                                        int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
+                                        int num_kv_heads, int head_size, int block_size, int num_blocks,
+                                        float softmax_scale, int causal, int sliding_window, void* out,
+                                        int64_t out_token_stride, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_status, void* stream);
+
+/*
  * kv_int4_rht -- the block-diagonal randomized Hadamard rotation on its own:
  * the rotation the write path applies to K and V before quantising them (the
  * pages' single_rht step), and its inverse.

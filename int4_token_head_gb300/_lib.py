@@ -44,6 +44,18 @@ _SIGNATURES = {
                                   c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                   c_int, c_float, c_int, c_int, c_void_p, c_int64, c_void_p, c_size_t,
                                   c_void_p, c_void_p]),
+    "kv_int4_inslot_slot_bytes": (c_int, [c_int, c_int]),
+    "kv_int4_write_inslot": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int,
+                                     c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "kv_int8_write_inslot": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int,
+                                     c_int, c_int, c_void_p, c_void_p]),
+    "kv_int4_attention_inslot": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                         c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                         c_int, c_void_p, c_void_p, c_int64, c_void_p, c_size_t, c_void_p,
+                                         c_void_p]),
+    "kv_int8_attention_inslot": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                         c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                         c_int, c_void_p, c_int64, c_void_p, c_size_t, c_void_p, c_void_p]),
     "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
     "kv_int4_timing_enable": (c_int, [c_int]),
     "kv_int4_timing_collect": (c_int, [c_void_p, c_void_p, c_void_p]),
@@ -312,3 +324,65 @@ def attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                                     float(softmax_scale), int(bool(causal)), int(sliding_window), _ptr(out), os_,
                                     _ptr(workspace), int(workspace.numel()), _ptr(dev_status), _stream(stream))
     _raise(code, "kv_int8_attention")
+
+
+def inslot_slot_bytes(head_size: int, int8: bool = False) -> int:
+    """Bytes P of one (token, head) slot of the in-slot layout (0: unsupported head size)."""
+    return int(load().kv_int4_inslot_slot_bytes(int(head_size), int(bool(int8))))
+
+
+def _inslot_dims(kv_cache, head_size, int8):
+    _check(kv_cache.dtype == torch.uint8 and kv_cache.dim() == 5 and kv_cache.shape[1] == 2 and
+           kv_cache.is_contiguous(), "in-slot cache must be contiguous uint8 [blocks, 2, block_size, heads, P]")
+    nb, _, bs, hkv, p = kv_cache.shape
+    _check(p == inslot_slot_bytes(head_size, int8), f"slot bytes must be {inslot_slot_bytes(head_size, int8)}")
+    return nb, bs, hkv
+
+
+def write_inslot(k, v, slot_mapping, kv_cache, signs=None, int8: bool = False,
+                 dev_status: Optional[torch.Tensor] = None, stream=None):
+    """The INT4 (or int8_per_token_head) write into an in-slot cache."""
+    d = k.shape[-1]
+    nb, bs, hkv = _inslot_dims(kv_cache, d, int8)
+    ks = _token_major(k, "k", hkv, d)
+    vs = _token_major(v, "v", hkv, d)
+    _check(k.shape[0] == v.shape[0] == slot_mapping.shape[0], "k, v and slot_mapping disagree on tokens")
+    _check(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), "slot_mapping must be contiguous int64")
+    lib = load()
+    if int8:
+        code = lib.kv_int8_write_inslot(_ptr(k), ks, _ptr(v), vs, _ptr(slot_mapping), int(k.shape[0]),
+                                        _ptr(kv_cache), nb, bs, hkv, d, _ptr(dev_status), _stream(stream))
+    else:
+        _check(signs is not None and signs.dtype == torch.int8 and signs.numel() == d, "signs must be int8 [d]")
+        code = lib.kv_int4_write_inslot(_ptr(k), ks, _ptr(v), vs, _ptr(slot_mapping), int(k.shape[0]),
+                                        _ptr(kv_cache), nb, bs, hkv, d, _ptr(signs), _ptr(dev_status),
+                                        _stream(stream))
+    _raise(code, "kv_int8_write_inslot" if int8 else "kv_int4_write_inslot")
+
+
+def attention_inslot(q, kv_cache, block_table, seq_lens, query_start_loc, max_query_len, max_seq_len,
+                     softmax_scale, causal, out, workspace, signs=None, int8: bool = False,
+                     dev_status: Optional[torch.Tensor] = None, stream=None, sliding_window: int = 0):
+    """Attention over an in-slot INT4 (or int8_per_token_head) cache."""
+    _check(q.dim() == 3, "q must be [tokens, q_heads, d]")
+    hq, d = q.shape[1], q.shape[2]
+    nb, bs, hkv = _inslot_dims(kv_cache, d, int8)
+    qs = _token_major(q, "q", hq, d)
+    os_ = _token_major(out, "out", hq, d)
+    _check(out.shape[0] == q.shape[0], "out must match q")
+    _check(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous(),
+           "block_table must be contiguous int32 [seqs, max_blocks]")
+    num_seqs = seq_lens.shape[0]
+    _check(query_start_loc.shape[0] == num_seqs + 1 and block_table.shape[0] == num_seqs, "metadata shapes")
+    _check(workspace.dtype == torch.uint8 and workspace.is_contiguous(), "workspace must be contiguous uint8")
+    lib = load()
+    common = (_ptr(q), qs, _ptr(kv_cache), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+              _ptr(query_start_loc), int(num_seqs), int(q.shape[0]), int(max_query_len), int(max_seq_len), int(hq),
+              int(hkv), int(d), int(bs), int(nb), float(softmax_scale), int(bool(causal)), int(sliding_window))
+    tail = (_ptr(out), os_, _ptr(workspace), int(workspace.numel()), _ptr(dev_status), _stream(stream))
+    if int8:
+        code = lib.kv_int8_attention_inslot(*common, *tail)
+    else:
+        _check(signs is not None and signs.dtype == torch.int8 and signs.numel() == d, "signs must be int8 [d]")
+        code = lib.kv_int4_attention_inslot(*common, _ptr(signs), *tail)
+    _raise(code, "kv_int8_attention_inslot" if int8 else "kv_int4_attention_inslot")

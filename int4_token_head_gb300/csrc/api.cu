@@ -102,20 +102,33 @@ static int validate_write(const void* k, int64_t ks, const void* v, int64_t vs, 
   if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc) || (ks % 8) || (vs % 8) || ks < 0 || vs < 0)
     return KV_INT4_ERR_ALIGN;
   if ((int64_t)num_tokens * 2 * hkv >= (1ll << 31)) return KV_INT4_ERR_SIZE;
-  if ((int64_t)num_blocks * block_size * hkv * (d / 2) >= (1ll << 62)) return KV_INT4_ERR_SIZE;
   return KV_INT4_OK;
 }
 
+// One write path for every format and layout.  in-slot: kc is the combined
+// [blocks][2][16][Hkv][P] cache (vc, ksc, vsc unused by the caller).
 static int do_write(const void* k, int64_t ks, const void* v, int64_t vs, const int64_t* slots, int num_tokens,
                     uint8_t* kc, uint8_t* vc, float* ksc, float* vsc, int num_blocks, int block_size, int hkv,
-                    int d, const int8_t* signs, int32_t* status, void* stream, bool prerot) {
+                    int d, const int8_t* signs, int32_t* status, void* stream, bool prerot, bool int8,
+                    bool inslot) {
+  const int cb = int8 ? d : d / 2;  // code bytes per head vector (valid d only; checked below)
+  if (inslot) {
+    if (!kc && num_tokens > 0) return KV_INT4_ERR_NULL;
+    const int P = inslot_bytes(cb);
+    vc = kc ? kc + 16ll * hkv * P : nullptr;
+    ksc = kc ? reinterpret_cast<float*>(kc + cb) : nullptr;
+    vsc = kc ? reinterpret_cast<float*>(kc + 16ll * hkv * P + cb) : nullptr;
+  }
   int e = validate_write(k, ks, v, vs, slots, num_tokens, kc, vc, ksc, vsc, num_blocks, block_size, hkv, d, signs,
-                         !prerot);
+                         !prerot && !int8);
   if (e != KV_INT4_OK) return e;
   if (num_tokens == 0) return KV_INT4_OK;
+  const CacheGeo geo = inslot ? inslot_geo(hkv, cb) : separate_geo(hkv, cb);
+  if ((int64_t)num_blocks * geo.cblk >= (1ll << 62)) return KV_INT4_ERR_SIZE;
   if (current_device() < 0) return KV_INT4_ERR_CUDA;
-  WriteArgs a{k, ks, v, vs, slots, num_tokens, kc, vc, ksc, vsc, num_blocks, block_size, hkv, d, signs, status};
-  return launch_write(a, prerot, static_cast<cudaStream_t>(stream));
+  WriteArgs a{k, ks, v, vs, slots, num_tokens, kc, vc, ksc, vsc, num_blocks, block_size, hkv, d, signs, status, geo};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return int8 ? launch_write_int8(a, st) : launch_write(a, prerot, st);
 }
 
 int kv_int4_write(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
@@ -123,24 +136,17 @@ int kv_int4_write(const void* k, int64_t k_token_stride, const void* v, int64_t 
                   float* k_scale_cache, float* v_scale_cache, int num_blocks, int block_size, int num_kv_heads,
                   int head_size, const int8_t* signs, int32_t* dev_status, void* stream) {
   return do_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, k_cache, v_cache, k_scale_cache,
-                  v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, signs, dev_status, stream, false);
+                  v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, signs, dev_status, stream, false,
+                  false, false);
 }
 
 int kv_int8_write(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
                   const int64_t* slot_mapping, int num_tokens, int8_t* k_cache, int8_t* v_cache, float* k_scale_cache,
                   float* v_scale_cache, int num_blocks, int block_size, int num_kv_heads, int head_size,
                   int32_t* dev_status, void* stream) {
-  int e = validate_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens,
-                         reinterpret_cast<const uint8_t*>(k_cache), reinterpret_cast<const uint8_t*>(v_cache),
-                         k_scale_cache, v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, nullptr,
-                         false);
-  if (e != KV_INT4_OK || num_tokens == 0) return e;
-  if ((int64_t)num_blocks * block_size * num_kv_heads * head_size >= (1ll << 62)) return KV_INT4_ERR_SIZE;
-  if (current_device() < 0) return KV_INT4_ERR_CUDA;
-  WriteArgs a{k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, reinterpret_cast<uint8_t*>(k_cache),
-              reinterpret_cast<uint8_t*>(v_cache), k_scale_cache, v_scale_cache, num_blocks, block_size,
-              num_kv_heads, head_size, nullptr, dev_status};
-  return launch_write_int8(a, static_cast<cudaStream_t>(stream));
+  return do_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, reinterpret_cast<uint8_t*>(k_cache),
+                  reinterpret_cast<uint8_t*>(v_cache), k_scale_cache, v_scale_cache, num_blocks, block_size,
+                  num_kv_heads, head_size, nullptr, dev_status, stream, false, true, false);
 }
 
 int kv_int4_write_prerotated(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
@@ -148,7 +154,30 @@ int kv_int4_write_prerotated(const void* k, int64_t k_token_stride, const void* 
                              float* k_scale_cache, float* v_scale_cache, int num_blocks, int block_size,
                              int num_kv_heads, int head_size, int32_t* dev_status, void* stream) {
   return do_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, k_cache, v_cache, k_scale_cache,
-                  v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, nullptr, dev_status, stream, true);
+                  v_scale_cache, num_blocks, block_size, num_kv_heads, head_size, nullptr, dev_status, stream, true,
+                  false, false);
+}
+
+int kv_int4_inslot_slot_bytes(int head_size, int int8) {
+  if (!head_size_ok(head_size)) return 0;
+  return inslot_bytes(int8 ? head_size : head_size / 2);
+}
+
+int kv_int4_write_inslot(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                         const int64_t* slot_mapping, int num_tokens, uint8_t* kv_cache, int num_blocks,
+                         int block_size, int num_kv_heads, int head_size, const int8_t* signs, int32_t* dev_status,
+                         void* stream) {
+  return do_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, kv_cache, nullptr, nullptr,
+                  nullptr, num_blocks, block_size, num_kv_heads, head_size, signs, dev_status, stream, false, false,
+                  true);
+}
+
+int kv_int8_write_inslot(const void* k, int64_t k_token_stride, const void* v, int64_t v_token_stride,
+                         const int64_t* slot_mapping, int num_tokens, uint8_t* kv_cache, int num_blocks,
+                         int block_size, int num_kv_heads, int head_size, int32_t* dev_status, void* stream) {
+  return do_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, kv_cache, nullptr, nullptr,
+                  nullptr, num_blocks, block_size, num_kv_heads, head_size, nullptr, dev_status, stream, false, true,
+                  true);
 }
 
 size_t kv_int4_attention_workspace_size(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
@@ -165,7 +194,15 @@ static int do_attention(const void* q, int64_t q_token_stride, const uint8_t* k_
                         int num_seqs, int num_q_tokens, int max_query_len, int max_seq_len, int num_q_heads,
                         int num_kv_heads, int head_size, int block_size, int num_blocks, float softmax_scale,
                         int causal, int sliding_window, const int8_t* signs, void* out, int64_t out_token_stride,
-                        void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream, bool int8) {
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream, bool int8,
+                        bool inslot) {
+  if (inslot && head_size_ok(head_size) && num_kv_heads > 0 && k_cache) {
+    // k_cache is the combined [blocks][2][16][Hkv][P] cache
+    const int cb = int8 ? head_size : head_size / 2, P = inslot_bytes(cb);
+    v_cache = k_cache + 16ll * num_kv_heads * P;
+    k_scale_cache = reinterpret_cast<const float*>(k_cache + cb);
+    v_scale_cache = reinterpret_cast<const float*>(v_cache + cb);
+  }
   if (num_seqs < 0 || num_q_tokens < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0 ||
       max_blocks_per_seq < 0 || sliding_window < 0)
     return KV_INT4_ERR_SIZE;
@@ -188,7 +225,10 @@ static int do_attention(const void* q, int64_t q_token_stride, const uint8_t* k_
   AttnArgs a{q, q_token_stride, k_cache, v_cache, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
              seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len, max_seq_len, num_q_heads,
              num_kv_heads, head_size, block_size, num_blocks, softmax_scale, causal, sliding_window, signs, out,
-             out_token_stride, workspace, workspace_bytes, dev_status, int8};
+             out_token_stride, workspace, workspace_bytes, dev_status, int8,
+             inslot ? inslot_geo(num_kv_heads, int8 ? head_size : head_size / 2)
+                    : separate_geo(num_kv_heads, int8 ? head_size : head_size / 2)};
+  if ((int64_t)num_blocks * a.geo.cblk >= (1ll << 62)) return KV_INT4_ERR_SIZE;
   return launch_attention(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -203,7 +243,7 @@ int kv_int4_attention(const void* q, int64_t q_token_stride, const uint8_t* k_ca
                       max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len,
                       max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
                       causal, sliding_window, signs, out, out_token_stride, workspace, workspace_bytes, dev_status,
-                      stream, false);
+                      stream, false, false);
 }
 
 int kv_int8_attention(const void* q, int64_t q_token_stride, const int8_t* k_cache, const int8_t* v_cache,
@@ -218,7 +258,33 @@ int kv_int8_attention(const void* q, int64_t q_token_stride, const int8_t* k_cac
                       max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len,
                       max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
                       causal, sliding_window, nullptr, out, out_token_stride, workspace, workspace_bytes, dev_status,
-                      stream, true);
+                      stream, true, false);
+}
+
+int kv_int4_attention_inslot(const void* q, int64_t q_token_stride, const uint8_t* kv_cache,
+                             const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                             const int32_t* query_start_loc, int num_seqs, int num_q_tokens, int max_query_len,
+                             int max_seq_len, int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                             int num_blocks, float softmax_scale, int causal, int sliding_window, const int8_t* signs,
+                             void* out, int64_t out_token_stride, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, void* stream) {
+  return do_attention(q, q_token_stride, kv_cache, kv_cache, nullptr, nullptr, block_table, max_blocks_per_seq,
+                      seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len, max_seq_len, num_q_heads,
+                      num_kv_heads, head_size, block_size, num_blocks, softmax_scale, causal, sliding_window, signs,
+                      out, out_token_stride, workspace, workspace_bytes, dev_status, stream, false, true);
+}
+
+int kv_int8_attention_inslot(const void* q, int64_t q_token_stride, const uint8_t* kv_cache,
+                             const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                             const int32_t* query_start_loc, int num_seqs, int num_q_tokens, int max_query_len,
+                             int max_seq_len, int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                             int num_blocks, float softmax_scale, int causal, int sliding_window, void* out,
+                             int64_t out_token_stride, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             void* stream) {
+  return do_attention(q, q_token_stride, kv_cache, kv_cache, nullptr, nullptr, block_table, max_blocks_per_seq,
+                      seq_lens, query_start_loc, num_seqs, num_q_tokens, max_query_len, max_seq_len, num_q_heads,
+                      num_kv_heads, head_size, block_size, num_blocks, softmax_scale, causal, sliding_window, nullptr,
+                      out, out_token_stride, workspace, workspace_bytes, dev_status, stream, true, true);
 }
 
 }  // extern "C"

@@ -83,6 +83,7 @@ struct Common {
   const uint8_t* v_cache;
   const float* k_scale;
   const float* v_scale;
+  CacheGeo geo;  // cache strides (separate or in-slot scales)
   const int32_t* block_table;
   int max_blocks;
   const int32_t* seq_lens;
@@ -480,15 +481,14 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const int kvr = rest / HG;
     const int kv = kvr / 16, r = kvr % 16;
     c_saddr[j] = smem_addr(smem) + h * G::HTILE + (kv ? G::KTILE + r * G::VROW : r * G::KROW) + col * 16;
-    c_src[j] = (kv ? c.v_cache : c.k_cache) + ((long long)r * c.hkv + h) * G::CB + col * 16;
+    c_src[j] = (kv ? c.v_cache : c.k_cache) + r * c.geo.crow + (long long)h * c.geo.chead + col * 16;
   }
   // one 4-byte scale per thread: [K/V][row][h]
   const int s_kv = tid / (16 * HG), s_rem = tid % (16 * HG);
   const int s_r = s_rem / HG, s_h = s_rem % HG;
   const uint32_t s_saddr = smem_addr(smem) + HG * G::HTILE + (s_kv * HG + s_h) * 64 + s_r * 4;
-  const float* s_src = (s_kv ? c.v_scale : c.k_scale) + (long long)s_r * c.hkv + s_h;
-  const uint32_t blk_bytes = 16u * c.hkv * G::CB;  // < 2^32 (host-checked head counts)
-  const uint32_t blk_scales = 16u * c.hkv;
+  const float* s_src = (s_kv ? c.v_scale : c.k_scale) + s_r * c.geo.srow + (long long)s_h * c.geo.shead;
+  const uint64_t blk_bytes = (uint64_t)c.geo.cblk, blk_scales = (uint64_t)c.geo.sblk;
 
   // block j of a position, or kAbsent past the end of the sequence (NP > 1)
   constexpr int kAbsent = -0x7fffffff - 1;
@@ -500,13 +500,13 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const bool ok = blk >= 0 && blk < c.num_blocks;
     if (ok) {
       const uint32_t soff = (uint32_t)(slot * SB);
-      const uint32_t goff = (uint32_t)(grp * HG * G::CB);
+      const uint64_t goff = (uint64_t)(grp * HG) * c.geo.chead;
 #pragma unroll
       for (int j = 0; j < G::CHR; j++) {
         const uint8_t* src = c_src[j] + (uint64_t)(uint32_t)blk * blk_bytes + goff;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(c_saddr[j] + soff), "l"(src));
       }
-      const float* ssrc = s_src + (uint64_t)(uint32_t)blk * blk_scales + grp * HG;
+      const float* ssrc = s_src + (uint64_t)(uint32_t)blk * blk_scales + (uint64_t)(grp * HG) * c.geo.shead;
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s_saddr + soff), "l"(ssrc));
     }
     if (tid == 0) {
@@ -994,16 +994,16 @@ __global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PrePa
       uint8_t* st = stages + stage * G::STAGE;
       const int blk = c.block_table[(long long)seq * c.max_blocks + kb];
       if (blk < 0 || blk >= c.num_blocks) return;  // reported and masked by the consumer
-      const long long row0 = (long long)blk * 16;
+      const long long cb0 = (long long)blk * c.geo.cblk, sb0 = (long long)blk * c.geo.sblk;
       for (int q = tid; q < G::CB; q += G::THREADS) {  // 16 rows x CB/16 chunks
         const int r = q / (G::CB / 16), col = q - r * (G::CB / 16);
-        const long long goff = ((row0 + r) * c.hkv + h) * G::CB + col * 16;
+        const long long goff = cb0 + r * c.geo.crow + (long long)h * c.geo.chead + col * 16;
         cp_async16(st + r * G::CB + col * 16, c.k_cache + goff);
         cp_async16(st + G::TILE + r * G::CB + col * 16, c.v_cache + goff);
       }
       if (tid < 32) {
         const int r = tid & 15;
-        const long long soff = (row0 + r) * c.hkv + h;
+        const long long soff = sb0 + r * c.geo.srow + (long long)h * c.geo.shead;
         if (tid < 16) cp_async4(st + 2 * G::TILE + r * 4, c.k_scale + soff);
         else cp_async4(st + 2 * G::TILE + 64 + r * 4, c.v_scale + soff);
       }
@@ -1249,6 +1249,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.v_cache = a.v_cache;
   c.k_scale = a.k_scale;
   c.v_scale = a.v_scale;
+  c.geo = a.geo;
   c.block_table = a.block_table;
   c.max_blocks = a.max_blocks_per_seq;
   c.seq_lens = a.seq_lens;

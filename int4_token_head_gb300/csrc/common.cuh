@@ -42,6 +42,16 @@ struct FastDiv {
   }
 };
 
+// cache offsets of (slot, head): codes in bytes, scale in floats (layouts in internal.h)
+template <typename Geo>
+__device__ __forceinline__ int64_t code_off(const Geo& g, int64_t slot, int h) {
+  return (slot >> 4) * g.cblk + (slot & 15) * g.crow + (int64_t)h * g.chead;
+}
+template <typename Geo>
+__device__ __forceinline__ int64_t scale_off(const Geo& g, int64_t slot, int h) {
+  return (slot >> 4) * g.sblk + (slot & 15) * g.srow + (int64_t)h * g.shead;
+}
+
 // ---------------------------------------------------------------------------
 // cp.async (LDGSTS) staging
 // ---------------------------------------------------------------------------

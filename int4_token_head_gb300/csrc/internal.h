@@ -15,6 +15,32 @@ int current_device();
 // cached multiprocessor count of device `dev`
 int sm_count(int dev);
 
+// Where the codes and the scale of (slot, kv head) live.  A slot is
+// (block, row) = (slot / 16, slot % 16); codes start at
+//   code base + block * cblk + row * crow + head * chead        (bytes)
+// and the f32 scale at
+//   scale base + block * sblk + row * srow + head * shead       (floats).
+// Separate caches ([blocks][16][Hkv][code bytes] + [blocks][16][Hkv] f32):
+// crow = Hkv * code bytes, chead = code bytes, srow = Hkv, shead = 1.
+// In-slot caches ([blocks][2 (K, V)][16][Hkv][P] bytes, the scale at byte
+// code bytes of each P-byte slot): crow = Hkv * P, chead = P, and the same
+// strides in floats for the scales.
+struct CacheGeo {
+  int64_t cblk, crow;
+  int32_t chead;
+  int64_t sblk, srow;
+  int32_t shead;
+};
+inline CacheGeo separate_geo(int hkv, int code_bytes) {
+  return CacheGeo{16ll * hkv * code_bytes, (int64_t)hkv * code_bytes, code_bytes, 16ll * hkv, hkv, 1};
+}
+// bytes of one in-slot (token, head) slot: codes + f32 scale, rounded up to 16
+inline int inslot_bytes(int code_bytes) { return (code_bytes + 4 + 15) / 16 * 16; }
+inline CacheGeo inslot_geo(int hkv, int code_bytes) {
+  const int P = inslot_bytes(code_bytes);
+  return CacheGeo{32ll * hkv * P, (int64_t)hkv * P, P, 8ll * hkv * P, (int64_t)hkv * P / 4, P / 4};
+}
+
 struct WriteArgs {
   const void* k;
   int64_t k_stride;
@@ -32,6 +58,7 @@ struct WriteArgs {
   int head_size;
   const int8_t* signs;
   int32_t* dev_status;
+  CacheGeo geo;
 };
 
 int launch_write(const WriteArgs& a, bool prerotated, cudaStream_t stream);
@@ -68,6 +95,7 @@ struct AttnArgs {
   size_t workspace_bytes;
   int32_t* dev_status;
   bool int8;  // int8_per_token_head cache (int8 codes, no rotation, no signs)
+  CacheGeo geo;
 };
 
 // Workspace layout, shared by the size query and the launcher.

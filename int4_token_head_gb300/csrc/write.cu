@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(WriteGeom<D>::NT)
 write_kernel(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* __restrict__ v,
              int64_t v_stride, const int64_t* __restrict__ slot_mapping, int num_tokens,
              uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
-             float* __restrict__ v_scale, int64_t num_slots, int hkv, FastDiv div2h,
+             float* __restrict__ v_scale, CacheGeo geo, int64_t num_slots, int hkv, FastDiv div2h,
              const int8_t* __restrict__ signs, int32_t* status) {
   using G = WriteGeom<D>;
   constexpr int B = G::B, SEG = G::SEG, F = G::F, TPV = G::TPV, UT = G::UT, NT = G::NT;
@@ -239,10 +239,10 @@ write_kernel(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* _
           out[wq] = __byte_perm(x01, x23, 0x5410) ^ 0x88888888u;  // offset binary -> two's complement
         }
         uint8_t* cache = kv ? v_cache : k_cache;
-        uint4* dst = reinterpret_cast<uint4*>(cache + (slot * hkv + h) * (int64_t)(D / 2) + (blk * B + jj * SEG) / 2);
+        uint4* dst = reinterpret_cast<uint4*>(cache + code_off(geo, slot, h) + (blk * B + jj * SEG) / 2);
 #pragma unroll
         for (int q = 0; q < SEG / 32; q++) dst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-        if (j == 0) (kv ? v_scale : k_scale)[slot * hkv + h] = sc;
+        if (j == 0) (kv ? v_scale : k_scale)[scale_off(geo, slot, h)] = sc;
       }
     }
     __syncthreads();  // the stage (and the absmax buffer) may now be overwritten
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(WriteGeom<D>::NT)
 write_kernel_tok(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* __restrict__ v,
                  int64_t v_stride, const int64_t* __restrict__ slot_mapping, int num_tokens,
                  uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
-                 float* __restrict__ v_scale, int64_t num_slots, int hkv, int tt_per_tile,
+                 float* __restrict__ v_scale, CacheGeo geo, int64_t num_slots, int hkv, int tt_per_tile,
                  const int8_t* __restrict__ signs, int32_t* status) {
   using G = WriteGeom<D>;
   constexpr int B = G::B, SEG = G::SEG, F = G::F, TPV = G::TPV, UT = G::UT, NT = G::NT;
@@ -446,10 +446,10 @@ write_kernel_tok(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_
           const uint32_t x23 = __byte_perm(bytes[2], bytes[3], 0x0040);
           out[wq] = __byte_perm(x01, x23, 0x5410) ^ 0x88888888u;  // offset binary -> two's complement
         }
-        uint4* dst = reinterpret_cast<uint4*>(u_cache + (slot * hkv + u_h) * (int64_t)(D / 2) + (blk * B + jj * SEG) / 2);
+        uint4* dst = reinterpret_cast<uint4*>(u_cache + code_off(geo, slot, u_h) + (blk * B + jj * SEG) / 2);
 #pragma unroll
         for (int q = 0; q < SEG / 32; q++) dst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-        if (j == 0) u_scale[slot * hkv + u_h] = sc;
+        if (j == 0) u_scale[scale_off(geo, slot, u_h)] = sc;
       }
     }
     __syncthreads();  // the stage (and the absmax buffer) may now be overwritten
@@ -511,7 +511,8 @@ __global__ void __launch_bounds__(TcGeom<D>::NT, TcGeom<D>::MIN_CTAS)
 write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* __restrict__ v, int64_t v_stride,
                 const int64_t* __restrict__ slot_mapping, int num_tokens, uint8_t* __restrict__ k_cache,
                 uint8_t* __restrict__ v_cache, float* __restrict__ k_scale, float* __restrict__ v_scale,
-                int64_t num_slots, int hkv, int tt_per_tile, const int8_t* __restrict__ signs, int32_t* status) {
+                CacheGeo geo, int64_t num_slots, int hkv, int tt_per_tile, const int8_t* __restrict__ signs,
+                int32_t* status) {
   using G = TcGeom<D>;
   constexpr int NG = G::NG, GB = G::GB, NT = G::NT;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -720,7 +721,7 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
         // outputs 4cq..4cq+3 of group q = bytes 8q + 2cq, 8q + 2cq + 1
         *reinterpret_cast<uint16_t*>(orow + 8 * q + 2 * cq) = (uint16_t)__byte_perm(bytes[0], bytes[1], 0x0040);
       }
-      if (cq == 0 && r_slot[rr] >= 0) (r_kv[rr] ? v_scale : k_scale)[r_slot[rr] * hkv + r_h[rr]] = sc;
+      if (cq == 0 && r_slot[rr] >= 0) (r_kv[rr] ? v_scale : k_scale)[scale_off(geo, r_slot[rr], r_h[rr])] = sc;
     }
     __syncwarp();
     // 16-byte stores: the quad of rows g, g + 8 stores those rows' chunks
@@ -728,7 +729,7 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
 #pragma unroll
     for (int rr = 0; rr < 2; rr++) {
       if (r_slot[rr] < 0) continue;
-      uint8_t* dst = (r_kv[rr] ? v_cache : k_cache) + (r_slot[rr] * hkv + r_h[rr]) * (int64_t)(D / 2);
+      uint8_t* dst = (r_kv[rr] ? v_cache : k_cache) + code_off(geo, r_slot[rr], r_h[rr]);
 #pragma unroll
       for (int ch = cq; ch < CPR; ch += 4)
         *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(wbase + tc_vec_off<D>(2 * g + rr) + ch * 16);
@@ -789,7 +790,7 @@ static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
       timing_begin(kTimedWrite, stream);
       tckern<<<grid, T::NT, T::SMEM, stream>>>(
           static_cast<const uint16_t*>(a.k), a.k_stride, static_cast<const uint16_t*>(a.v), a.v_stride,
-          a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale,
+          a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale, a.geo,
           (int64_t)a.num_blocks * a.block_size, a.num_kv_heads, tt, a.signs, a.dev_status);
       timing_end(kTimedWrite, stream);
       return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
@@ -810,7 +811,7 @@ static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
     timing_begin(kTimedWrite, stream);
     tkern<<<grid, G::NT, G::SMEM, stream>>>(
         static_cast<const uint16_t*>(a.k), a.k_stride, static_cast<const uint16_t*>(a.v), a.v_stride,
-        a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale,
+        a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale, a.geo,
         (int64_t)a.num_blocks * a.block_size, a.num_kv_heads, tt, a.signs, a.dev_status);
     timing_end(kTimedWrite, stream);
     return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
@@ -821,7 +822,7 @@ static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
   timing_begin(kTimedWrite, stream);
   write_kernel<D, PREROT><<<grid, G::NT, G::SMEM, stream>>>(
       static_cast<const uint16_t*>(a.k), a.k_stride, static_cast<const uint16_t*>(a.v), a.v_stride,
-      a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale,
+      a.slot_mapping, a.num_tokens, a.k_cache, a.v_cache, a.k_scale, a.v_scale, a.geo,
       (int64_t)a.num_blocks * a.block_size, a.num_kv_heads, FastDiv(2u * a.num_kv_heads), a.signs,
       a.dev_status);
   timing_end(kTimedWrite, stream);

@@ -45,6 +45,7 @@ struct I8Args {
   int hkv;
   int32_t* status;
   FastDiv upt;  // vectors per token (2 hkv)
+  CacheGeo geo;
 };
 
 template <int D>
@@ -125,9 +126,9 @@ __global__ void __launch_bounds__(kI8Warps * 32) write_int8_kernel(I8Args a) {
         continue;
       }
       const bool kv = unit[u] >= a.hkv;
-      const int64_t row = slot * a.hkv + (kv ? unit[u] - a.hkv : unit[u]);
-      *reinterpret_cast<uint4*>((kv ? a.v_cache : a.k_cache) + row * D + 16 * c) = codes;
-      if (c == 0) (kv ? a.v_scale : a.k_scale)[row] = sc;
+      const int h = kv ? unit[u] - a.hkv : unit[u];
+      *reinterpret_cast<uint4*>((kv ? a.v_cache : a.k_cache) + code_off(a.geo, slot, h) + 16 * c) = codes;
+      if (c == 0) (kv ? a.v_scale : a.k_scale)[scale_off(a.geo, slot, h)] = sc;
     }
   }
 }
@@ -154,7 +155,7 @@ int launch_write_int8(const WriteArgs& w, cudaStream_t stream) {
   I8Args a{static_cast<const uint16_t*>(w.k), w.k_stride, static_cast<const uint16_t*>(w.v), w.v_stride,
            w.slot_mapping, (int64_t)w.num_tokens * 2 * w.num_kv_heads, w.k_cache, w.v_cache, w.k_scale,
            w.v_scale, (int64_t)w.num_blocks * w.block_size, w.num_kv_heads, w.dev_status,
-           FastDiv((uint32_t)(2 * w.num_kv_heads))};
+           FastDiv((uint32_t)(2 * w.num_kv_heads)), w.geo};
   switch (w.head_size) {
     case 64: return launch_t<64>(a, stream);
     case 96: return launch_t<96>(a, stream);

@@ -170,3 +170,28 @@ def test_int8_entry_points_validation(lib):
     assert a(out=None) == D["KV_INT4_ERR_NULL"]
     assert a(kc=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
     assert a(win=-2) == D["KV_INT4_ERR_SIZE"]
+
+
+def test_inslot_entry_points_validation(lib):
+    assert lib.kv_int4_inslot_slot_bytes(128, 0) == 80
+    assert lib.kv_int4_inslot_slot_bytes(96, 0) == 64
+    assert lib.kv_int4_inslot_slot_bytes(128, 1) == 144
+    assert lib.kv_int4_inslot_slot_bytes(100, 0) == 0
+    w = lambda **kw: lib.kv_int4_write_inslot(FAKE, 8 * 128, FAKE, 8 * 128, FAKE, kw.get("nt", 4),
+                                              kw.get("kv", FAKE), 4, 16, 8, kw.get("d", 128), kw.get("signs", FAKE),
+                                              None, None)
+    assert w(nt=0, kv=None) == D["KV_INT4_OK"]
+    assert w(kv=None) == D["KV_INT4_ERR_NULL"]
+    assert w(signs=None) == D["KV_INT4_ERR_NULL"]
+    assert w(kv=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
+    assert w(d=72) == D["KV_INT4_ERR_HEAD_SIZE"]
+    assert lib.kv_int8_write_inslot(FAKE, 1024, FAKE, 1024, FAKE, 4, None, 4, 16, 8, 128, None, None) == \
+        D["KV_INT4_ERR_NULL"]
+    ws = lib.kv_int4_attention_workspace_size(2, 8, 32, 8, 128)
+    a = lambda **kw: lib.kv_int4_attention_inslot(FAKE, 32 * 128, kw.get("kv", FAKE), FAKE, 8, FAKE, FAKE,
+                                                  kw.get("ns", 2), 8, 4, 128, 32, 8, 128, 16, 16, 0.1, 1, 0,
+                                                  kw.get("signs", FAKE), FAKE, 32 * 128, FAKE, ws, None, None)
+    assert a(ns=0) == D["KV_INT4_OK"]
+    assert a(kv=None) == D["KV_INT4_ERR_NULL"]
+    assert a(signs=None) == D["KV_INT4_ERR_NULL"]
+    assert a(kv=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
