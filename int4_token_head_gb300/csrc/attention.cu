@@ -1218,6 +1218,8 @@ __global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PrePa
   }
 }
 
+#include "prefill_tc.cuh"
+
 // ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
@@ -1268,7 +1270,11 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.out = static_cast<uint16_t*>(a.out);
   c.out_stride = a.out_stride;
   c.status = a.dev_status;
-  c.tile_tokens = kPrefillRows / c.group > 0 ? kPrefillRows / c.group : 1;
+  // prefill tiles: 128 rows on the tensor-core kernel (head sizes up to 192),
+  // 64 on the warp-MMA one
+  constexpr bool kTcPrefill = D <= 192;
+  constexpr int kTileRows = kTcPrefill ? 128 : kPrefillRows;
+  c.tile_tokens = kTileRows / c.group > 0 ? kTileRows / c.group : 1;
   c.max_items = L.max_prefill_items;
   // kv heads per decode CTA: the largest divisor of Hkv up to 8 whose
   // staging ring fits in shared memory (int8 tiles are twice as large)
@@ -1340,17 +1346,29 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   // 2. prefill
   const bool may_prefill = c.group > c.dcols || (long long)a.max_query_len * c.group > c.dcols;
   if (may_prefill) {
-    using G = PreGeom<D, FMT>;
     static bool done[kMaxDevices] = {};
     static int occ_c[kMaxDevices] = {};
     int occ = 0;
-    if (!configure(prefill_kernel<D, FMT>, G::SMEM, G::THREADS, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
-    long long grid = (long long)sms * occ;
-    if (grid > L.max_prefill_items) grid = L.max_prefill_items;
-    if (grid < 1) grid = 1;
-    timing_begin(kTimedPrefill, stream);
-    prefill_kernel<D, FMT><<<(unsigned)grid, G::THREADS, G::SMEM, stream>>>(PreParams{c, pv});
-    timing_end(kTimedPrefill, stream);
+    if constexpr (kTcPrefill) {
+      using G = TcPreGeom<D, FMT>;
+      if (!configure(prefill_tc_kernel<D, FMT>, G::SMEM, 128, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
+      long long grid = (long long)sms * occ;
+      if (grid > L.max_prefill_items) grid = L.max_prefill_items;
+      if (grid < 1) grid = 1;
+      timing_begin(kTimedPrefill, stream);
+      prefill_tc_kernel<D, FMT><<<(unsigned)grid, 128, G::SMEM, stream>>>(PreParams{c, pv});
+      timing_end(kTimedPrefill, stream);
+    } else {
+      using G = PreGeom<D, FMT>;
+      if (!configure(prefill_kernel<D, FMT>, G::SMEM, G::THREADS, &occ, &done[dev], &occ_c[dev]))
+        return KV_INT4_ERR_CUDA;
+      long long grid = (long long)sms * occ;
+      if (grid > L.max_prefill_items) grid = L.max_prefill_items;
+      if (grid < 1) grid = 1;
+      timing_begin(kTimedPrefill, stream);
+      prefill_kernel<D, FMT><<<(unsigned)grid, G::THREADS, G::SMEM, stream>>>(PreParams{c, pv});
+      timing_end(kTimedPrefill, stream);
+    }
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
   // 3. decode + 4. reduce
