@@ -256,3 +256,55 @@ def test_full_size_long_context_sampled():
     assert pk.status.item() == 0
     assert torch.isfinite(out.float()).all()
     _check_sampled(w, q, out, seqs=[0, 255], heads=[0, 31])
+
+
+def _magnitude_kv(w, s, vmul_big):
+    """K/V of sequence s with per-block magnitudes: V x vmul_big in blocks 6
+    and 11 (V scales near 3000, far above 128), K x 3.5 in block 6 (the row
+    max rises by 4 to 8 log2 units there, where P' = p * v_scale would
+    overflow f16 unless the reference follows the max) and K x 10 in block 9
+    (a jump of more than 8 log2 units)."""
+    k, v = w.seq_kv(s, "cpu")
+    k, v = k.float(), v.float()
+    kv = k.shape[0]
+    blk = torch.arange(kv) // w.block_size
+    vmul = torch.where((blk == 6) | (blk == 11), vmul_big, 1.0)
+    kmul = torch.ones(kv)
+    kmul[blk == 6] = 3.5
+    kmul[blk == 9] = 10.0
+    return (k * kmul[:, None, None]).to(torch.bfloat16), (v * vmul[:, None, None]).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", ["int4", "int8"])
+@pytest.mark.parametrize("d", [128, 192])
+def test_prefill_rescale_policies_with_large_v_scales_and_score_jumps(fmt, d):
+    """The tensor-core prefill moves a row's exponent reference lazily only
+    while every V scale of the step is below 128; this case mixes steps of
+    both kinds with score jumps below and above the lazy threshold.  Rows
+    are compared relative to their own magnitude (max |ref| of the row, at
+    least 1)."""
+    w = synthetic.custom_workload(16, 4, d, [(150, 150), (64, 230), (1, 200)], seed=53)
+    pk = PagedKV(w, fmt=fmt)
+    caches = [t.cpu().numpy() for t in (pk.k_cache, pk.v_cache, pk.k_scale, pk.v_scale)]
+    vmul_big = 680.0 if fmt == "int4" else 1.27e5  # rotated INT4 scales ~ 4.4 sigma, int8 ~ sigma / 42
+    for s, (q, kv) in enumerate(w.seqs):
+        k, v = _magnitude_kv(w, s, vmul_big)
+        args = (k.double().numpy(), v.double().numpy(), w.slots(s, 0, kv).numpy(), *caches, w.block_size)
+        if fmt == "int4":
+            O.write_cache(*args, w.signs.numpy())
+        else:
+            O.write_cache_int8(*args)
+    _upload(pk, caches)
+    vs = caches[3][np.isfinite(caches[3])]
+    assert vs.max() > 1000 and np.median(vs) < 128
+    q = w.queries("cpu")
+    out = torch.full((w.num_q_tokens, w.num_q_heads, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pk.attend(q.cuda(), out)
+    torch.cuda.synchronize()
+    assert pk.status.item() == 0
+    args = (q.float().numpy(), *caches, w.block_table.numpy(), w.seq_lens.numpy(), w.query_start_loc.numpy(),
+            w.num_kv_heads, w.block_size, 1.0 / math.sqrt(d), w.causal)
+    ref = O.attention(*args, w.signs.numpy()) if fmt == "int4" else O.attention_int8(*args)
+    scale = np.maximum(1.0, np.abs(ref).max(axis=-1, keepdims=True))
+    assert scale.max() > 100  # the large-V blocks carry weight
+    assert_close_attention(out.float().cpu().numpy() / scale, ref / scale, what=f"{fmt} d={d} magnitudes")
