@@ -323,6 +323,11 @@ def window_bench(pk, q, out, window: int, iters: int):
             "algorithmic_bytes": nbytes}
 
 
+def prefill_kernel_name(d: int) -> str:
+    """Head sizes up to 192 take the tensor-core (tcgen05) prefill, 256 the mma.sync one."""
+    return "prefill_tc_kernel" if d <= 192 else "prefill_kernel"
+
+
 def int8_decode_bench(w, dev, iters: int):
     """The int8_per_token_head mode on this workload: a second cache (int8
     codes, no rotation) populated through kv_int8_write, then `iters`
@@ -355,7 +360,8 @@ def int8_decode_bench(w, dev, iters: int):
     step_ms = sum(kern[k][0] for k in ("prep", "prefill", "decode", "reduce")) / iters
     del pk
     torch.cuda.empty_cache()
-    return {"kernel": f"{dom}_kernel", "ms": round(ms, 5), "attention_ms": round(step_ms, 5),
+    return {"kernel": prefill_kernel_name(w.head_size) if dom == "prefill" else "decode_kernel", "ms": round(ms, 5),
+            "attention_ms": round(step_ms, 5),
             "gbs": round(nbytes / (ms / 1e3) / 1e9, 1) if dom == "decode" else None,
             "cache_bytes_read": nbytes}
 
@@ -615,7 +621,7 @@ def run_ours(args):
         achieved = flops / launch_s / 1e12 if launch_s else None
         roofline = {"bound": "tensor", "achieved": round(achieved, 2) if achieved else None, "peak": tc_peak,
                     "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4) if achieved else None,
-                    "traffic": recorded_traffic(dom, args.workload), "kernel": "prefill_kernel",
+                    "traffic": recorded_traffic(dom, args.workload), "kernel": prefill_kernel_name(d),
                     "peak_source": f"{peak_kind} bf16 dense, sustained (cuBLAS); f16 has the same nominal rate",
                     "algorithmic_flops_per_launch": flops}
     roofline["avg_launch_ms"] = round(dom_ms / dom_n, 5) if dom_n else None

@@ -1237,6 +1237,35 @@ static bool configure(K kern, int smem, int threads, int* occ_out, bool* done, i
   return true;
 }
 
+// CTAs per SM for a kernel that allocates tensor memory: the occupancy API
+// answers 1 for any such kernel, so the count is taken from the kernel's
+// registers and shared memory and the TMEM columns each CTA holds
+template <typename K>
+static bool configure_tmem(K kern, int smem, int threads, int tmem_cols, int* occ_out, bool* done, int* occ_cache) {
+  if (!*done) {
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return false;
+    cudaFuncAttributes fa;
+    int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
+      return false;
+    const int warps = (threads + 31) / 32;
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocated per warp in 256-register units
+    const int by_regs = regs_sm / (regs_warp * warps);
+    const int by_smem = smem_sm / (smem + fa.sharedSizeBytes + reserved);
+    const int by_tmem = 512 / tmem_cols;
+    const int o = min(by_regs, min(by_smem, by_tmem));
+    if (o < 1) return false;
+    *occ_cache = o;
+    *done = true;
+  }
+  *occ_out = *occ_cache;
+  return true;
+}
+
 template <int D, int FMT>
 static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   WorkspaceLayout L;
@@ -1351,7 +1380,8 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     int occ = 0;
     if constexpr (kTcPrefill) {
       using G = TcPreGeom<D, FMT>;
-      if (!configure(prefill_tc_kernel<D, FMT>, G::SMEM, 128, &occ, &done[dev], &occ_c[dev])) return KV_INT4_ERR_CUDA;
+      if (!configure_tmem(prefill_tc_kernel<D, FMT>, G::SMEM, 128, G::TMEM_COLS, &occ, &done[dev], &occ_c[dev]))
+        return KV_INT4_ERR_CUDA;
       long long grid = (long long)sms * occ;
       if (grid > L.max_prefill_items) grid = L.max_prefill_items;
       if (grid < 1) grid = 1;
