@@ -49,7 +49,8 @@ extern "C" {
 #define KV_INT4_OK 0
 #define KV_INT4_ERR_NULL 1          /* a required pointer is NULL */
 #define KV_INT4_ERR_HEAD_SIZE 2     /* head_size not in {64, 96, 128, 192, 256} */
-#define KV_INT4_ERR_HEADS 3         /* num_q_heads % num_kv_heads != 0, or a head count <= 0 */
+#define KV_INT4_ERR_HEADS 3         /* num_q_heads % num_kv_heads != 0, a head count <= 0, or a group
+                                       (num_q_heads / num_kv_heads) above 64 */
 #define KV_INT4_ERR_BLOCK_SIZE 4    /* block_size != 16 */
 #define KV_INT4_ERR_ALIGN 5         /* a pointer or stride breaks the 16-byte alignment rule */
 #define KV_INT4_ERR_WORKSPACE 6     /* workspace NULL or smaller than kv_int4_attention_workspace_size() */

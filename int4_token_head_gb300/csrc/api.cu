@@ -77,7 +77,7 @@ const char* kv_int4_status_string(int status) {
     case KV_INT4_OK: return "ok";
     case KV_INT4_ERR_NULL: return "a required pointer is NULL";
     case KV_INT4_ERR_HEAD_SIZE: return "unsupported head_size (expected 64, 96, 128, 192 or 256)";
-    case KV_INT4_ERR_HEADS: return "invalid head counts (num_q_heads must be a positive multiple of num_kv_heads)";
+    case KV_INT4_ERR_HEADS: return "invalid head counts (num_q_heads must be a positive multiple of num_kv_heads, at most 64 times it)";
     case KV_INT4_ERR_BLOCK_SIZE: return "unsupported block_size (expected 16)";
     case KV_INT4_ERR_ALIGN: return "a pointer is not 16-byte aligned or a token stride is not a multiple of 8 elements";
     case KV_INT4_ERR_WORKSPACE: return "workspace is NULL or smaller than kv_int4_attention_workspace_size()";
@@ -206,7 +206,8 @@ static int do_attention(const void* q, int64_t q_token_stride, const uint8_t* k_
   if (num_seqs < 0 || num_q_tokens < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0 ||
       max_blocks_per_seq < 0 || sliding_window < 0)
     return KV_INT4_ERR_SIZE;
-  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return KV_INT4_ERR_HEADS;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > kPrefillRows)
+    return KV_INT4_ERR_HEADS;
   if (!head_size_ok(head_size)) return KV_INT4_ERR_HEAD_SIZE;
   if (block_size != 16) return KV_INT4_ERR_BLOCK_SIZE;
   if (num_seqs == 0 || num_q_tokens == 0) return KV_INT4_OK;

@@ -1219,6 +1219,7 @@ __global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PrePa
 }
 
 #include "prefill_tc.cuh"
+#include "prefill_ws.cuh"
 
 // ---------------------------------------------------------------------------
 // host launcher
@@ -1254,7 +1255,7 @@ static bool configure_tmem(K kern, int smem, int threads, int tmem_cols, int* oc
       return false;
     const int warps = (threads + 31) / 32;
     const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocated per warp in 256-register units
-    const int by_regs = regs_sm / (regs_warp * warps);
+    const int by_regs = regs_sm / (regs_warp * ((warps + 3) / 4 * 4));  // and per group of four warps
     const int by_smem = smem_sm / (smem + fa.sharedSizeBytes + reserved);
     const int by_tmem = 512 / tmem_cols;
     const int o = min(by_regs, min(by_smem, by_tmem));
@@ -1299,10 +1300,10 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.out = static_cast<uint16_t*>(a.out);
   c.out_stride = a.out_stride;
   c.status = a.dev_status;
-  // prefill tiles: 128 rows on the tensor-core kernel (head sizes up to 192),
-  // 64 on the warp-MMA one
+  // prefill items: 256 rows on the warp-specialised tensor-core kernel
+  // (head sizes up to 192), 64 on the warp-MMA one
   constexpr bool kTcPrefill = D <= 192;
-  constexpr int kTileRows = kTcPrefill ? 128 : kPrefillRows;
+  constexpr int kTileRows = kTcPrefill ? kWsRows : kPrefillRows;
   c.tile_tokens = kTileRows / c.group > 0 ? kTileRows / c.group : 1;
   c.max_items = L.max_prefill_items;
   // kv heads per decode CTA: the largest divisor of Hkv up to 8 whose
@@ -1379,14 +1380,14 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     static int occ_c[kMaxDevices] = {};
     int occ = 0;
     if constexpr (kTcPrefill) {
-      using G = TcPreGeom<D, FMT>;
-      if (!configure_tmem(prefill_tc_kernel<D, FMT>, G::SMEM, 128, G::TMEM_COLS, &occ, &done[dev], &occ_c[dev]))
+      using G = WsGeom<D, FMT>;
+      if (!configure_tmem(prefill_ws_kernel<D, FMT>, G::SMEM, G::THREADS, G::TMEM_COLS, &occ, &done[dev], &occ_c[dev]))
         return KV_INT4_ERR_CUDA;
       long long grid = (long long)sms * occ;
       if (grid > L.max_prefill_items) grid = L.max_prefill_items;
       if (grid < 1) grid = 1;
       timing_begin(kTimedPrefill, stream);
-      prefill_tc_kernel<D, FMT><<<(unsigned)grid, 128, G::SMEM, stream>>>(PreParams{c, pv});
+      prefill_ws_kernel<D, FMT><<<(unsigned)grid, G::THREADS, G::SMEM, stream>>>(PreParams{c, pv});
       timing_end(kTimedPrefill, stream);
     } else {
       using G = PreGeom<D, FMT>;

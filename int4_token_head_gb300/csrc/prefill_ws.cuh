@@ -1,0 +1,552 @@
+// Warp-specialised prefill on the tcgen05 tensor cores, included by
+// attention.cu after prefill_tc.cuh (whose tile helpers it shares).
+//
+// One CTA per SM (all 512 TMEM columns), one item = 256 query rows
+// (query token x q head of one kv group) in two halves of 128, the MMA's M.
+// Thirteen warps in three roles, 64 keys (four cache blocks) per step:
+//   * dequant warps (8-11): stage the step's codes and scales with
+//     cp.async (two staging buffers), dequantise K into one f16 tile and V
+//     into one of two (exact, as in the single-CTA kernel), and copy the
+//     step's K/V scales and block flags into a two-entry ring;
+//   * MMA warp (12, one lane issues): S_h = Q_h K^T into TMEM columns
+//     [64h, 64h + 64); O_h += P_h V with P_h read from TMEM (the A operand
+//     of the MMA may live in tensor memory) into columns
+//     [128 + hD, 128 + (h+1)D).  Issue order S0 S1 | PV0 S0' | PV1 S1' | ...
+//     lets each half's softmax run while the other half's MMAs do;
+//   * softmax warps (0-3 for half 0, 4-7 for half 1): one query row per
+//     thread, the same masked base-2 online softmax with the lazy exponent
+//     reference as the single-CTA kernel, P' = p * v_scale written back as
+//     f16 pairs over the row's S columns; then the epilogue.
+// Hand-offs are mbarriers (every wait bounded; a wait that runs out sets
+// KV_INT4_DEV_TIMEOUT and a CTA-wide abort flag that ends every later
+// wait at once, so a fault in the pipeline costs one time-out, not one
+// per step):
+//   kfull  (dequant -> MMA)  K tile and the step's ring entry written
+//   vfull[b] (dequant -> MMA) V tile b written
+//   kfree  (MMA commit -> dequant) S0 and S1 of the step complete
+//   vfree[b] (MMA commit -> dequant) PV0 and PV1 that read V tile b complete
+//   sfull[h] (MMA commit -> softmax h) S_h complete (and every earlier MMA)
+//   pfull[h] (softmax h -> MMA) P_h in TMEM, O_h rescaled if it had to be
+//   odone  (MMA commit -> softmax) the item's last PV complete
+// The ring entry of step j is rewritten at step j + 2 only after kfree of
+// step j + 1, which follows both halves' P of step j.
+
+constexpr int kWsRows = 256;  // query rows per item
+
+template <int D, int FMT>
+struct WsGeom {
+  static constexpr int ROWS = kWsRows;
+  static constexpr int NK = 64;                       // keys per step
+  static constexpr int KB = (D + 63) / 64;            // 128-byte blocks of an f16 head vector
+  static constexpr int QBYTES = ROWS * 128 * KB;
+  static constexpr int KVBYTES = NK * 128 * KB;       // one K or V tile
+  static constexpr int CB = FMT == kFmtInt8 ? D : D / 2;
+  static constexpr int SC_OFF = 4 * 2 * 16 * CB;      // staging: codes [block][K/V][16][CB], scales, flags
+  static constexpr int FL_OFF = SC_OFF + 4 * 2 * 16 * 4;
+  static constexpr int STG = (FL_OFF + 16 + 127) / 128 * 128;
+  static constexpr int RING = 2 * NK * 4 + 32;        // K scales, V scales, 4 block flags, 2 votes
+  static constexpr int TMEM_COLS = 128 + 2 * D <= 256 ? 256 : 512;
+  static constexpr int NBARS = 12;
+  static constexpr int USED = 1024 + QBYTES + 3 * KVBYTES + 2 * STG + 2 * RING + D * 4 + NBARS * 8 + 32;
+  static constexpr int SMEM = USED;
+  static constexpr int THREADS = 13 * 32;
+  static_assert(D % 32 == 0 && D <= 192, "head sizes served by the warp-specialised prefill");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// a bounded mbarrier wait that gives up at once after any wait of the CTA
+// has run out (abort flag set)
+__device__ __forceinline__ bool ws_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status) {
+  for (int n = 0; n < kMaxWaitIters; n++) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255) == 255 && *abort) return false;
+  }
+  *abort = 1;
+  flag(status, KV_INT4_DEV_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// named barrier over the dequant warps only
+__device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+// named barrier over the softmax warps and the MMA warp: the item's Q' tile is written
+__device__ __forceinline__ void q_sync() { asm volatile("bar.sync 2, 288;\n" ::: "memory"); }
+
+template <int D, int FMT>
+__global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
+  using G = WsGeom<D, FMT>;
+  constexpr bool ROT = FMT == kFmtInt4;
+  constexpr int B = Head<D>::b;
+  constexpr int KSTEPS = D / 16;
+  constexpr int NK = G::NK, ROWS = G::ROWS;
+  constexpr uint32_t IDESC_S = umma_idesc_f16(128, NK, false);
+  constexpr uint32_t IDESC_O = umma_idesc_f16(128, D, true);
+  const Common& c = prm.c;
+  const PlanView& pv = prm.pv;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* const sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* const sQ = sm;                     // [KB][256 rows][128 B], swizzled
+  uint8_t* const sK = sQ + G::QBYTES;         // [KB][64 keys][128 B]
+  uint8_t* const sV = sK + G::KVBYTES;        // two V tiles
+  uint8_t* const stg = sV + 2 * G::KVBYTES;   // two staging buffers
+  uint8_t* const ring = stg + 2 * G::STG;     // two entries: K scales [64], V scales [64], flags [4], votes [2]
+  float* const ssign = reinterpret_cast<float*>(ring + 2 * G::RING);
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(ssign + D);
+  int* const sitem = reinterpret_cast<int*>(bars + G::NBARS);  // item [4], abort flag
+  uint32_t* const tslot = reinterpret_cast<uint32_t*>(sitem + 6);
+  volatile int* const abort_flag = sitem + 4;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // barrier indices
+  enum { KFULL = 0, VFULL = 1, KFREE = 3, VFREE = 4, SFULL = 6, PFULL = 8, ODONE = 10, DRAIN = 11 };
+  auto bar = [&](int i) { return smem_addr(&bars[i]); };
+  for (int i = tid; i < D; i += G::THREADS) ssign[i] = (ROT && c.signs[i] < 0) ? -1.f : 1.f;
+  if (tid == 0) {
+    mbar_init(bar(KFULL), 4);
+    mbar_init(bar(VFULL), 4);
+    mbar_init(bar(VFULL + 1), 4);
+    mbar_init(bar(KFREE), 1);
+    mbar_init(bar(VFREE), 1);
+    mbar_init(bar(VFREE + 1), 1);
+    mbar_init(bar(SFULL), 1);
+    mbar_init(bar(SFULL + 1), 1);
+    mbar_init(bar(PFULL), 4);
+    mbar_init(bar(PFULL + 1), 4);
+    mbar_init(bar(ODONE), 1);
+    mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_addr(tslot), G::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  // phase bits of the barriers each role waits on (one completion per wait)
+  uint32_t ph_kfull = 0, ph_vfull = 0, ph_kfree = 0, ph_vfree = 0, ph_sfull = 0, ph_pfull = 0, ph_odone = 0;
+  const int n_items = pv.plan[1], n_pseq = pv.plan[3];
+
+#pragma unroll 1
+  while (true) {
+    if (tid == 0) {
+      // next item: (prefill sequence, tile in descending order of work, kv head)
+      const int itn = *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1);
+      int4 it = make_int4(-1, 0, 0, 0);
+      if (itn < n_items) {
+        int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pv.ptab[mid].y <= itn) lo = mid;
+          else hi = mid;
+        }
+        const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
+        const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
+        const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
+        const int t = ntiles - 1 - r / c.hkv;
+        const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
+        it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
+      }
+      sitem[0] = it.x; sitem[1] = it.y; sitem[2] = it.z; sitem[3] = it.w;
+    }
+    __syncthreads();
+    const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
+    if (item.x < 0) break;
+    const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
+    const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+    const int L = c.seq_lens[seq], ctx = L - ql;
+    const int tok0 = tile * c.tile_tokens;
+    const int ntok = min(c.tile_tokens, ql - tok0);
+    const int nrows = ntok * c.group;
+    const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
+    const int nsteps = (nkb - kb0 + 3) / 4;
+
+    if (warp >= 8 && warp < 12) {
+      // ================= dequant warps =================
+      const int dt = tid - 256;
+      // stage step st into staging buffer sb: thread (block b4, K/V, row)
+      // copies one code row and its scale
+      auto issue = [&](int st, uint8_t* sb) {
+        const int b4 = dt >> 5, kv = (dt >> 4) & 1, row = dt & 15;
+        const int kb = kb0 + st * 4 + b4;
+        const int blk = kb < nkb ? c.block_table[(long long)seq * c.max_blocks + kb] : -1;
+        const bool ok = kb < nkb && blk >= 0 && blk < c.num_blocks;
+        if (ok) {
+          const uint8_t* src = (kv ? c.v_cache : c.k_cache) + (long long)blk * c.geo.cblk + row * c.geo.crow +
+                               (long long)h * c.geo.chead;
+          uint8_t* dst = sb + ((b4 * 2 + kv) * 16 + row) * G::CB;
+#pragma unroll
+          for (int col = 0; col < G::CB / 16; col++) cp_async16(dst + col * 16, src + col * 16);
+          cp_async4(sb + G::SC_OFF + ((b4 * 2 + kv) * 16 + row) * 4,
+                    (kv ? c.v_scale : c.k_scale) + (long long)blk * c.geo.sblk + row * c.geo.srow +
+                        (long long)h * c.geo.shead);
+        }
+        if (kv == 0 && row == 0) {
+          reinterpret_cast<int*>(sb + G::FL_OFF)[b4] = ok;
+          if (kb < nkb && !ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
+        }
+      };
+      // dequantise the K (kv = 0) or V (kv = 1) codes of staging sb into a tile
+      auto dequant = [&](const uint8_t* sb, uint8_t* tile_dst, int kv, int fmask) {
+        constexpr int CPK = D / 8;                        // 16-byte f16 chunks per key
+        constexpr int CBYTES = FMT == kFmtInt8 ? 8 : 4;   // code bytes of 8 elements
+#pragma unroll 4
+        for (int q = dt; q < NK * CPK; q += 128) {
+          const int k = q / CPK, ch = q - k * CPK;
+          const int b4 = k >> 4;
+          const uint8_t* src = sb + (b4 * 16 + k + kv * 16) * G::CB + ch * CBYTES;  // row (b4, kv, k & 15)
+          *reinterpret_cast<uint4*>(tile_dst + sw128(NK, k, ch)) = dequant8<FMT>(src, (fmask >> b4) & 1);
+        }
+      };
+      issue(0, stg);
+      cp_async_commit();
+      if (nsteps > 1) issue(1, stg + G::STG);
+      cp_async_commit();
+#pragma unroll 1
+      for (int j = 0; j < nsteps; j++) {
+        const int b = j & 1;
+        uint8_t* const sb = stg + b * G::STG;
+        cp_async_wait<1>();
+        dq_sync();  // every thread's copies of step j have landed
+        if (j >= 1) {
+          ws_wait(bar(KFREE), ph_kfree, abort_flag, c.status);  // S of step j - 1 done: K tile and ring[b] free
+          ph_kfree ^= 1;
+        }
+        const int* sfl = reinterpret_cast<const int*>(sb + G::FL_OFF);
+        uint8_t* const re = ring + b * G::RING;
+        const int fmask = (sfl[0] != 0) | (sfl[1] != 0) << 1 | (sfl[2] != 0) << 2 | (sfl[3] != 0) << 3;
+        if (dt < NK) {
+          const float* scs = reinterpret_cast<const float*>(sb + G::SC_OFF);
+          const float vsc = scs[(dt >> 4) * 32 + 16 + (dt & 15)];
+          reinterpret_cast<float*>(re)[dt] = scs[(dt >> 4) * 32 + (dt & 15)];
+          reinterpret_cast<float*>(re)[NK + dt] = vsc;
+          // the vote reads only keys that exist (usable block, position below the
+          // sequence length): the threshold, and so the rounding, depend on the
+          // cache's contents alone
+          const bool exists = ((fmask >> (dt >> 4)) & 1) && (kb0 + j * 4) * 16 + dt < L;
+          const bool small = __all_sync(0xffffffffu, !exists || fabsf(vsc) < 128.f);
+          if (lane == 0) reinterpret_cast<int*>(re + 2 * NK * 4)[4 + (dt >> 5)] = small;
+        } else if (dt < NK + 4) {
+          reinterpret_cast<int*>(re + 2 * NK * 4)[dt - NK] = sfl[dt - NK];
+        }
+        dequant(sb, sK, 0, fmask);
+        fence_proxy_async_smem();  // the tile is read by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KFULL));
+        if (j >= 2) {
+          ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);  // PVs of step j - 2 done
+          ph_vfree ^= 1u << b;
+        }
+        dequant(sb, sV + b * G::KVBYTES, 1, fmask);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(VFULL + b));
+        dq_sync();  // every thread is done with staging b
+        if (j + 2 < nsteps) issue(j + 2, sb);
+        cp_async_commit();
+      }
+      cp_async_wait<0>();
+      // the completions not waited for above: kfree of the last step, vfree of the last use of each V tile
+      if (nsteps >= 1) {
+        ws_wait(bar(KFREE), ph_kfree, abort_flag, c.status);
+        ph_kfree ^= 1;
+      }
+      for (int b = 0; b < 2 && b < nsteps; b++) {
+        ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
+        ph_vfree ^= 1u << b;
+      }
+    } else if (warp == 12) {
+      // ================= MMA warp (lane 0 issues, the warp waits together) =================
+      const bool leader = lane == 0;
+      const uint32_t qa = smem_addr(sQ), ka = smem_addr(sK), va = smem_addr(sV);
+      // S_h = Q_h K^T over the head dimension into TMEM columns [64h, 64h + 64)
+      auto issue_s = [&](int hh) {
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ks++)
+            umma_f16(tmem + 64 * hh,
+                     umma_desc(qa + (ks >> 2) * ROWS * 128 + hh * 128 * 128 + (ks & 3) * 32, 16, 1024),
+                     umma_desc(ka + (ks >> 2) * NK * 128 + (ks & 3) * 32, 16, 1024), IDESC_S, ks > 0);
+        }
+      };
+      // O_h += P_h V_b, P_h the f16 pairs over S_h's first 32 columns
+      auto issue_pv = [&](int hh, int b, bool first) {
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++)
+            umma_f16_ts(tmem + 128 + hh * D, tmem + 64 * hh + kk * 8,
+                        umma_desc(va + b * G::KVBYTES + kk * 2048, NK * 128, 1024), IDESC_O, !first || kk > 0);
+        }
+      };
+      auto commit = [&](int i) {
+        if (leader) umma_commit(bar(i));
+        __syncwarp();
+      };
+      q_sync();  // the softmax warps have written Q'
+      if (nsteps > 0) {
+        ws_wait(bar(KFULL), ph_kfull, abort_flag, c.status);
+        ph_kfull ^= 1;
+        tc_fence_after();
+        issue_s(0);
+        commit(SFULL);
+        issue_s(1);
+        commit(SFULL + 1);
+        commit(KFREE);
+      }
+#pragma unroll 1
+      for (int j = 0; j < nsteps; j++) {
+        const int b = j & 1;
+        ws_wait(bar(PFULL), ph_pfull & 1, abort_flag, c.status);
+        ph_pfull ^= 1;
+        ws_wait(bar(VFULL + b), (ph_vfull >> b) & 1, abort_flag, c.status);
+        ph_vfull ^= 1u << b;
+        tc_fence_after();
+        issue_pv(0, b, j == 0);
+        if (j + 1 < nsteps) {
+          ws_wait(bar(KFULL), ph_kfull, abort_flag, c.status);
+          ph_kfull ^= 1;
+          tc_fence_after();
+          issue_s(0);
+          commit(SFULL);
+        }
+        ws_wait(bar(PFULL + 1), (ph_pfull >> 1) & 1, abort_flag, c.status);
+        ph_pfull ^= 2;
+        tc_fence_after();
+        issue_pv(1, b, j == 0);
+        commit(VFREE + b);
+        if (j + 1 < nsteps) {
+          issue_s(1);
+          commit(SFULL + 1);
+          commit(KFREE);
+        }
+      }
+      commit(ODONE);
+    } else if (warp < 8) {
+      // ================= softmax warps: half hf, one query row per thread =================
+      const int hf = warp >> 2;
+      const int r = tid;  // row of the item (half hf holds rows [128 hf, 128 hf + 128))
+      const int j = r / c.group, jj = r - j * c.group;
+      const bool rok = r < nrows;
+      {
+        const __half* src = pv.qrot + ((long long)(q0 + tok0 + (rok ? j : 0)) * c.hq + h * c.group + (rok ? jj : 0)) * D;
+#pragma unroll 4
+        for (int ch = 0; ch < D / 8; ch++) {
+          uint4 v = rok ? reinterpret_cast<const uint4*>(src)[ch] : make_uint4(0, 0, 0, 0);
+          if constexpr (FMT == kFmtInt4) {
+            // the tiles' nibble order: (q0, q4), (q1, q5), (q2, q6), (q3, q7)
+            v = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                           __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+          }
+          *reinterpret_cast<uint4*>(sQ + sw128(ROWS, r, ch)) = v;
+        }
+      }
+      fence_proxy_async_smem();  // Q' is read by the tensor cores
+      q_sync();
+      const int qp = ctx + tok0 + (rok ? j : 0);
+      const int lim = c.causal ? min(L, qp + 1) : L;
+      const int lo = window_lo(c, qp);
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + 64 * hf + lane_off, tO = tmem + 128 + hf * D + lane_off;
+      float m_ref = -INFINITY, l_run = 0.f;  // exponent reference of the row, sum of its weights
+#pragma unroll 1
+      for (int st = 0; st < nsteps; st++) {
+        const uint8_t* re = ring + (st & 1) * G::RING;
+        const float* sks = reinterpret_cast<const float*>(re);
+        const float* svs = sks + NK;
+        const int* sfl = reinterpret_cast<const int*>(re + 2 * NK * 4);
+        ws_wait(bar(SFULL + hf), ph_sfull, abort_flag, c.status);
+        ph_sfull ^= 1;
+        tc_fence_after();
+        float sv[NK];
+        {
+          float t0[32], t1[32];
+          tmem_ld32(tS, t0);
+          tmem_ld32(tS + 32, t1);
+#pragma unroll
+          for (int k = 0; k < 32; k++) {
+            sv[k] = t0[k];
+            sv[32 + k] = t1[k];
+          }
+        }
+        const int pos0 = (kb0 + st * 4) * 16;
+        const float tau = (sfl[4] && sfl[5]) ? 8.f : 0.f;
+        // a step wholly inside the row's visible range over usable blocks needs no mask
+        const bool full = pos0 >= lo && pos0 + NK <= lim && sfl[0] && sfl[1] && sfl[2] && sfl[3];
+        const float4* ks4 = reinterpret_cast<const float4*>(sks);
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < NK; k += 4) {
+            const float4 f = ks4[k / 4];
+            const float2 a = __fmul2_rn(make_float2(sv[k], sv[k + 1]), make_float2(f.x, f.y));
+            const float2 bb = __fmul2_rn(make_float2(sv[k + 2], sv[k + 3]), make_float2(f.z, f.w));
+            sv[k] = a.x; sv[k + 1] = a.y; sv[k + 2] = bb.x; sv[k + 3] = bb.y;
+            mx4[0] = fmaxf(mx4[0], a.x); mx4[1] = fmaxf(mx4[1], a.y);
+            mx4[2] = fmaxf(mx4[2], bb.x); mx4[3] = fmaxf(mx4[3], bb.y);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < NK; k++) {
+            const int pos = pos0 + k;
+            const bool vis = sfl[k >> 4] != 0 && pos >= lo && pos < lim;
+            sv[k] = vis ? sv[k] * sks[k] : -INFINITY;
+            mx4[k & 3] = fmaxf(mx4[k & 3], sv[k]);
+          }
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        // the reference moves when the row max passes it by more than tau; a
+        // row with no visible key so far (O' = 0, l = 0) takes the max as is
+        const bool grow = m_ref != -INFINITY && mx > m_ref + tau;
+        const float alpha = grow ? fast_exp2(m_ref - mx) : 1.f;
+        if (grow || m_ref == -INFINITY) m_ref = mx;
+        if (__any_sync(0xffffffffu, grow)) {
+          // O' of this half is complete up to the previous step (S_h of this step was issued after it)
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; cc++) {
+            float o[32];
+            tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; i++) o[i] *= alpha;
+            tmem_st32(tO + cc * 32, o);
+          }
+        }
+        l_run *= alpha;
+        float pf[NK / 2];  // P' as f16 pairs (bit patterns)
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4* vs4 = reinterpret_cast<const float4*>(svs);
+        if (full) {
+          const float2 nm = make_float2(-m_ref, -m_ref);
+#pragma unroll
+          for (int k = 0; k < NK; k += 4) {
+            const float4 f = vs4[k / 4];
+            const float2 da = __fadd2_rn(make_float2(sv[k], sv[k + 1]), nm);
+            const float2 db = __fadd2_rn(make_float2(sv[k + 2], sv[k + 3]), nm);
+            const float2 pa = make_float2(fast_exp2(da.x), fast_exp2(da.y));
+            const float2 pb = make_float2(fast_exp2(db.x), fast_exp2(db.y));
+            ps[0] += pa.x; ps[1] += pa.y; ps[2] += pb.x; ps[3] += pb.y;
+            const float2 wa = __fmul2_rn(pa, make_float2(f.x, f.y));
+            const float2 wb = __fmul2_rn(pb, make_float2(f.z, f.w));
+            pf[k / 2] = __uint_as_float(pack_f16x2(wa.x, wa.y));
+            pf[k / 2 + 1] = __uint_as_float(pack_f16x2(wb.x, wb.y));
+          }
+        } else {
+          const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+          for (int k = 0; k < NK; k += 2) {
+            const float p0 = sv[k] == -INFINITY ? 0.f : fast_exp2(sv[k] - mu);
+            const float p1 = sv[k + 1] == -INFINITY ? 0.f : fast_exp2(sv[k + 1] - mu);
+            ps[k & 3] += p0;
+            ps[(k & 3) + 1] += p1;
+            // masked keys may carry unwritten (NaN) scales: select, do not multiply
+            const float w0 = p0 == 0.f ? 0.f : p0 * svs[k];
+            const float w1 = p1 == 0.f ? 0.f : p1 * svs[k + 1];
+            pf[k / 2] = __uint_as_float(pack_f16x2(w0, w1));
+          }
+        }
+        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        tmem_st32(tS, pf);  // P' over the row's first 32 S columns (S is consumed)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(PFULL + hf));
+      }
+
+      // ---- epilogue: normalise, inverse rotation (INT4), bf16 store ----
+      ws_wait(bar(ODONE), ph_odone, abort_flag, c.status);
+      ph_odone ^= 1;
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / (l_run * (ROT ? (float)B : 1.f)) : 0.f;
+      uint16_t* dst = c.out + (long long)(q0 + tok0 + (rok ? j : 0)) * c.out_stride + (long long)(h * c.group + jj) * D;
+      // store 8 natural-order outputs y(i0 .. i0 + 7) (a row that saw no usable key, l = 0, as zeros)
+      auto store8 = [&](int col, const float (&y)[8]) {
+        float z[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) z[e] = l_run > 0.f ? y[e] * inv * ssign[col + e] : 0.f;
+        *reinterpret_cast<uint4*>(dst + col) =
+            make_uint4(pack_bf16x2_rn(z[0], z[1]), pack_bf16x2_rn(z[2], z[3]), pack_bf16x2_rn(z[4], z[5]),
+                       pack_bf16x2_rn(z[6], z[7]));
+      };
+      // TMEM column slot of natural element i within a chunk (INT4 columns are in nibble order)
+      auto slot = [](int i) { return FMT == kFmtInt4 ? (i & ~7) + (i & 3) * 2 + ((i >> 2) & 1) : i; };
+      constexpr int CHUNK = (ROT && B > 32) ? (B > 64 ? 64 : B) : 32;  // columns transformed in registers
+#pragma unroll 1
+      for (int base = 0; base < D; base += CHUNK) {
+        float o[CHUNK];  // TMEM column order
+#pragma unroll
+        for (int cc = 0; cc < CHUNK / 32; cc++) tmem_ld32(tO + base + cc * 32, *reinterpret_cast<float(*)[32]>(o + cc * 32));
+        if constexpr (ROT) {
+          // H over each CHUNK-block (H_b itself when b <= 64)
+#pragma unroll
+          for (int hh = 1; hh < (B < CHUNK ? B : CHUNK); hh <<= 1) {
+#pragma unroll
+            for (int i = 0; i < CHUNK; i++) {
+              if ((i & hh) == 0) {
+                const float a0 = o[slot(i)], b0 = o[slot(i + hh)];
+                o[slot(i)] = a0 + b0;
+                o[slot(i + hh)] = a0 - b0;
+              }
+            }
+          }
+        }
+        if constexpr (ROT && B > 64) {
+          // b = 128: park the H_64 halves in TMEM in natural order for the last stage
+          float nat[CHUNK];
+#pragma unroll
+          for (int i = 0; i < CHUNK; i++) nat[i] = o[slot(i)];
+#pragma unroll
+          for (int cc = 0; cc < CHUNK / 32; cc++) tmem_st32(tO + base + cc * 32, *reinterpret_cast<float(*)[32]>(nat + cc * 32));
+        } else if (rok) {
+#pragma unroll
+          for (int i = 0; i < CHUNK; i += 8) {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) y[e] = o[slot(i + e)];
+            store8(base + i, y);
+          }
+        }
+      }
+      if constexpr (ROT && B > 64) {
+        static_assert(B == 128, "the two-pass epilogue takes b = 128");
+        // H_128 = (H_2 (x) I_64)(I_2 (x) H_64): pair natural columns i and i + 64 of each 128-block
+#pragma unroll 1
+        for (int base = 0; base < D; base += 128) {
+#pragma unroll 1
+          for (int q = 0; q < 64; q += 32) {
+            float a[32], b2[32];
+            tmem_ld32(tO + base + q, a);
+            tmem_ld32(tO + base + 64 + q, b2);
+            if (rok) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                float y0[8], y1[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                  y0[e] = a[i + e] + b2[i + e];
+                  y1[e] = a[i + e] - b2[i + e];
+                }
+                store8(base + q + i, y0);
+                store8(base + 64 + q + i, y1);
+              }
+            }
+          }
+        }
+      }
+    }
+    // item end: every role is done with TMEM, the tiles and the ring
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (warp == 12) {
+    // after a time-out MMAs may still be in flight: they end by themselves
+    // (they wait on nothing) and must end before the columns are freed
+    if (lane == 0) umma_commit(bar(DRAIN));
+    __syncwarp();
+    if (!mbar_wait_bounded(bar(DRAIN), 0)) flag(c.status, KV_INT4_DEV_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, G::TMEM_COLS);
+}

@@ -124,6 +124,7 @@ def test_attention_validation(lib):
     assert _attn(lib, wsb=1024) == D["KV_INT4_ERR_WORKSPACE"]
     assert _attn(lib, hkv=6) == D["KV_INT4_ERR_HEADS"]
     assert _attn(lib, hq=0) == D["KV_INT4_ERR_HEADS"]
+    assert _attn(lib, hq=64 * 8) != D["KV_INT4_ERR_HEADS"] and _attn(lib, hq=65 * 8) == D["KV_INT4_ERR_HEADS"]
     assert _attn(lib, d=72) == D["KV_INT4_ERR_HEAD_SIZE"]
     assert _attn(lib, bs=8) == D["KV_INT4_ERR_BLOCK_SIZE"]
     assert _attn(lib, out=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
