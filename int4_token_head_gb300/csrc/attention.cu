@@ -93,6 +93,7 @@ struct Common {
   int hq;
   int hkv;
   int group;
+  FastDiv gdiv{1};  // division by group
   int num_blocks;
   int causal;
   int window;    // sliding window (0: none): the query at position p sees no key at p - window or before
@@ -1291,6 +1292,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.hq = a.num_q_heads;
   c.hkv = a.num_kv_heads;
   c.group = a.num_q_heads / a.num_kv_heads;
+  c.gdiv = FastDiv((uint32_t)c.group);
   c.num_blocks = a.num_blocks;
   c.causal = a.causal;
   c.window = a.sliding_window;

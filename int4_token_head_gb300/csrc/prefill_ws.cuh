@@ -3,12 +3,12 @@
 //
 // One CTA per SM (all 512 TMEM columns), one item = 256 query rows
 // (query token x q head of one kv group) in two halves of 128, the MMA's M.
-// Thirteen warps in three roles, 64 keys (four cache blocks) per step:
-//   * dequant warps (8-11): stage the step's codes and scales with
+// Sixteen warps in three roles, 64 keys (four cache blocks) per step:
+//   * dequant warps (8-14): stage the step's codes and scales with
 //     cp.async (two staging buffers), dequantise K into one f16 tile and V
 //     into one of two (exact, as in the single-CTA kernel), and copy the
 //     step's K/V scales and block flags into a two-entry ring;
-//   * MMA warp (12, one lane issues): S_h = Q_h K^T into TMEM columns
+//   * MMA warp (15, one lane issues): S_h = Q_h K^T into TMEM columns
 //     [64h, 64h + 64); O_h += P_h V with P_h read from TMEM (the A operand
 //     of the MMA may live in tensor memory) into columns
 //     [128 + hD, 128 + (h+1)D).  Issue order S0 S1 | PV0 S0' | PV1 S1' | ...
@@ -49,7 +49,8 @@ struct WsGeom {
   static constexpr int NBARS = 12;
   static constexpr int USED = 1024 + QBYTES + 3 * KVBYTES + 2 * STG + 2 * RING + D * 4 + NBARS * 8 + 32;
   static constexpr int SMEM = USED;
-  static constexpr int THREADS = 13 * 32;
+  static constexpr int THREADS = 16 * 32;
+  static constexpr int DQ_WARPS = 7;  // warps 8 .. 14
   static_assert(D % 32 == 0 && D <= 192, "head sizes served by the warp-specialised prefill");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -71,12 +72,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // named barrier over the dequant warps only
-__device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+__device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 1, 224;\n" ::: "memory"); }
 // named barrier over the softmax warps and the MMA warp: the item's Q' tile is written
 __device__ __forceinline__ void q_sync() { asm volatile("bar.sync 2, 288;\n" ::: "memory"); }
+// named barrier over the softmax warps
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 3, 256;\n" ::: "memory"); }
 
 template <int D, int FMT>
-__global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
+__global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
   using G = WsGeom<D, FMT>;
   constexpr bool ROT = FMT == kFmtInt4;
   constexpr int B = Head<D>::b;
@@ -105,9 +108,9 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
   for (int i = tid; i < D; i += G::THREADS) ssign[i] = (ROT && c.signs[i] < 0) ? -1.f : 1.f;
   if (tid == 0) {
-    mbar_init(bar(KFULL), 4);
-    mbar_init(bar(VFULL), 4);
-    mbar_init(bar(VFULL + 1), 4);
+    mbar_init(bar(KFULL), G::DQ_WARPS);
+    mbar_init(bar(VFULL), G::DQ_WARPS);
+    mbar_init(bar(VFULL + 1), G::DQ_WARPS);
     mbar_init(bar(KFREE), 1);
     mbar_init(bar(VFREE), 1);
     mbar_init(bar(VFREE + 1), 1);
@@ -163,15 +166,20 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
     const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
     const int nsteps = (nkb - kb0 + 3) / 4;
 
-    if (warp >= 8 && warp < 12) {
+    if (warp >= 8 && warp < 15) {
       // ================= dequant warps =================
       const int dt = tid - 256;
-      // stage step st into staging buffer sb: thread (block b4, K/V, row)
-      // copies one code row and its scale
-      auto issue = [&](int st, uint8_t* sb) {
+      // staging is done by the first 128 dequant threads: thread (block b4,
+      // K/V, row) copies one code row and its scale; the block id of a step
+      // is loaded a step before its copies are issued
+      auto block_of = [&](int st) -> int {
+        const int kb = kb0 + st * 4 + (dt >> 5);
+        return (dt < 128 && kb < nkb) ? c.block_table[(long long)seq * c.max_blocks + kb] : -1;
+      };
+      auto issue = [&](int st, uint8_t* sb, int blk) {
+        if (dt >= 128) return;
         const int b4 = dt >> 5, kv = (dt >> 4) & 1, row = dt & 15;
         const int kb = kb0 + st * 4 + b4;
-        const int blk = kb < nkb ? c.block_table[(long long)seq * c.max_blocks + kb] : -1;
         const bool ok = kb < nkb && blk >= 0 && blk < c.num_blocks;
         if (ok) {
           const uint8_t* src = (kv ? c.v_cache : c.k_cache) + (long long)blk * c.geo.cblk + row * c.geo.crow +
@@ -193,17 +201,18 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
         constexpr int CPK = D / 8;                        // 16-byte f16 chunks per key
         constexpr int CBYTES = FMT == kFmtInt8 ? 8 : 4;   // code bytes of 8 elements
 #pragma unroll 4
-        for (int q = dt; q < NK * CPK; q += 128) {
+        for (int q = dt; q < NK * CPK; q += 32 * G::DQ_WARPS) {
           const int k = q / CPK, ch = q - k * CPK;
           const int b4 = k >> 4;
           const uint8_t* src = sb + (b4 * 16 + k + kv * 16) * G::CB + ch * CBYTES;  // row (b4, kv, k & 15)
           *reinterpret_cast<uint4*>(tile_dst + sw128(NK, k, ch)) = dequant8<FMT>(src, (fmask >> b4) & 1);
         }
       };
-      issue(0, stg);
+      issue(0, stg, block_of(0));
       cp_async_commit();
-      if (nsteps > 1) issue(1, stg + G::STG);
+      if (nsteps > 1) issue(1, stg + G::STG, block_of(1));
       cp_async_commit();
+      int blk_next = block_of(2);
 #pragma unroll 1
       for (int j = 0; j < nsteps; j++) {
         const int b = j & 1;
@@ -244,8 +253,9 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(VFULL + b));
         dq_sync();  // every thread is done with staging b
-        if (j + 2 < nsteps) issue(j + 2, sb);
+        if (j + 2 < nsteps) issue(j + 2, sb, blk_next);
         cp_async_commit();
+        blk_next = block_of(j + 3);
       }
       cp_async_wait<0>();
       // the completions not waited for above: kfree of the last step, vfree of the last use of each V tile
@@ -257,7 +267,7 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
         ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
         ph_vfree ^= 1u << b;
       }
-    } else if (warp == 12) {
+    } else if (warp == 15) {
       // ================= MMA warp (lane 0 issues, the warp waits together) =================
       const bool leader = lane == 0;
       const uint32_t qa = smem_addr(sQ), ka = smem_addr(sK), va = smem_addr(sV);
@@ -329,17 +339,35 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
       const int r = tid;  // row of the item (half hf holds rows [128 hf, 128 hf + 128))
       const int j = r / c.group, jj = r - j * c.group;
       const bool rok = r < nrows;
+      constexpr int CPR = D / 8;  // 16-byte chunks of a row (Q' and the output)
       {
-        const __half* src = pv.qrot + ((long long)(q0 + tok0 + (rok ? j : 0)) * c.hq + h * c.group + (rok ? jj : 0)) * D;
+        // Q' rows of the item, consecutive threads on consecutive 16-byte
+        // chunks (the rows of one token's group are contiguous)
 #pragma unroll 4
-        for (int ch = 0; ch < D / 8; ch++) {
-          uint4 v = rok ? reinterpret_cast<const uint4*>(src)[ch] : make_uint4(0, 0, 0, 0);
-          if constexpr (FMT == kFmtInt4) {
-            // the tiles' nibble order: (q0, q4), (q1, q5), (q2, q6), (q3, q7)
-            v = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
-                           __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+        for (int u = tid; u < ROWS * CPR; u += 256) {
+          const int rr = u / CPR, ch = u - rr * CPR;
+          uint8_t* d = sQ + sw128(ROWS, rr, ch);
+          if (rr < nrows) {
+            const int tj = (int)c.gdiv.div((uint32_t)rr), tjj = rr - tj * c.group;
+            cp_async16(d, reinterpret_cast<const uint8_t*>(
+                              pv.qrot + ((long long)(q0 + tok0 + tj) * c.hq + h * c.group + tjj) * D) + ch * 16);
+          } else {
+            *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
           }
-          *reinterpret_cast<uint4*>(sQ + sw128(ROWS, r, ch)) = v;
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        if constexpr (FMT == kFmtInt4) {
+          // each thread reorders the chunks it copied into the tiles' nibble
+          // order: (q0, q4), (q1, q5), (q2, q6), (q3, q7)
+#pragma unroll 4
+          for (int u = tid; u < nrows * CPR; u += 256) {
+            const int rr = u / CPR, ch = u - rr * CPR;
+            uint4* pq = reinterpret_cast<uint4*>(sQ + sw128(ROWS, rr, ch));
+            const uint4 v = *pq;
+            *pq = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                             __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+          }
         }
       }
       fence_proxy_async_smem();  // Q' is read by the tensor cores
@@ -456,18 +484,28 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
       ws_wait(bar(ODONE), ph_odone, abort_flag, c.status);
       ph_odone ^= 1;
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / (l_run * (ROT ? (float)B : 1.f)) : 0.f;
-      uint16_t* dst = c.out + (long long)(q0 + tok0 + (rok ? j : 0)) * c.out_stride + (long long)(h * c.group + jj) * D;
-      // store 8 natural-order outputs y(i0 .. i0 + 7) (a row that saw no usable key, l = 0, as zeros)
-      auto store8 = [&](int col, const float (&y)[8]) {
-        float z[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++) z[e] = l_run > 0.f ? y[e] * inv * ssign[col + e] : 0.f;
-        *reinterpret_cast<uint4*>(dst + col) =
-            make_uint4(pack_bf16x2_rn(z[0], z[1]), pack_bf16x2_rn(z[2], z[3]), pack_bf16x2_rn(z[4], z[5]),
-                       pack_bf16x2_rn(z[6], z[7]));
+      const bool live = l_run > 0.f;  // a row that saw no usable key is written as zeros
+      const float inv = live ? 1.f / (l_run * (ROT ? (float)B : 1.f)) : 0.f;
+      // the output rows are staged as bf16 over the Q' and K tiles (every
+      // MMA of the item is complete) at a padded stride, then written out
+      // with consecutive threads on consecutive 16-byte chunks
+      constexpr int OSTR = 2 * D + 16;
+      static_assert(ROWS * OSTR <= G::QBYTES + G::KVBYTES, "output staging");
+      uint8_t* const orow = sQ + r * OSTR;
+      auto put8 = [&](int col, const float (&y)[8]) {
+        const float4 s0 = *reinterpret_cast<const float4*>(ssign + col);
+        const float4 s1 = *reinterpret_cast<const float4*>(ssign + col + 4);
+        const float2 iv = make_float2(inv, inv);
+        const float2 z0 = __fmul2_rn(__fmul2_rn(make_float2(y[0], y[1]), iv), make_float2(s0.x, s0.y));
+        const float2 z1 = __fmul2_rn(__fmul2_rn(make_float2(y[2], y[3]), iv), make_float2(s0.z, s0.w));
+        const float2 z2 = __fmul2_rn(__fmul2_rn(make_float2(y[4], y[5]), iv), make_float2(s1.x, s1.y));
+        const float2 z3 = __fmul2_rn(__fmul2_rn(make_float2(y[6], y[7]), iv), make_float2(s1.z, s1.w));
+        const uint4 w = make_uint4(pack_bf16x2_rn(z0.x, z0.y), pack_bf16x2_rn(z1.x, z1.y), pack_bf16x2_rn(z2.x, z2.y),
+                                   pack_bf16x2_rn(z3.x, z3.y));
+        *reinterpret_cast<uint4*>(orow + col * 2) = live ? w : make_uint4(0, 0, 0, 0);
       };
-      // TMEM column slot of natural element i within a chunk (INT4 columns are in nibble order)
+      // TMEM column slot of natural element i within a chunk: INT4 columns are
+      // in nibble order, so elements i and i + 4 (i % 8 < 4) sit in slots s, s + 1
       auto slot = [](int i) { return FMT == kFmtInt4 ? (i & ~7) + (i & 3) * 2 + ((i >> 2) & 1) : i; };
       constexpr int CHUNK = (ROT && B > 32) ? (B > 64 ? 64 : B) : 32;  // columns transformed in registers
 #pragma unroll 1
@@ -476,15 +514,30 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
 #pragma unroll
         for (int cc = 0; cc < CHUNK / 32; cc++) tmem_ld32(tO + base + cc * 32, *reinterpret_cast<float(*)[32]>(o + cc * 32));
         if constexpr (ROT) {
-          // H over each CHUNK-block (H_b itself when b <= 64)
+          // H over each CHUNK-block (H_b itself when b <= 64): the stride-4
+          // level pairs the two halves of a slot pair, every other level
+          // pairs slot pairs with packed f32x2 arithmetic
 #pragma unroll
           for (int hh = 1; hh < (B < CHUNK ? B : CHUNK); hh <<= 1) {
+            if (hh == 4) {
 #pragma unroll
-            for (int i = 0; i < CHUNK; i++) {
-              if ((i & hh) == 0) {
-                const float a0 = o[slot(i)], b0 = o[slot(i + hh)];
-                o[slot(i)] = a0 + b0;
-                o[slot(i + hh)] = a0 - b0;
+              for (int i = 0; i < CHUNK; i++) {
+                if ((i & 4) == 0) {
+                  const float a0 = o[slot(i)], b0 = o[slot(i + 4)];
+                  o[slot(i)] = a0 + b0;
+                  o[slot(i + 4)] = a0 - b0;
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < CHUNK; i++) {
+                if ((i & hh) == 0 && (i & 4) == 0) {
+                  const int sa = slot(i), sb = slot(i + hh);
+                  const float2 x = make_float2(o[sa], o[sa + 1]), y = make_float2(o[sb], o[sb + 1]);
+                  const float2 u = f2add(x, y), v = f2sub(x, y);
+                  o[sa] = u.x; o[sa + 1] = u.y;
+                  o[sb] = v.x; o[sb + 1] = v.y;
+                }
               }
             }
           }
@@ -496,13 +549,13 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
           for (int i = 0; i < CHUNK; i++) nat[i] = o[slot(i)];
 #pragma unroll
           for (int cc = 0; cc < CHUNK / 32; cc++) tmem_st32(tO + base + cc * 32, *reinterpret_cast<float(*)[32]>(nat + cc * 32));
-        } else if (rok) {
+        } else {
 #pragma unroll
           for (int i = 0; i < CHUNK; i += 8) {
             float y[8];
 #pragma unroll
             for (int e = 0; e < 8; e++) y[e] = o[slot(i + e)];
-            store8(base + i, y);
+            put8(base + i, y);
           }
         }
       }
@@ -516,21 +569,27 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
             float a[32], b2[32];
             tmem_ld32(tO + base + q, a);
             tmem_ld32(tO + base + 64 + q, b2);
-            if (rok) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 8) {
-                float y0[8], y1[8];
+            for (int i = 0; i < 32; i += 8) {
+              float y0[8], y1[8];
 #pragma unroll
-                for (int e = 0; e < 8; e++) {
-                  y0[e] = a[i + e] + b2[i + e];
-                  y1[e] = a[i + e] - b2[i + e];
-                }
-                store8(base + q + i, y0);
-                store8(base + 64 + q + i, y1);
+              for (int e = 0; e < 8; e++) {
+                y0[e] = a[i + e] + b2[i + e];
+                y1[e] = a[i + e] - b2[i + e];
               }
+              put8(base + q + i, y0);
+              put8(base + 64 + q + i, y1);
             }
           }
         }
+      }
+      softmax_sync();  // every row is staged
+#pragma unroll 4
+      for (int u = tid; u < nrows * CPR; u += 256) {
+        const int rr = u / CPR, ch = u - rr * CPR;
+        const int tj = (int)c.gdiv.div((uint32_t)rr), tjj = rr - tj * c.group;
+        *reinterpret_cast<uint4*>(c.out + (long long)(q0 + tok0 + tj) * c.out_stride + (long long)(h * c.group + tjj) * D +
+                                  ch * 8) = *reinterpret_cast<const uint4*>(sQ + rr * OSTR + ch * 16);
       }
     }
     // item end: every role is done with TMEM, the tiles and the ring
@@ -538,7 +597,7 @@ __global__ void __launch_bounds__(13 * 32, 1) prefill_ws_kernel(PreParams prm) {
     __syncthreads();
     tc_fence_after();
   }
-  if (warp == 12) {
+  if (warp == 15) {
     // after a time-out MMAs may still be in flight: they end by themselves
     // (they wait on nothing) and must end before the columns are freed
     if (lane == 0) umma_commit(bar(DRAIN));
