@@ -20,16 +20,19 @@
 // Hand-offs are mbarriers (every wait bounded; a wait that runs out sets
 // KV_INT4_DEV_TIMEOUT and a CTA-wide abort flag that ends every later
 // wait at once, so a fault in the pipeline costs one time-out, not one
-// per step):
-//   kfull  (dequant -> MMA)  K tile and the step's ring entry written
-//   vfull[b] (dequant -> MMA) V tile b written
-//   kfree  (MMA commit -> dequant) S0 and S1 of the step complete
+// per step).  Each comes in a pair, per K/V tile or per half, so that no
+// barrier can complete twice before its waiter has seen the first:
+//   kfull[b] (dequant -> MMA)  K tile b and the step's ring entry written
+//   vfull[b] (dequant -> MMA)  V tile b written
+//   kfree[b] (MMA commit -> dequant) S0 and S1 that read K tile b complete
 //   vfree[b] (MMA commit -> dequant) PV0 and PV1 that read V tile b complete
 //   sfull[h] (MMA commit -> softmax h) S_h complete (and every earlier MMA)
 //   pfull[h] (softmax h -> MMA) P_h in TMEM, O_h rescaled if it had to be
-//   odone  (MMA commit -> softmax) the item's last PV complete
-// The ring entry of step j is rewritten at step j + 2 only after kfree of
-// step j + 1, which follows both halves' P of step j.
+//   odone    (MMA commit -> softmax) the item's last PV complete
+// K has two tiles where shared memory allows (K of step j + 1 is
+// dequantised while S of step j runs), else one.  The ring of step
+// scales has three entries: the one of step j is rewritten at step j + 3,
+// after S of step j + 1 completed, which follows both halves' P of step j.
 
 constexpr int kWsRows = 256;  // query rows per item
 
@@ -45,9 +48,15 @@ struct WsGeom {
   static constexpr int FL_OFF = SC_OFF + 4 * 2 * 16 * 4;
   static constexpr int STG = (FL_OFF + 16 + 127) / 128 * 128;
   static constexpr int RING = 2 * NK * 4 + 32;        // K scales, V scales, 4 block flags, 2 votes
+  static constexpr int NRING = 3;                     // ring entries: step j's is rewritten at step j + 3
   static constexpr int TMEM_COLS = 128 + 2 * D <= 256 ? 256 : 512;
-  static constexpr int NBARS = 12;
-  static constexpr int USED = 1024 + QBYTES + 3 * KVBYTES + 2 * STG + 2 * RING + D * 4 + NBARS * 8 + 32;
+  static constexpr int NBARS = 14;
+  static constexpr int fixed_bytes(int kbuf) {
+    return 1024 + QBYTES + (kbuf + 2) * KVBYTES + 2 * STG + NRING * RING + D * 4 + NBARS * 8 + 32;
+  }
+  // two K tiles (dequantise K(j + 1) while S(j) runs) where shared memory allows
+  static constexpr int KBUF = fixed_bytes(2) <= 227 * 1024 ? 2 : 1;
+  static constexpr int USED = fixed_bytes(KBUF);
   static constexpr int SMEM = USED;
   static constexpr int THREADS = 16 * 32;
   static constexpr int DQ_WARPS = 7;  // warps 8 .. 14
@@ -71,6 +80,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 
+// per-thread register budget of the calling warpgroup (all four warps execute it)
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
+
 // named barrier over the dequant warps only
 __device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 1, 224;\n" ::: "memory"); }
 // named barrier over the softmax warps and the MMA warp: the item's Q' tile is written
@@ -92,11 +107,11 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* const sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* const sQ = sm;                     // [KB][256 rows][128 B], swizzled
-  uint8_t* const sK = sQ + G::QBYTES;         // [KB][64 keys][128 B]
-  uint8_t* const sV = sK + G::KVBYTES;        // two V tiles
+  uint8_t* const sK = sQ + G::QBYTES;         // KBUF K tiles [KB][64 keys][128 B]
+  uint8_t* const sV = sK + G::KBUF * G::KVBYTES;  // two V tiles
   uint8_t* const stg = sV + 2 * G::KVBYTES;   // two staging buffers
   uint8_t* const ring = stg + 2 * G::STG;     // two entries: K scales [64], V scales [64], flags [4], votes [2]
-  float* const ssign = reinterpret_cast<float*>(ring + 2 * G::RING);
+  float* const ssign = reinterpret_cast<float*>(ring + G::NRING * G::RING);
   uint64_t* const bars = reinterpret_cast<uint64_t*>(ssign + D);
   int* const sitem = reinterpret_cast<int*>(bars + G::NBARS);  // item [4], abort flag
   uint32_t* const tslot = reinterpret_cast<uint32_t*>(sitem + 6);
@@ -104,14 +119,18 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // barrier indices
-  enum { KFULL = 0, VFULL = 1, KFREE = 3, VFREE = 4, SFULL = 6, PFULL = 8, ODONE = 10, DRAIN = 11 };
+  // two of each pair: per K/V tile (full, free) or per half (S, P); every
+  // barrier is waited once per completion, in order
+  enum { KFULL = 0, VFULL = 2, KFREE = 4, VFREE = 6, SFULL = 8, PFULL = 10, ODONE = 12, DRAIN = 13 };
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
   for (int i = tid; i < D; i += G::THREADS) ssign[i] = (ROT && c.signs[i] < 0) ? -1.f : 1.f;
   if (tid == 0) {
     mbar_init(bar(KFULL), G::DQ_WARPS);
+    mbar_init(bar(KFULL + 1), G::DQ_WARPS);
     mbar_init(bar(VFULL), G::DQ_WARPS);
     mbar_init(bar(VFULL + 1), G::DQ_WARPS);
     mbar_init(bar(KFREE), 1);
+    mbar_init(bar(KFREE + 1), 1);
     mbar_init(bar(VFREE), 1);
     mbar_init(bar(VFREE + 1), 1);
     mbar_init(bar(SFULL), 1);
@@ -128,12 +147,21 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  // phase bits of the barriers each role waits on (one completion per wait)
-  uint32_t ph_kfull = 0, ph_vfull = 0, ph_kfree = 0, ph_vfree = 0, ph_sfull = 0, ph_pfull = 0, ph_odone = 0;
+  // registers: the launch gives 128 a thread to all four warpgroups (65,536);
+  // the softmax warpgroups take 168, the dequant/MMA ones keep 88
+  // (2 x 128 x 168 + 2 x 128 x 88 = 65,536: the increase can always be met)
   const int n_items = pv.plan[1], n_pseq = pv.plan[3];
-
+  // each role runs its own item loop (the same items, the same CTA-wide
+  // barriers), so that the register budget set for its warpgroups covers
+  // only its own code
+  static_assert(G::THREADS == 512, "four warpgroups");
+  if (warp < 8) {
+    // ======================= softmax warpgroups =======================
+    regs_inc<160>();
+    // phase bits of the barriers the role waits on (one completion per wait)
+    uint32_t ph_sfull = 0, ph_odone = 0;
 #pragma unroll 1
-  while (true) {
+    while (true) {
     if (tid == 0) {
       // next item: (prefill sequence, tile in descending order of work, kv head)
       const int itn = *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1);
@@ -154,7 +182,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
       }
       sitem[0] = it.x; sitem[1] = it.y; sitem[2] = it.z; sitem[3] = it.w;
     }
-    __syncthreads();
+      __syncthreads();
     const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
     if (item.x < 0) break;
     const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
@@ -165,179 +193,10 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
     const int nrows = ntok * c.group;
     const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
     const int nsteps = (nkb - kb0 + 3) / 4;
-
-    if (warp >= 8 && warp < 15) {
-      // ================= dequant warps =================
-      const int dt = tid - 256;
-      // staging is done by the first 128 dequant threads: thread (block b4,
-      // K/V, row) copies one code row and its scale; the block id of a step
-      // is loaded a step before its copies are issued
-      auto block_of = [&](int st) -> int {
-        const int kb = kb0 + st * 4 + (dt >> 5);
-        return (dt < 128 && kb < nkb) ? c.block_table[(long long)seq * c.max_blocks + kb] : -1;
-      };
-      auto issue = [&](int st, uint8_t* sb, int blk) {
-        if (dt >= 128) return;
-        const int b4 = dt >> 5, kv = (dt >> 4) & 1, row = dt & 15;
-        const int kb = kb0 + st * 4 + b4;
-        const bool ok = kb < nkb && blk >= 0 && blk < c.num_blocks;
-        if (ok) {
-          const uint8_t* src = (kv ? c.v_cache : c.k_cache) + (long long)blk * c.geo.cblk + row * c.geo.crow +
-                               (long long)h * c.geo.chead;
-          uint8_t* dst = sb + ((b4 * 2 + kv) * 16 + row) * G::CB;
-#pragma unroll
-          for (int col = 0; col < G::CB / 16; col++) cp_async16(dst + col * 16, src + col * 16);
-          cp_async4(sb + G::SC_OFF + ((b4 * 2 + kv) * 16 + row) * 4,
-                    (kv ? c.v_scale : c.k_scale) + (long long)blk * c.geo.sblk + row * c.geo.srow +
-                        (long long)h * c.geo.shead);
-        }
-        if (kv == 0 && row == 0) {
-          reinterpret_cast<int*>(sb + G::FL_OFF)[b4] = ok;
-          if (kb < nkb && !ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
-        }
-      };
-      // dequantise the K (kv = 0) or V (kv = 1) codes of staging sb into a tile
-      auto dequant = [&](const uint8_t* sb, uint8_t* tile_dst, int kv, int fmask) {
-        constexpr int CPK = D / 8;                        // 16-byte f16 chunks per key
-        constexpr int CBYTES = FMT == kFmtInt8 ? 8 : 4;   // code bytes of 8 elements
-#pragma unroll 4
-        for (int q = dt; q < NK * CPK; q += 32 * G::DQ_WARPS) {
-          const int k = q / CPK, ch = q - k * CPK;
-          const int b4 = k >> 4;
-          const uint8_t* src = sb + (b4 * 16 + k + kv * 16) * G::CB + ch * CBYTES;  // row (b4, kv, k & 15)
-          *reinterpret_cast<uint4*>(tile_dst + sw128(NK, k, ch)) = dequant8<FMT>(src, (fmask >> b4) & 1);
-        }
-      };
-      issue(0, stg, block_of(0));
-      cp_async_commit();
-      if (nsteps > 1) issue(1, stg + G::STG, block_of(1));
-      cp_async_commit();
-      int blk_next = block_of(2);
-#pragma unroll 1
-      for (int j = 0; j < nsteps; j++) {
-        const int b = j & 1;
-        uint8_t* const sb = stg + b * G::STG;
-        cp_async_wait<1>();
-        dq_sync();  // every thread's copies of step j have landed
-        if (j >= 1) {
-          ws_wait(bar(KFREE), ph_kfree, abort_flag, c.status);  // S of step j - 1 done: K tile and ring[b] free
-          ph_kfree ^= 1;
-        }
-        const int* sfl = reinterpret_cast<const int*>(sb + G::FL_OFF);
-        uint8_t* const re = ring + b * G::RING;
-        const int fmask = (sfl[0] != 0) | (sfl[1] != 0) << 1 | (sfl[2] != 0) << 2 | (sfl[3] != 0) << 3;
-        if (dt < NK) {
-          const float* scs = reinterpret_cast<const float*>(sb + G::SC_OFF);
-          const float vsc = scs[(dt >> 4) * 32 + 16 + (dt & 15)];
-          reinterpret_cast<float*>(re)[dt] = scs[(dt >> 4) * 32 + (dt & 15)];
-          reinterpret_cast<float*>(re)[NK + dt] = vsc;
-          // the vote reads only keys that exist (usable block, position below the
-          // sequence length): the threshold, and so the rounding, depend on the
-          // cache's contents alone
-          const bool exists = ((fmask >> (dt >> 4)) & 1) && (kb0 + j * 4) * 16 + dt < L;
-          const bool small = __all_sync(0xffffffffu, !exists || fabsf(vsc) < 128.f);
-          if (lane == 0) reinterpret_cast<int*>(re + 2 * NK * 4)[4 + (dt >> 5)] = small;
-        } else if (dt < NK + 4) {
-          reinterpret_cast<int*>(re + 2 * NK * 4)[dt - NK] = sfl[dt - NK];
-        }
-        dequant(sb, sK, 0, fmask);
-        fence_proxy_async_smem();  // the tile is read by the tensor cores
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KFULL));
-        if (j >= 2) {
-          ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);  // PVs of step j - 2 done
-          ph_vfree ^= 1u << b;
-        }
-        dequant(sb, sV + b * G::KVBYTES, 1, fmask);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(VFULL + b));
-        dq_sync();  // every thread is done with staging b
-        if (j + 2 < nsteps) issue(j + 2, sb, blk_next);
-        cp_async_commit();
-        blk_next = block_of(j + 3);
-      }
-      cp_async_wait<0>();
-      // the completions not waited for above: kfree of the last step, vfree of the last use of each V tile
-      if (nsteps >= 1) {
-        ws_wait(bar(KFREE), ph_kfree, abort_flag, c.status);
-        ph_kfree ^= 1;
-      }
-      for (int b = 0; b < 2 && b < nsteps; b++) {
-        ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
-        ph_vfree ^= 1u << b;
-      }
-    } else if (warp == 15) {
-      // ================= MMA warp (lane 0 issues, the warp waits together) =================
-      const bool leader = lane == 0;
-      const uint32_t qa = smem_addr(sQ), ka = smem_addr(sK), va = smem_addr(sV);
-      // S_h = Q_h K^T over the head dimension into TMEM columns [64h, 64h + 64)
-      auto issue_s = [&](int hh) {
-        if (leader) {
-#pragma unroll
-          for (int ks = 0; ks < KSTEPS; ks++)
-            umma_f16(tmem + 64 * hh,
-                     umma_desc(qa + (ks >> 2) * ROWS * 128 + hh * 128 * 128 + (ks & 3) * 32, 16, 1024),
-                     umma_desc(ka + (ks >> 2) * NK * 128 + (ks & 3) * 32, 16, 1024), IDESC_S, ks > 0);
-        }
-      };
-      // O_h += P_h V_b, P_h the f16 pairs over S_h's first 32 columns
-      auto issue_pv = [&](int hh, int b, bool first) {
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < 4; kk++)
-            umma_f16_ts(tmem + 128 + hh * D, tmem + 64 * hh + kk * 8,
-                        umma_desc(va + b * G::KVBYTES + kk * 2048, NK * 128, 1024), IDESC_O, !first || kk > 0);
-        }
-      };
-      auto commit = [&](int i) {
-        if (leader) umma_commit(bar(i));
-        __syncwarp();
-      };
-      q_sync();  // the softmax warps have written Q'
-      if (nsteps > 0) {
-        ws_wait(bar(KFULL), ph_kfull, abort_flag, c.status);
-        ph_kfull ^= 1;
-        tc_fence_after();
-        issue_s(0);
-        commit(SFULL);
-        issue_s(1);
-        commit(SFULL + 1);
-        commit(KFREE);
-      }
-#pragma unroll 1
-      for (int j = 0; j < nsteps; j++) {
-        const int b = j & 1;
-        ws_wait(bar(PFULL), ph_pfull & 1, abort_flag, c.status);
-        ph_pfull ^= 1;
-        ws_wait(bar(VFULL + b), (ph_vfull >> b) & 1, abort_flag, c.status);
-        ph_vfull ^= 1u << b;
-        tc_fence_after();
-        issue_pv(0, b, j == 0);
-        if (j + 1 < nsteps) {
-          ws_wait(bar(KFULL), ph_kfull, abort_flag, c.status);
-          ph_kfull ^= 1;
-          tc_fence_after();
-          issue_s(0);
-          commit(SFULL);
-        }
-        ws_wait(bar(PFULL + 1), (ph_pfull >> 1) & 1, abort_flag, c.status);
-        ph_pfull ^= 2;
-        tc_fence_after();
-        issue_pv(1, b, j == 0);
-        commit(VFREE + b);
-        if (j + 1 < nsteps) {
-          issue_s(1);
-          commit(SFULL + 1);
-          commit(KFREE);
-        }
-      }
-      commit(ODONE);
-    } else if (warp < 8) {
       // ================= softmax warps: half hf, one query row per thread =================
       const int hf = warp >> 2;
       const int r = tid;  // row of the item (half hf holds rows [128 hf, 128 hf + 128))
-      const int j = r / c.group, jj = r - j * c.group;
+      const int j = (int)c.gdiv.div((uint32_t)r);  // token of the row within the item
       const bool rok = r < nrows;
       constexpr int CPR = D / 8;  // 16-byte chunks of a row (Q' and the output)
       {
@@ -380,7 +239,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
       float m_ref = -INFINITY, l_run = 0.f;  // exponent reference of the row, sum of its weights
 #pragma unroll 1
       for (int st = 0; st < nsteps; st++) {
-        const uint8_t* re = ring + (st & 1) * G::RING;
+        const uint8_t* re = ring + (st % G::NRING) * G::RING;
         const float* sks = reinterpret_cast<const float*>(re);
         const float* svs = sks + NK;
         const int* sfl = reinterpret_cast<const int*>(re + 2 * NK * 4);
@@ -591,11 +450,216 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
         *reinterpret_cast<uint4*>(c.out + (long long)(q0 + tok0 + tj) * c.out_stride + (long long)(h * c.group + tjj) * D +
                                   ch * 8) = *reinterpret_cast<const uint4*>(sQ + rr * OSTR + ch * 16);
       }
-    }
     // item end: every role is done with TMEM, the tiles and the ring
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    }
+  } else {
+    // ==================== dequant and MMA warpgroups ====================
+    regs_dec<96>();
+    uint32_t ph_kfull = 0, ph_vfull = 0, ph_kfree = 0, ph_vfree = 0, ph_pfull = 0;
+#pragma unroll 1
+    while (true) {
+      __syncthreads();
+    const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
+    if (item.x < 0) break;
+    const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
+    const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+    const int L = c.seq_lens[seq], ctx = L - ql;
+    const int tok0 = tile * c.tile_tokens;
+    const int ntok = min(c.tile_tokens, ql - tok0);
+    const int nrows = ntok * c.group;
+    const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
+    const int nsteps = (nkb - kb0 + 3) / 4;
+      (void)nrows;
+      if (warp < 15) {
+      // ================= dequant warps =================
+      const int dt = tid - 256;
+      // staging is done by the first 128 dequant threads: thread (block b4,
+      // K/V, row) copies one code row and its scale; the block id of a step
+      // is loaded a step before its copies are issued
+      auto block_of = [&](int st) -> int {
+        const int kb = kb0 + st * 4 + (dt >> 5);
+        return (dt < 128 && kb < nkb) ? c.block_table[(long long)seq * c.max_blocks + kb] : -1;
+      };
+      auto issue = [&](int st, uint8_t* sb, int blk) {
+        if (dt >= 128) return;
+        const int b4 = dt >> 5, kv = (dt >> 4) & 1, row = dt & 15;
+        const int kb = kb0 + st * 4 + b4;
+        const bool ok = kb < nkb && blk >= 0 && blk < c.num_blocks;
+        if (ok) {
+          const uint8_t* src = (kv ? c.v_cache : c.k_cache) + (long long)blk * c.geo.cblk + row * c.geo.crow +
+                               (long long)h * c.geo.chead;
+          uint8_t* dst = sb + ((b4 * 2 + kv) * 16 + row) * G::CB;
+#pragma unroll
+          for (int col = 0; col < G::CB / 16; col++) cp_async16(dst + col * 16, src + col * 16);
+          cp_async4(sb + G::SC_OFF + ((b4 * 2 + kv) * 16 + row) * 4,
+                    (kv ? c.v_scale : c.k_scale) + (long long)blk * c.geo.sblk + row * c.geo.srow +
+                        (long long)h * c.geo.shead);
+        }
+        if (kv == 0 && row == 0) {
+          reinterpret_cast<int*>(sb + G::FL_OFF)[b4] = ok;
+          if (kb < nkb && !ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
+        }
+      };
+      // dequantise the K (kv = 0) or V (kv = 1) codes of staging sb into a tile
+      auto dequant = [&](const uint8_t* sb, uint8_t* tile_dst, int kv, int fmask) {
+        constexpr int CPK = D / 8;                        // 16-byte f16 chunks per key
+        constexpr int CBYTES = FMT == kFmtInt8 ? 8 : 4;   // code bytes of 8 elements
+#pragma unroll 4
+        for (int q = dt; q < NK * CPK; q += 32 * G::DQ_WARPS) {
+          const int k = q / CPK, ch = q - k * CPK;
+          const int b4 = k >> 4;
+          const uint8_t* src = sb + (b4 * 16 + k + kv * 16) * G::CB + ch * CBYTES;  // row (b4, kv, k & 15)
+          *reinterpret_cast<uint4*>(tile_dst + sw128(NK, k, ch)) = dequant8<FMT>(src, (fmask >> b4) & 1);
+        }
+      };
+      issue(0, stg, block_of(0));
+      cp_async_commit();
+      if (nsteps > 1) issue(1, stg + G::STG, block_of(1));
+      cp_async_commit();
+      int blk_next = block_of(2);
+#pragma unroll 1
+      for (int j = 0; j < nsteps; j++) {
+        const int b = j & 1;
+        uint8_t* const sb = stg + b * G::STG;
+        cp_async_wait<1>();
+        dq_sync();  // every thread's copies of step j have landed
+        // the K tile of step j is free once S of step j - KBUF is complete;
+        // the ring entry of step j once the softmax of step j - 3 is (S of
+        // step j - 2 follows both halves' P of step j - 3)
+        if (j >= G::KBUF) {
+          const int fb = (j - G::KBUF) & 1;
+          ws_wait(bar(KFREE + fb), (ph_kfree >> fb) & 1, abort_flag, c.status);
+          ph_kfree ^= 1u << fb;
+        }
+        const int* sfl = reinterpret_cast<const int*>(sb + G::FL_OFF);
+        uint8_t* const re = ring + (j % G::NRING) * G::RING;
+        const int fmask = (sfl[0] != 0) | (sfl[1] != 0) << 1 | (sfl[2] != 0) << 2 | (sfl[3] != 0) << 3;
+        if (dt < NK) {
+          const float* scs = reinterpret_cast<const float*>(sb + G::SC_OFF);
+          const float vsc = scs[(dt >> 4) * 32 + 16 + (dt & 15)];
+          reinterpret_cast<float*>(re)[dt] = scs[(dt >> 4) * 32 + (dt & 15)];
+          reinterpret_cast<float*>(re)[NK + dt] = vsc;
+          // the vote reads only keys that exist (usable block, position below the
+          // sequence length): the threshold, and so the rounding, depend on the
+          // cache's contents alone
+          const bool exists = ((fmask >> (dt >> 4)) & 1) && (kb0 + j * 4) * 16 + dt < L;
+          const bool small = __all_sync(0xffffffffu, !exists || fabsf(vsc) < 128.f);
+          if (lane == 0) reinterpret_cast<int*>(re + 2 * NK * 4)[4 + (dt >> 5)] = small;
+        } else if (dt < NK + 4) {
+          reinterpret_cast<int*>(re + 2 * NK * 4)[dt - NK] = sfl[dt - NK];
+        }
+        dequant(sb, sK + (G::KBUF == 2 ? b : 0) * G::KVBYTES, 0, fmask);
+        fence_proxy_async_smem();  // the tile is read by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KFULL + b));
+        if (j >= 2) {
+          ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);  // PVs of step j - 2 done
+          ph_vfree ^= 1u << b;
+        }
+        dequant(sb, sV + b * G::KVBYTES, 1, fmask);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(VFULL + b));
+        dq_sync();  // every thread is done with staging b
+        if (j + 2 < nsteps) issue(j + 2, sb, blk_next);
+        cp_async_commit();
+        blk_next = block_of(j + 3);
+      }
+      cp_async_wait<0>();
+      // the completions not waited for above: kfree of the last step, vfree of the last use of each V tile
+      for (int st = nsteps - G::KBUF < 0 ? 0 : nsteps - G::KBUF; st < nsteps; st++) {
+        ws_wait(bar(KFREE + (st & 1)), (ph_kfree >> (st & 1)) & 1, abort_flag, c.status);
+        ph_kfree ^= 1u << (st & 1);
+      }
+      for (int b = 0; b < 2 && b < nsteps; b++) {
+        ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
+        ph_vfree ^= 1u << b;
+      }
+      } else {
+      // ================= MMA warp (lane 0 issues, the warp waits together) =================
+      const bool leader = lane == 0;
+      // operand descriptors: the start address is the low 14-bit field of
+      // (address >> 4), so an offset below 256 KB adds to the descriptor
+      const uint64_t dq = umma_desc(smem_addr(sQ), 16, 1024);
+      const uint64_t dk = umma_desc(smem_addr(sK), 16, 1024);
+      const uint64_t dv = umma_desc(smem_addr(sV), NK * 128, 1024);
+      // S_h = Q_h K^T over the head dimension into TMEM columns [64h, 64h + 64)
+      auto issue_s = [&](int hh, int st) {
+        if (leader) {
+          const uint64_t kt = dk + (uint64_t)((G::KBUF == 2 ? (st & 1) : 0) * (G::KVBYTES >> 4));
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ks++)
+            umma_f16(tmem + 64 * hh, dq + (uint64_t)(((ks >> 2) * ROWS * 128 + hh * 128 * 128 + (ks & 3) * 32) >> 4),
+                     kt + (uint64_t)(((ks >> 2) * NK * 128 + (ks & 3) * 32) >> 4), IDESC_S, ks > 0);
+        }
+      };
+      // O_h += P_h V_b, P_h the f16 pairs over S_h's first 32 columns
+      auto issue_pv = [&](int hh, int b, bool first) {
+        if (leader) {
+          const uint64_t vt = dv + (uint64_t)(b * (G::KVBYTES >> 4));
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++)
+            umma_f16_ts(tmem + 128 + hh * D, tmem + 64 * hh + kk * 8, vt + (uint64_t)(kk * (2048 >> 4)), IDESC_O,
+                        !first || kk > 0);
+        }
+      };
+      auto commit = [&](int i) {
+        if (leader) umma_commit(bar(i));
+        __syncwarp();
+      };
+      q_sync();  // the softmax warps have written Q'
+      if (nsteps > 0) {
+        ws_wait(bar(KFULL), ph_kfull & 1, abort_flag, c.status);
+        ph_kfull ^= 1;
+        tc_fence_after();
+        issue_s(0, 0);
+        commit(SFULL);
+        issue_s(1, 0);
+        commit(SFULL + 1);
+        commit(KFREE);
+      }
+#pragma unroll 1
+      for (int j = 0; j < nsteps; j++) {
+        const int b = j & 1, nb = (j + 1) & 1;
+        // V of this step and K of the next are normally ready long before
+        // P: wait for them first, so that PV and the next S issue as soon
+        // as the half's P lands (neither waits on anything this warp issues
+        // later: V(j) follows PV(j - 2), K(j + 1) follows S(j + 1 - KBUF))
+        ws_wait(bar(VFULL + b), (ph_vfull >> b) & 1, abort_flag, c.status);
+        ph_vfull ^= 1u << b;
+        if (j + 1 < nsteps) {
+          ws_wait(bar(KFULL + nb), (ph_kfull >> nb) & 1, abort_flag, c.status);
+          ph_kfull ^= 1u << nb;
+        }
+        ws_wait(bar(PFULL), ph_pfull & 1, abort_flag, c.status);
+        ph_pfull ^= 1;
+        tc_fence_after();
+        issue_pv(0, b, j == 0);
+        if (j + 1 < nsteps) {
+          issue_s(0, j + 1);
+          commit(SFULL);
+        }
+        ws_wait(bar(PFULL + 1), (ph_pfull >> 1) & 1, abort_flag, c.status);
+        ph_pfull ^= 2;
+        tc_fence_after();
+        issue_pv(1, b, j == 0);
+        commit(VFREE + b);
+        if (j + 1 < nsteps) {
+          issue_s(1, j + 1);
+          commit(SFULL + 1);
+          commit(KFREE + nb);
+        }
+      }
+      commit(ODONE);
+      }
+    // item end: every role is done with TMEM, the tiles and the ring
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    }
   }
   if (warp == 15) {
     // after a time-out MMAs may still be in flight: they end by themselves
