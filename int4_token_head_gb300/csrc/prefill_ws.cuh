@@ -44,7 +44,11 @@ struct WsGeom {
   static constexpr int QBYTES = ROWS * 128 * KB;
   static constexpr int KVBYTES = NK * 128 * KB;       // one K or V tile
   static constexpr int CB = FMT == kFmtInt8 ? D : D / 2;
-  static constexpr int SC_OFF = 4 * 2 * 16 * CB;      // staging: codes [block][K/V][16][CB], scales, flags
+  // staging: code rows [block][K/V][16] at a stride of an odd number of
+  // 16-byte units (eight consecutive rows hit eight bank groups), then
+  // scales, then flags
+  static constexpr int SROW = CB + ((CB / 16) % 2 == 0 ? 16 : 0);
+  static constexpr int SC_OFF = 4 * 2 * 16 * SROW;
   static constexpr int FL_OFF = SC_OFF + 4 * 2 * 16 * 4;
   static constexpr int STG = (FL_OFF + 16 + 127) / 128 * 128;
   static constexpr int RING = 2 * NK * 4 + 32;        // K scales, V scales, 4 block flags, 2 votes
@@ -78,6 +82,39 @@ __device__ __forceinline__ bool ws_wait(uint32_t bar, uint32_t parity, volatile 
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// 8 exact f16 values of one 32-bit word of INT4 codes, in nibble order
+// (elements 0,4,1,5,2,6,3,7): the low nibbles of bytes (0, 2) become
+// 1032 + c exactly (minus 1032), the high ones 1152 + 16c (/ 16 - 72 in one
+// rounding of an exact value)
+__device__ __forceinline__ uint4 dq_word_int4(uint32_t x) {
+  const uint32_t y = x >> 8;
+  const uint32_t n1032 = kF16x2_M1032, h16 = 0x2c002c00u, m72 = 0xd480d480u;  // (-1032), (1/16), (-72)
+  const __half2 m1032 = *reinterpret_cast<const __half2*>(&n1032);
+  const __half2 inv16 = *reinterpret_cast<const __half2*>(&h16), n72 = *reinterpret_cast<const __half2*>(&m72);
+  uint32_t a = nib_lo(x), b = nib_hi(x), e = nib_lo(y), f = nib_hi(y);
+  __half2 ha = __hadd2(*reinterpret_cast<__half2*>(&a), m1032);
+  __half2 hb = __hfma2(*reinterpret_cast<__half2*>(&b), inv16, n72);
+  __half2 he = __hadd2(*reinterpret_cast<__half2*>(&e), m1032);
+  __half2 hf = __hfma2(*reinterpret_cast<__half2*>(&f), inv16, n72);
+  return make_uint4(*reinterpret_cast<uint32_t*>(&ha), *reinterpret_cast<uint32_t*>(&hb),
+                    *reinterpret_cast<uint32_t*>(&he), *reinterpret_cast<uint32_t*>(&hf));
+}
+// 8 exact f16 values of two words of int8 codes, natural order: the byte
+// c + 128 paired with 0x64 is 1024 + (c + 128); minus 1152
+__device__ __forceinline__ uint4 dq_pair_int8(uint32_t wx, uint32_t wy) {
+  const uint32_t a = wx ^ 0x80808080u, b = wy ^ 0x80808080u, m1152 = kF16x2_M1152;
+  const __half2 off = *reinterpret_cast<const __half2*>(&m1152);
+  uint32_t h[4] = {__byte_perm(a, kBytes64, 0x4140), __byte_perm(a, kBytes64, 0x4342), __byte_perm(b, kBytes64, 0x4140),
+                   __byte_perm(b, kBytes64, 0x4342)};
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    __half2 v = __hadd2(*reinterpret_cast<__half2*>(&h[i]), off);
+    r[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 // per-thread register budget of the calling warpgroup (all four warps execute it)
@@ -270,8 +307,8 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
             const float2 a = __fmul2_rn(make_float2(sv[k], sv[k + 1]), make_float2(f.x, f.y));
             const float2 bb = __fmul2_rn(make_float2(sv[k + 2], sv[k + 3]), make_float2(f.z, f.w));
             sv[k] = a.x; sv[k + 1] = a.y; sv[k + 2] = bb.x; sv[k + 3] = bb.y;
-            mx4[0] = fmaxf(mx4[0], a.x); mx4[1] = fmaxf(mx4[1], a.y);
-            mx4[2] = fmaxf(mx4[2], bb.x); mx4[3] = fmaxf(mx4[3], bb.y);
+            mx4[(k >> 2) & 1] = fmax3(mx4[(k >> 2) & 1], a.x, a.y);
+            mx4[2 + ((k >> 2) & 1)] = fmax3(mx4[2 + ((k >> 2) & 1)], bb.x, bb.y);
           }
         } else {
 #pragma unroll
@@ -302,6 +339,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
         l_run *= alpha;
         float pf[NK / 2];  // P' as f16 pairs (bit patterns)
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         const float4* vs4 = reinterpret_cast<const float4*>(svs);
         if (full) {
           const float2 nm = make_float2(-m_ref, -m_ref);
@@ -312,7 +350,8 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
             const float2 db = __fadd2_rn(make_float2(sv[k + 2], sv[k + 3]), nm);
             const float2 pa = make_float2(fast_exp2(da.x), fast_exp2(da.y));
             const float2 pb = make_float2(fast_exp2(db.x), fast_exp2(db.y));
-            ps[0] += pa.x; ps[1] += pa.y; ps[2] += pb.x; ps[3] += pb.y;
+            ps2[0] = f2add(ps2[0], pa);
+            ps2[1] = f2add(ps2[1], pb);
             const float2 wa = __fmul2_rn(pa, make_float2(f.x, f.y));
             const float2 wb = __fmul2_rn(pb, make_float2(f.z, f.w));
             pf[k / 2] = __uint_as_float(pack_f16x2(wa.x, wa.y));
@@ -332,7 +371,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
             pf[k / 2] = __uint_as_float(pack_f16x2(w0, w1));
           }
         }
-        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps2[0].x + ps2[0].y) + (ps2[1].x + ps2[1].y));
         tmem_st32(tS, pf);  // P' over the row's first 32 S columns (S is consumed)
         tc_fence_before();
         __syncwarp();
@@ -491,7 +530,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
         if (ok) {
           const uint8_t* src = (kv ? c.v_cache : c.k_cache) + (long long)blk * c.geo.cblk + row * c.geo.crow +
                                (long long)h * c.geo.chead;
-          uint8_t* dst = sb + ((b4 * 2 + kv) * 16 + row) * G::CB;
+          uint8_t* dst = sb + ((b4 * 2 + kv) * 16 + row) * G::SROW;
 #pragma unroll
           for (int col = 0; col < G::CB / 16; col++) cp_async16(dst + col * 16, src + col * 16);
           cp_async4(sb + G::SC_OFF + ((b4 * 2 + kv) * 16 + row) * 4,
@@ -503,16 +542,29 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
           if (kb < nkb && !ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
         }
       };
-      // dequantise the K (kv = 0) or V (kv = 1) codes of staging sb into a tile
+      // dequantise the K (kv = 0) or V (kv = 1) codes of staging sb into a
+      // tile: a thread takes 16 code bytes (one shared load) of one key;
+      // consecutive threads take consecutive keys, so that the eight keys
+      // of a store phase cover the eight swizzled 16-byte positions
       auto dequant = [&](const uint8_t* sb, uint8_t* tile_dst, int kv, int fmask) {
-        constexpr int CPK = D / 8;                        // 16-byte f16 chunks per key
-        constexpr int CBYTES = FMT == kFmtInt8 ? 8 : 4;   // code bytes of 8 elements
-#pragma unroll 4
-        for (int q = dt; q < NK * CPK; q += 32 * G::DQ_WARPS) {
-          const int k = q / CPK, ch = q - k * CPK;
-          const int b4 = k >> 4;
-          const uint8_t* src = sb + (b4 * 16 + k + kv * 16) * G::CB + ch * CBYTES;  // row (b4, kv, k & 15)
-          *reinterpret_cast<uint4*>(tile_dst + sw128(NK, k, ch)) = dequant8<FMT>(src, (fmask >> b4) & 1);
+        constexpr int UC = FMT == kFmtInt8 ? 2 : 4;  // 8-element chunks per 16 code bytes
+        constexpr int UPK = D / 8 / UC;              // 16-byte code units per key
+#pragma unroll 2
+        for (int q = dt; q < NK * UPK; q += 32 * G::DQ_WARPS) {
+          const int k = q & (NK - 1), g = q >> 6;
+          const int b4 = k >> 4, x7 = k & 7;
+          uint4 w = *reinterpret_cast<const uint4*>(sb + (k + (b4 + kv) * 16) * G::SROW + g * 16);
+          if (!((fmask >> b4) & 1)) w = make_uint4(0, 0, 0, 0);  // code 0 in both formats
+          uint8_t* const dst = tile_dst + (((g * UC) >> 3) * NK + k) * 128;
+          if constexpr (FMT == kFmtInt4) {
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+              *reinterpret_cast<uint4*>(dst + ((((g * 4 + i) & 7) ^ x7) << 4)) = dq_word_int4(wv[i]);
+          } else {
+            *reinterpret_cast<uint4*>(dst + ((((g * 2) & 7) ^ x7) << 4)) = dq_pair_int8(w.x, w.y);
+            *reinterpret_cast<uint4*>(dst + ((((g * 2 + 1) & 7) ^ x7) << 4)) = dq_pair_int8(w.z, w.w);
+          }
         }
       };
       issue(0, stg, block_of(0));
