@@ -324,8 +324,8 @@ def window_bench(pk, q, out, window: int, iters: int):
 
 
 def prefill_kernel_name(d: int) -> str:
-    """Head sizes up to 192 take the tensor-core (tcgen05) prefill, 256 the mma.sync one."""
-    return "prefill_tc_kernel" if d <= 192 else "prefill_kernel"
+    """Head sizes up to 192 take the warp-specialised tcgen05 prefill, 256 the mma.sync one."""
+    return "prefill_ws_kernel" if d <= 192 else "prefill_kernel"
 
 
 def int8_decode_bench(w, dev, iters: int):

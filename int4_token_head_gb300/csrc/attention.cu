@@ -1219,7 +1219,6 @@ __global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PrePa
   }
 }
 
-#include "prefill_tc.cuh"
 #include "prefill_ws.cuh"
 
 // ---------------------------------------------------------------------------

@@ -1,22 +1,42 @@
-// Warp-specialised prefill on the tcgen05 tensor cores, included by
-// attention.cu after prefill_tc.cuh (whose tile helpers it shares).
+// Warp-specialised prefill on the 5th-generation tensor cores (tcgen05),
+// included by attention.cu after the schedule and parameter types it uses.
 //
 // One CTA per SM (all 512 TMEM columns), one item = 256 query rows
-// (query token x q head of one kv group) in two halves of 128, the MMA's M.
-// Sixteen warps in three roles, 64 keys (four cache blocks) per step:
-//   * dequant warps (8-14): stage the step's codes and scales with
-//     cp.async (two staging buffers), dequantise K into one f16 tile and V
-//     into one of two (exact, as in the single-CTA kernel), and copy the
-//     step's K/V scales and block flags into a two-entry ring;
-//   * MMA warp (15, one lane issues): S_h = Q_h K^T into TMEM columns
+// (query token x q head of one kv group) in two halves of 128, the MMA's M;
+// 64 keys (four cache blocks) per step.  Sixteen warps in three roles, each
+// role running its own item loop so that a register budget can be set per
+// warpgroup (softmax 160 a thread, the others 96):
+//   * dequant warps (8-14): stage the step's code rows and scales with
+//     cp.async into one of two staging buffers (block ids loaded a step
+//     ahead), dequantise K into one of two f16 tiles (one where shared
+//     memory is short) and V into one of two, exactly (an INT4 nibble u
+//     becomes the f16 pattern 0x6400 | u = 1024 + u, an int8 byte u the
+//     pattern 0x64uu), and copy the step's K/V scales, block flags and the
+//     V-scale vote into a three-entry ring;
+//   * MMA warp (15, lane 0 issues): S_h = Q_h K^T into TMEM columns
 //     [64h, 64h + 64); O_h += P_h V with P_h read from TMEM (the A operand
 //     of the MMA may live in tensor memory) into columns
 //     [128 + hD, 128 + (h+1)D).  Issue order S0 S1 | PV0 S0' | PV1 S1' | ...
 //     lets each half's softmax run while the other half's MMAs do;
 //   * softmax warps (0-3 for half 0, 4-7 for half 1): one query row per
-//     thread, the same masked base-2 online softmax with the lazy exponent
-//     reference as the single-CTA kernel, P' = p * v_scale written back as
-//     f16 pairs over the row's S columns; then the epilogue.
+//     thread, a masked base-2 online softmax whose exponent reference m_ref
+//     moves (and the row's O in TMEM is rescaled) only when the row max
+//     passes m_ref + tau: tau = 8 while every V scale of the step's
+//     existing keys is below 128, so p <= 2^8 keeps P' below 2^15 in f16,
+//     else tau = 0 (the exact running max); P' = p * v_scale is written back
+//     as f16 pairs over the row's S columns.  The epilogue normalises O,
+//     applies D (I_n (x) H_b) (.) / b in registers (packed f32x2 butterflies)
+//     and stages the bf16 rows over the Q' and K tiles for coalesced stores.
+// INT4 tiles keep each 8-element group in nibble order (elements 0,4,1,5,
+// 2,6,3,7: the two nibble lanes of a 32-bit word per f16x2, no byte
+// shuffles); Q' is stored with the same permutation, which leaves Q' K^T
+// unchanged, and the epilogue undoes it on O (its columns are V's dims) by
+// register renaming.
+// Shared-memory operands: K-major tiles are [D/64 blocks][rows][128 bytes]
+// with the 16-byte chunk index XORed by row % 8 (1024-byte atoms; leading
+// byte offset unused, stride byte offset 1024); the V tiles use the same
+// layout as MN-major operands (dims are the MMA's N: leading byte offset =
+// one 64-dim block = 64 keys x 128 bytes, stride byte offset = 8 keys).
 // Hand-offs are mbarriers (every wait bounded; a wait that runs out sets
 // KV_INT4_DEV_TIMEOUT and a CTA-wide abort flag that ends every later
 // wait at once, so a fault in the pipeline costs one time-out, not one
@@ -29,12 +49,17 @@
 //   sfull[h] (MMA commit -> softmax h) S_h complete (and every earlier MMA)
 //   pfull[h] (softmax h -> MMA) P_h in TMEM, O_h rescaled if it had to be
 //   odone    (MMA commit -> softmax) the item's last PV complete
-// K has two tiles where shared memory allows (K of step j + 1 is
-// dequantised while S of step j runs), else one.  The ring of step
-// scales has three entries: the one of step j is rewritten at step j + 3,
-// after S of step j + 1 completed, which follows both halves' P of step j.
+// The ring entry of step j is rewritten at step j + 3, after S of step
+// j + 1 completed, which follows both halves' P of step j.
 
 constexpr int kWsRows = 256;  // query rows per item
+
+// byte offset of 16-byte chunk c (elements 8c .. 8c+7) of row r in a
+// 128-byte-swizzled K-major tile of `rows` rows: [c / 8][rows][128 bytes],
+// the chunk index within a 128-byte row XORed by r % 8
+__device__ __forceinline__ uint32_t sw128(int rows, int r, int c) {
+  return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
 
 template <int D, int FMT>
 struct WsGeom {
@@ -199,37 +224,37 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
     uint32_t ph_sfull = 0, ph_odone = 0;
 #pragma unroll 1
     while (true) {
-    if (tid == 0) {
-      // next item: (prefill sequence, tile in descending order of work, kv head)
-      const int itn = *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1);
-      int4 it = make_int4(-1, 0, 0, 0);
-      if (itn < n_items) {
-        int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (pv.ptab[mid].y <= itn) lo = mid;
-          else hi = mid;
+      if (tid == 0) {
+        // next item: (prefill sequence, tile in descending order of work, kv head)
+        const int itn = *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1);
+        int4 it = make_int4(-1, 0, 0, 0);
+        if (itn < n_items) {
+          int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pv.ptab[mid].y <= itn) lo = mid;
+            else hi = mid;
+          }
+          const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
+          const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
+          const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
+          const int t = ntiles - 1 - r / c.hkv;
+          const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
+          it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
         }
-        const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
-        const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
-        const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
-        const int t = ntiles - 1 - r / c.hkv;
-        const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
-        it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
+        sitem[0] = it.x; sitem[1] = it.y; sitem[2] = it.z; sitem[3] = it.w;
       }
-      sitem[0] = it.x; sitem[1] = it.y; sitem[2] = it.z; sitem[3] = it.w;
-    }
       __syncthreads();
-    const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
-    if (item.x < 0) break;
-    const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
-    const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
-    const int L = c.seq_lens[seq], ctx = L - ql;
-    const int tok0 = tile * c.tile_tokens;
-    const int ntok = min(c.tile_tokens, ql - tok0);
-    const int nrows = ntok * c.group;
-    const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
-    const int nsteps = (nkb - kb0 + 3) / 4;
+      const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
+      if (item.x < 0) break;
+      const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
+      const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+      const int L = c.seq_lens[seq], ctx = L - ql;
+      const int tok0 = tile * c.tile_tokens;
+      const int ntok = min(c.tile_tokens, ql - tok0);
+      const int nrows = ntok * c.group;
+      const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
+      const int nsteps = (nkb - kb0 + 3) / 4;
       // ================= softmax warps: half hf, one query row per thread =================
       const int hf = warp >> 2;
       const int r = tid;  // row of the item (half hf holds rows [128 hf, 128 hf + 128))
@@ -489,10 +514,10 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
         *reinterpret_cast<uint4*>(c.out + (long long)(q0 + tok0 + tj) * c.out_stride + (long long)(h * c.group + tjj) * D +
                                   ch * 8) = *reinterpret_cast<const uint4*>(sQ + rr * OSTR + ch * 16);
       }
-    // item end: every role is done with TMEM, the tiles and the ring
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+      // item end: every role is done with TMEM, the tiles and the ring
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
     }
   } else {
     // ==================== dequant and MMA warpgroups ====================
@@ -501,216 +526,216 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
 #pragma unroll 1
     while (true) {
       __syncthreads();
-    const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
-    if (item.x < 0) break;
-    const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
-    const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
-    const int L = c.seq_lens[seq], ctx = L - ql;
-    const int tok0 = tile * c.tile_tokens;
-    const int ntok = min(c.tile_tokens, ql - tok0);
-    const int nrows = ntok * c.group;
-    const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
-    const int nsteps = (nkb - kb0 + 3) / 4;
+      const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
+      if (item.x < 0) break;
+      const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
+      const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+      const int L = c.seq_lens[seq], ctx = L - ql;
+      const int tok0 = tile * c.tile_tokens;
+      const int ntok = min(c.tile_tokens, ql - tok0);
+      const int nrows = ntok * c.group;
+      const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
+      const int nsteps = (nkb - kb0 + 3) / 4;
       (void)nrows;
       if (warp < 15) {
-      // ================= dequant warps =================
-      const int dt = tid - 256;
-      // staging is done by the first 128 dequant threads: thread (block b4,
-      // K/V, row) copies one code row and its scale; the block id of a step
-      // is loaded a step before its copies are issued
-      auto block_of = [&](int st) -> int {
-        const int kb = kb0 + st * 4 + (dt >> 5);
-        return (dt < 128 && kb < nkb) ? c.block_table[(long long)seq * c.max_blocks + kb] : -1;
-      };
-      auto issue = [&](int st, uint8_t* sb, int blk) {
-        if (dt >= 128) return;
-        const int b4 = dt >> 5, kv = (dt >> 4) & 1, row = dt & 15;
-        const int kb = kb0 + st * 4 + b4;
-        const bool ok = kb < nkb && blk >= 0 && blk < c.num_blocks;
-        if (ok) {
-          const uint8_t* src = (kv ? c.v_cache : c.k_cache) + (long long)blk * c.geo.cblk + row * c.geo.crow +
-                               (long long)h * c.geo.chead;
-          uint8_t* dst = sb + ((b4 * 2 + kv) * 16 + row) * G::SROW;
+        // ================= dequant warps =================
+        const int dt = tid - 256;
+        // staging is done by the first 128 dequant threads: thread (block b4,
+        // K/V, row) copies one code row and its scale; the block id of a step
+        // is loaded a step before its copies are issued
+        auto block_of = [&](int st) -> int {
+          const int kb = kb0 + st * 4 + (dt >> 5);
+          return (dt < 128 && kb < nkb) ? c.block_table[(long long)seq * c.max_blocks + kb] : -1;
+        };
+        auto issue = [&](int st, uint8_t* sb, int blk) {
+          if (dt >= 128) return;
+          const int b4 = dt >> 5, kv = (dt >> 4) & 1, row = dt & 15;
+          const int kb = kb0 + st * 4 + b4;
+          const bool ok = kb < nkb && blk >= 0 && blk < c.num_blocks;
+          if (ok) {
+            const uint8_t* src = (kv ? c.v_cache : c.k_cache) + (long long)blk * c.geo.cblk + row * c.geo.crow +
+                                 (long long)h * c.geo.chead;
+            uint8_t* dst = sb + ((b4 * 2 + kv) * 16 + row) * G::SROW;
 #pragma unroll
-          for (int col = 0; col < G::CB / 16; col++) cp_async16(dst + col * 16, src + col * 16);
-          cp_async4(sb + G::SC_OFF + ((b4 * 2 + kv) * 16 + row) * 4,
-                    (kv ? c.v_scale : c.k_scale) + (long long)blk * c.geo.sblk + row * c.geo.srow +
-                        (long long)h * c.geo.shead);
-        }
-        if (kv == 0 && row == 0) {
-          reinterpret_cast<int*>(sb + G::FL_OFF)[b4] = ok;
-          if (kb < nkb && !ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
-        }
-      };
-      // dequantise the K (kv = 0) or V (kv = 1) codes of staging sb into a
-      // tile: a thread takes 16 code bytes (one shared load) of one key;
-      // consecutive threads take consecutive keys, so that the eight keys
-      // of a store phase cover the eight swizzled 16-byte positions
-      auto dequant = [&](const uint8_t* sb, uint8_t* tile_dst, int kv, int fmask) {
-        constexpr int UC = FMT == kFmtInt8 ? 2 : 4;  // 8-element chunks per 16 code bytes
-        constexpr int UPK = D / 8 / UC;              // 16-byte code units per key
-#pragma unroll 2
-        for (int q = dt; q < NK * UPK; q += 32 * G::DQ_WARPS) {
-          const int k = q & (NK - 1), g = q >> 6;
-          const int b4 = k >> 4, x7 = k & 7;
-          uint4 w = *reinterpret_cast<const uint4*>(sb + (k + (b4 + kv) * 16) * G::SROW + g * 16);
-          if (!((fmask >> b4) & 1)) w = make_uint4(0, 0, 0, 0);  // code 0 in both formats
-          uint8_t* const dst = tile_dst + (((g * UC) >> 3) * NK + k) * 128;
-          if constexpr (FMT == kFmtInt4) {
-            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-              *reinterpret_cast<uint4*>(dst + ((((g * 4 + i) & 7) ^ x7) << 4)) = dq_word_int4(wv[i]);
-          } else {
-            *reinterpret_cast<uint4*>(dst + ((((g * 2) & 7) ^ x7) << 4)) = dq_pair_int8(w.x, w.y);
-            *reinterpret_cast<uint4*>(dst + ((((g * 2 + 1) & 7) ^ x7) << 4)) = dq_pair_int8(w.z, w.w);
+            for (int col = 0; col < G::CB / 16; col++) cp_async16(dst + col * 16, src + col * 16);
+            cp_async4(sb + G::SC_OFF + ((b4 * 2 + kv) * 16 + row) * 4,
+                      (kv ? c.v_scale : c.k_scale) + (long long)blk * c.geo.sblk + row * c.geo.srow +
+                          (long long)h * c.geo.shead);
           }
-        }
-      };
-      issue(0, stg, block_of(0));
-      cp_async_commit();
-      if (nsteps > 1) issue(1, stg + G::STG, block_of(1));
-      cp_async_commit();
-      int blk_next = block_of(2);
+          if (kv == 0 && row == 0) {
+            reinterpret_cast<int*>(sb + G::FL_OFF)[b4] = ok;
+            if (kb < nkb && !ok) flag(c.status, KV_INT4_DEV_BAD_BLOCK);
+          }
+        };
+        // dequantise the K (kv = 0) or V (kv = 1) codes of staging sb into a
+        // tile: a thread takes 16 code bytes (one shared load) of one key;
+        // consecutive threads take consecutive keys, so that the eight keys
+        // of a store phase cover the eight swizzled 16-byte positions
+        auto dequant = [&](const uint8_t* sb, uint8_t* tile_dst, int kv, int fmask) {
+          constexpr int UC = FMT == kFmtInt8 ? 2 : 4;  // 8-element chunks per 16 code bytes
+          constexpr int UPK = D / 8 / UC;              // 16-byte code units per key
+#pragma unroll 2
+          for (int q = dt; q < NK * UPK; q += 32 * G::DQ_WARPS) {
+            const int k = q & (NK - 1), g = q >> 6;
+            const int b4 = k >> 4, x7 = k & 7;
+            uint4 w = *reinterpret_cast<const uint4*>(sb + (k + (b4 + kv) * 16) * G::SROW + g * 16);
+            if (!((fmask >> b4) & 1)) w = make_uint4(0, 0, 0, 0);  // code 0 in both formats
+            uint8_t* const dst = tile_dst + (((g * UC) >> 3) * NK + k) * 128;
+            if constexpr (FMT == kFmtInt4) {
+              const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int i = 0; i < 4; i++)
+                *reinterpret_cast<uint4*>(dst + ((((g * 4 + i) & 7) ^ x7) << 4)) = dq_word_int4(wv[i]);
+            } else {
+              *reinterpret_cast<uint4*>(dst + ((((g * 2) & 7) ^ x7) << 4)) = dq_pair_int8(w.x, w.y);
+              *reinterpret_cast<uint4*>(dst + ((((g * 2 + 1) & 7) ^ x7) << 4)) = dq_pair_int8(w.z, w.w);
+            }
+          }
+        };
+        issue(0, stg, block_of(0));
+        cp_async_commit();
+        if (nsteps > 1) issue(1, stg + G::STG, block_of(1));
+        cp_async_commit();
+        int blk_next = block_of(2);
 #pragma unroll 1
-      for (int j = 0; j < nsteps; j++) {
-        const int b = j & 1;
-        uint8_t* const sb = stg + b * G::STG;
-        cp_async_wait<1>();
-        dq_sync();  // every thread's copies of step j have landed
-        // the K tile of step j is free once S of step j - KBUF is complete;
-        // the ring entry of step j once the softmax of step j - 3 is (S of
-        // step j - 2 follows both halves' P of step j - 3)
-        if (j >= G::KBUF) {
-          const int fb = (j - G::KBUF) & 1;
-          ws_wait(bar(KFREE + fb), (ph_kfree >> fb) & 1, abort_flag, c.status);
-          ph_kfree ^= 1u << fb;
+        for (int j = 0; j < nsteps; j++) {
+          const int b = j & 1;
+          uint8_t* const sb = stg + b * G::STG;
+          cp_async_wait<1>();
+          dq_sync();  // every thread's copies of step j have landed
+          // the K tile of step j is free once S of step j - KBUF is complete;
+          // the ring entry of step j once the softmax of step j - 3 is (S of
+          // step j - 2 follows both halves' P of step j - 3)
+          if (j >= G::KBUF) {
+            const int fb = (j - G::KBUF) & 1;
+            ws_wait(bar(KFREE + fb), (ph_kfree >> fb) & 1, abort_flag, c.status);
+            ph_kfree ^= 1u << fb;
+          }
+          const int* sfl = reinterpret_cast<const int*>(sb + G::FL_OFF);
+          uint8_t* const re = ring + (j % G::NRING) * G::RING;
+          const int fmask = (sfl[0] != 0) | (sfl[1] != 0) << 1 | (sfl[2] != 0) << 2 | (sfl[3] != 0) << 3;
+          if (dt < NK) {
+            const float* scs = reinterpret_cast<const float*>(sb + G::SC_OFF);
+            const float vsc = scs[(dt >> 4) * 32 + 16 + (dt & 15)];
+            reinterpret_cast<float*>(re)[dt] = scs[(dt >> 4) * 32 + (dt & 15)];
+            reinterpret_cast<float*>(re)[NK + dt] = vsc;
+            // the vote reads only keys that exist (usable block, position below the
+            // sequence length): the threshold, and so the rounding, depend on the
+            // cache's contents alone
+            const bool exists = ((fmask >> (dt >> 4)) & 1) && (kb0 + j * 4) * 16 + dt < L;
+            const bool small = __all_sync(0xffffffffu, !exists || fabsf(vsc) < 128.f);
+            if (lane == 0) reinterpret_cast<int*>(re + 2 * NK * 4)[4 + (dt >> 5)] = small;
+          } else if (dt < NK + 4) {
+            reinterpret_cast<int*>(re + 2 * NK * 4)[dt - NK] = sfl[dt - NK];
+          }
+          dequant(sb, sK + (G::KBUF == 2 ? b : 0) * G::KVBYTES, 0, fmask);
+          fence_proxy_async_smem();  // the tile is read by the tensor cores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(KFULL + b));
+          if (j >= 2) {
+            ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);  // PVs of step j - 2 done
+            ph_vfree ^= 1u << b;
+          }
+          dequant(sb, sV + b * G::KVBYTES, 1, fmask);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(VFULL + b));
+          dq_sync();  // every thread is done with staging b
+          if (j + 2 < nsteps) issue(j + 2, sb, blk_next);
+          cp_async_commit();
+          blk_next = block_of(j + 3);
         }
-        const int* sfl = reinterpret_cast<const int*>(sb + G::FL_OFF);
-        uint8_t* const re = ring + (j % G::NRING) * G::RING;
-        const int fmask = (sfl[0] != 0) | (sfl[1] != 0) << 1 | (sfl[2] != 0) << 2 | (sfl[3] != 0) << 3;
-        if (dt < NK) {
-          const float* scs = reinterpret_cast<const float*>(sb + G::SC_OFF);
-          const float vsc = scs[(dt >> 4) * 32 + 16 + (dt & 15)];
-          reinterpret_cast<float*>(re)[dt] = scs[(dt >> 4) * 32 + (dt & 15)];
-          reinterpret_cast<float*>(re)[NK + dt] = vsc;
-          // the vote reads only keys that exist (usable block, position below the
-          // sequence length): the threshold, and so the rounding, depend on the
-          // cache's contents alone
-          const bool exists = ((fmask >> (dt >> 4)) & 1) && (kb0 + j * 4) * 16 + dt < L;
-          const bool small = __all_sync(0xffffffffu, !exists || fabsf(vsc) < 128.f);
-          if (lane == 0) reinterpret_cast<int*>(re + 2 * NK * 4)[4 + (dt >> 5)] = small;
-        } else if (dt < NK + 4) {
-          reinterpret_cast<int*>(re + 2 * NK * 4)[dt - NK] = sfl[dt - NK];
+        cp_async_wait<0>();
+        // the completions not waited for above: kfree of the last step, vfree of the last use of each V tile
+        for (int st = nsteps - G::KBUF < 0 ? 0 : nsteps - G::KBUF; st < nsteps; st++) {
+          ws_wait(bar(KFREE + (st & 1)), (ph_kfree >> (st & 1)) & 1, abort_flag, c.status);
+          ph_kfree ^= 1u << (st & 1);
         }
-        dequant(sb, sK + (G::KBUF == 2 ? b : 0) * G::KVBYTES, 0, fmask);
-        fence_proxy_async_smem();  // the tile is read by the tensor cores
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KFULL + b));
-        if (j >= 2) {
-          ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);  // PVs of step j - 2 done
+        for (int b = 0; b < 2 && b < nsteps; b++) {
+          ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
           ph_vfree ^= 1u << b;
         }
-        dequant(sb, sV + b * G::KVBYTES, 1, fmask);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(VFULL + b));
-        dq_sync();  // every thread is done with staging b
-        if (j + 2 < nsteps) issue(j + 2, sb, blk_next);
-        cp_async_commit();
-        blk_next = block_of(j + 3);
-      }
-      cp_async_wait<0>();
-      // the completions not waited for above: kfree of the last step, vfree of the last use of each V tile
-      for (int st = nsteps - G::KBUF < 0 ? 0 : nsteps - G::KBUF; st < nsteps; st++) {
-        ws_wait(bar(KFREE + (st & 1)), (ph_kfree >> (st & 1)) & 1, abort_flag, c.status);
-        ph_kfree ^= 1u << (st & 1);
-      }
-      for (int b = 0; b < 2 && b < nsteps; b++) {
-        ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
-        ph_vfree ^= 1u << b;
-      }
       } else {
-      // ================= MMA warp (lane 0 issues, the warp waits together) =================
-      const bool leader = lane == 0;
-      // operand descriptors: the start address is the low 14-bit field of
-      // (address >> 4), so an offset below 256 KB adds to the descriptor
-      const uint64_t dq = umma_desc(smem_addr(sQ), 16, 1024);
-      const uint64_t dk = umma_desc(smem_addr(sK), 16, 1024);
-      const uint64_t dv = umma_desc(smem_addr(sV), NK * 128, 1024);
-      // S_h = Q_h K^T over the head dimension into TMEM columns [64h, 64h + 64)
-      auto issue_s = [&](int hh, int st) {
-        if (leader) {
-          const uint64_t kt = dk + (uint64_t)((G::KBUF == 2 ? (st & 1) : 0) * (G::KVBYTES >> 4));
+        // ================= MMA warp (lane 0 issues, the warp waits together) =================
+        const bool leader = lane == 0;
+        // operand descriptors: the start address is the low 14-bit field of
+        // (address >> 4), so an offset below 256 KB adds to the descriptor
+        const uint64_t dq = umma_desc(smem_addr(sQ), 16, 1024);
+        const uint64_t dk = umma_desc(smem_addr(sK), 16, 1024);
+        const uint64_t dv = umma_desc(smem_addr(sV), NK * 128, 1024);
+        // S_h = Q_h K^T over the head dimension into TMEM columns [64h, 64h + 64)
+        auto issue_s = [&](int hh, int st) {
+          if (leader) {
+            const uint64_t kt = dk + (uint64_t)((G::KBUF == 2 ? (st & 1) : 0) * (G::KVBYTES >> 4));
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS; ks++)
-            umma_f16(tmem + 64 * hh, dq + (uint64_t)(((ks >> 2) * ROWS * 128 + hh * 128 * 128 + (ks & 3) * 32) >> 4),
-                     kt + (uint64_t)(((ks >> 2) * NK * 128 + (ks & 3) * 32) >> 4), IDESC_S, ks > 0);
-        }
-      };
-      // O_h += P_h V_b, P_h the f16 pairs over S_h's first 32 columns
-      auto issue_pv = [&](int hh, int b, bool first) {
-        if (leader) {
-          const uint64_t vt = dv + (uint64_t)(b * (G::KVBYTES >> 4));
+            for (int ks = 0; ks < KSTEPS; ks++)
+              umma_f16(tmem + 64 * hh, dq + (uint64_t)(((ks >> 2) * ROWS * 128 + hh * 128 * 128 + (ks & 3) * 32) >> 4),
+                       kt + (uint64_t)(((ks >> 2) * NK * 128 + (ks & 3) * 32) >> 4), IDESC_S, ks > 0);
+          }
+        };
+        // O_h += P_h V_b, P_h the f16 pairs over S_h's first 32 columns
+        auto issue_pv = [&](int hh, int b, bool first) {
+          if (leader) {
+            const uint64_t vt = dv + (uint64_t)(b * (G::KVBYTES >> 4));
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++)
-            umma_f16_ts(tmem + 128 + hh * D, tmem + 64 * hh + kk * 8, vt + (uint64_t)(kk * (2048 >> 4)), IDESC_O,
-                        !first || kk > 0);
-        }
-      };
-      auto commit = [&](int i) {
-        if (leader) umma_commit(bar(i));
-        __syncwarp();
-      };
-      q_sync();  // the softmax warps have written Q'
-      if (nsteps > 0) {
-        ws_wait(bar(KFULL), ph_kfull & 1, abort_flag, c.status);
-        ph_kfull ^= 1;
-        tc_fence_after();
-        issue_s(0, 0);
-        commit(SFULL);
-        issue_s(1, 0);
-        commit(SFULL + 1);
-        commit(KFREE);
-      }
-#pragma unroll 1
-      for (int j = 0; j < nsteps; j++) {
-        const int b = j & 1, nb = (j + 1) & 1;
-        // V of this step and K of the next are normally ready long before
-        // P: wait for them first, so that PV and the next S issue as soon
-        // as the half's P lands (neither waits on anything this warp issues
-        // later: V(j) follows PV(j - 2), K(j + 1) follows S(j + 1 - KBUF))
-        ws_wait(bar(VFULL + b), (ph_vfull >> b) & 1, abort_flag, c.status);
-        ph_vfull ^= 1u << b;
-        if (j + 1 < nsteps) {
-          ws_wait(bar(KFULL + nb), (ph_kfull >> nb) & 1, abort_flag, c.status);
-          ph_kfull ^= 1u << nb;
-        }
-        ws_wait(bar(PFULL), ph_pfull & 1, abort_flag, c.status);
-        ph_pfull ^= 1;
-        tc_fence_after();
-        issue_pv(0, b, j == 0);
-        if (j + 1 < nsteps) {
-          issue_s(0, j + 1);
+            for (int kk = 0; kk < 4; kk++)
+              umma_f16_ts(tmem + 128 + hh * D, tmem + 64 * hh + kk * 8, vt + (uint64_t)(kk * (2048 >> 4)), IDESC_O,
+                          !first || kk > 0);
+          }
+        };
+        auto commit = [&](int i) {
+          if (leader) umma_commit(bar(i));
+          __syncwarp();
+        };
+        q_sync();  // the softmax warps have written Q'
+        if (nsteps > 0) {
+          ws_wait(bar(KFULL), ph_kfull & 1, abort_flag, c.status);
+          ph_kfull ^= 1;
+          tc_fence_after();
+          issue_s(0, 0);
           commit(SFULL);
-        }
-        ws_wait(bar(PFULL + 1), (ph_pfull >> 1) & 1, abort_flag, c.status);
-        ph_pfull ^= 2;
-        tc_fence_after();
-        issue_pv(1, b, j == 0);
-        commit(VFREE + b);
-        if (j + 1 < nsteps) {
-          issue_s(1, j + 1);
+          issue_s(1, 0);
           commit(SFULL + 1);
-          commit(KFREE + nb);
+          commit(KFREE);
         }
+#pragma unroll 1
+        for (int j = 0; j < nsteps; j++) {
+          const int b = j & 1, nb = (j + 1) & 1;
+          // V of this step and K of the next are normally ready long before
+          // P: wait for them first, so that PV and the next S issue as soon
+          // as the half's P lands (neither waits on anything this warp issues
+          // later: V(j) follows PV(j - 2), K(j + 1) follows S(j + 1 - KBUF))
+          ws_wait(bar(VFULL + b), (ph_vfull >> b) & 1, abort_flag, c.status);
+          ph_vfull ^= 1u << b;
+          if (j + 1 < nsteps) {
+            ws_wait(bar(KFULL + nb), (ph_kfull >> nb) & 1, abort_flag, c.status);
+            ph_kfull ^= 1u << nb;
+          }
+          ws_wait(bar(PFULL), ph_pfull & 1, abort_flag, c.status);
+          ph_pfull ^= 1;
+          tc_fence_after();
+          issue_pv(0, b, j == 0);
+          if (j + 1 < nsteps) {
+            issue_s(0, j + 1);
+            commit(SFULL);
+          }
+          ws_wait(bar(PFULL + 1), (ph_pfull >> 1) & 1, abort_flag, c.status);
+          ph_pfull ^= 2;
+          tc_fence_after();
+          issue_pv(1, b, j == 0);
+          commit(VFREE + b);
+          if (j + 1 < nsteps) {
+            issue_s(1, j + 1);
+            commit(SFULL + 1);
+            commit(KFREE + nb);
+          }
+        }
+        commit(ODONE);
       }
-      commit(ODONE);
-      }
-    // item end: every role is done with TMEM, the tiles and the ring
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+      // item end: every role is done with TMEM, the tiles and the ring
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
     }
   }
   if (warp == 15) {
