@@ -126,7 +126,9 @@ __device__ __forceinline__ bool is_decode_kind(int qlen, const Common& c) {
 // 1. prep: schedule (CTA 0) + query rotation (CTAs 1..)
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
-constexpr int kPrepRowsPerCta = 8;
+// query rotation: one thread per piece of kPrepPiece(D) consecutive elements
+// of a row (a whole Hadamard block, or 64 elements of a longer one)
+__host__ __device__ constexpr int kPrepPiece(int d) { return (d & -d) < 64 ? (d & -d) : 64; }
 
 template <typename T>
 __device__ T block_exclusive_scan(T v, T* total, T* sbuf /*[kPrepThreads/32]*/) {
@@ -213,45 +215,87 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
     return;
   }
 
-  // query rotation: one warp per (token, q head) row, held in registers
-  // (lane owns elements lane + 32k); butterfly stages h < 32 pair lanes,
-  // stages h >= 32 pair the lane's own registers
+  // query rotation: q' = (I_n (x) H_b) D q * qscale as f16.  A thread holds
+  // E = min(b, 64) consecutive elements of one row (16-byte loads and
+  // stores): D is applied as sign-bit XOR masks on the bf16 pairs, the
+  // Hadamard stages below E run in registers (packed f32x2), the stages from
+  // E to b across the b / E threads of the block (adjacent lanes).
   constexpr int B = Head<D>::b;
-  constexpr int PER = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = (long long)(blockIdx.x - 1) * kPrepRowsPerCta + warp;
-  if (row >= (long long)c.num_q_tokens * c.hq) return;
+  constexpr int E = kPrepPiece(D);
+  constexpr int TPB = B / E;  // threads per Hadamard block: 1, 2 or 4
+  constexpr int PPR = D / E;  // pieces per row
+  __shared__ __align__(16) uint32_t smask[D / 2];
+  if constexpr (ROT) {
+    for (int i = threadIdx.x; i < D / 2; i += kPrepThreads)
+      smask[i] = (c.signs[2 * i] < 0 ? 0x8000u : 0u) | (c.signs[2 * i + 1] < 0 ? 0x80000000u : 0u);
+    __syncthreads();
+  }
+  const long long piece = (long long)(blockIdx.x - 1) * kPrepThreads + threadIdx.x;
+  // the pieces of one Hadamard block are adjacent lanes and all valid or all
+  // not (PPR is a multiple of TPB): every lane stays for the shuffles
+  const bool live = piece < (long long)c.num_q_tokens * c.hq * PPR;
+  const long long row = live ? piece / PPR : 0;
+  const int e0 = (int)(piece - (piece / PPR) * PPR) * E;
   const long long t = row / c.hq;
   const int h = (int)(row - t * c.hq);
-  const uint16_t* src = c.q + t * c.q_stride + (long long)h * D;
-  float x[PER];
+  const uint16_t* src = c.q + t * c.q_stride + (long long)h * D + e0;
+  float x[E];
 #pragma unroll
-  for (int k = 0; k < PER; k++) {
-    const float v = __uint_as_float((uint32_t)src[lane + 32 * k] << 16);
-    x[k] = (ROT && c.signs[lane + 32 * k] < 0) ? -v : v;
-  }
-  if constexpr (ROT) {
+  for (int v = 0; v < E / 8; v++) {
+    uint4 w = live ? reinterpret_cast<const uint4*>(src)[v] : make_uint4(0, 0, 0, 0);
+    if constexpr (ROT) {
+      const uint4 m = *reinterpret_cast<const uint4*>(smask + (e0 >> 1) + 4 * v);
+      w.x ^= m.x; w.y ^= m.y; w.z ^= m.z; w.w ^= m.w;
+    }
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int hh = 1; hh < B && hh < 32; hh <<= 1) {
-    const float f = (lane & hh) ? -1.f : 1.f;  // upper element: partner - self
-#pragma unroll
-    for (int k = 0; k < PER; k++) x[k] = fmaf(f, x[k], __shfl_xor_sync(0xffffffffu, x[k], hh));
-  }
-#pragma unroll
-  for (int m = 1; 32 * m < B; m <<= 1) {
-#pragma unroll
-    for (int k = 0; k < PER; k++) {
-      if ((k & m) == 0) {
-        const float a0 = x[k], b0 = x[k + m];
-        x[k] = a0 + b0;
-        x[k + m] = a0 - b0;
-      }
+    for (int k = 0; k < 4; k++) {
+      x[8 * v + 2 * k] = bf16lo_to_f32(ww[k]);
+      x[8 * v + 2 * k + 1] = bf16hi_to_f32(ww[k]);
     }
   }
-  }
-  __half* dst = pv.qrot + row * D;
+  if constexpr (ROT) {
+    // stage 1: pairs (i, i + 1); packed as (x_i, x_{i+2}) +- (x_{i+1}, x_{i+3})
 #pragma unroll
-  for (int k = 0; k < PER; k++) dst[lane + 32 * k] = __float2half_rn(x[k] * c.qscale);
+    for (int i = 0; i < E; i += 4) {
+      const float2 a = make_float2(x[i], x[i + 2]), b = make_float2(x[i + 1], x[i + 3]);
+      const float2 u = f2add(a, b), w = f2sub(a, b);
+      x[i] = u.x; x[i + 2] = u.y; x[i + 1] = w.x; x[i + 3] = w.y;
+    }
+    // stages 2 .. E/2: pairs (i, i + hh) and (i + 1, i + 1 + hh) together
+#pragma unroll
+    for (int hh = 2; hh < E; hh <<= 1) {
+#pragma unroll
+      for (int i = 0; i < E; i += 2) {
+        if ((i & hh) == 0) {
+          const float2 a = make_float2(x[i], x[i + 1]), b = make_float2(x[i + hh], x[i + hh + 1]);
+          const float2 u = f2add(a, b), w = f2sub(a, b);
+          x[i] = u.x; x[i + 1] = u.y; x[i + hh] = w.x; x[i + hh + 1] = w.y;
+        }
+      }
+    }
+    // stages E .. b/2: the partner piece is lane ^ m (upper element = partner - self)
+#pragma unroll
+    for (int m = 1; m < TPB; m <<= 1) {
+      const float f = (threadIdx.x & m) ? -1.f : 1.f;
+#pragma unroll
+      for (int k = 0; k < E; k++) x[k] = fmaf(f, x[k], __shfl_xor_sync(0xffffffffu, x[k], m));
+    }
+  }
+  if (live) {
+    __half* dst = pv.qrot + row * D + e0;
+    const float2 qs = make_float2(c.qscale, c.qscale);
+#pragma unroll
+    for (int v = 0; v < E / 8; v++) {
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const float2 y = __fmul2_rn(make_float2(x[8 * v + 2 * k], x[8 * v + 2 * k + 1]), qs);
+        o[k] = pack_f16x2(y.x, y.y);
+      }
+      reinterpret_cast<uint4*>(dst)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1367,7 +1411,8 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   // 1. prep
   {
     const long long rows = (long long)a.num_q_tokens * a.num_q_heads;
-    const long long grid = 1 + (rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta;
+    const long long pieces = rows * (D / kPrepPiece(D));
+    const long long grid = 1 + (pieces + kPrepThreads - 1) / kPrepThreads;
     if (grid > 0x7fffffff) return KV_INT4_ERR_SIZE;
     timing_begin(kTimedPrep, stream);
     prep_kernel<D, ROT><<<(unsigned)grid, kPrepThreads, 0, stream>>>(c, pv);
