@@ -308,3 +308,32 @@ def test_prefill_rescale_policies_with_large_v_scales_and_score_jumps(fmt, d):
     scale = np.maximum(1.0, np.abs(ref).max(axis=-1, keepdims=True))
     assert scale.max() > 100  # the large-V blocks carry weight
     assert_close_attention(out.float().cpu().numpy() / scale, ref / scale, what=f"{fmt} d={d} magnitudes")
+
+
+@pytest.mark.parametrize("fmt", ["int4", "int8"])
+@pytest.mark.parametrize("case", [
+    ("mixed_window_d128", 16, 4, 128, [(1, 300), (40, 90), (1, 20)], 30),
+    ("mixed_d128", 16, 4, 128, [(1, 300), (40, 90), (1, 20)], 0),
+    ("prefill_d192_g4", 8, 2, 192, [(100, 130), (17, 17)], 0),
+    ("prefill_d96_g1_window", 4, 4, 96, [(70, 200), (33, 33)], 50),
+], ids=lambda c: c[0] if isinstance(c, tuple) else c)
+def test_attention_is_deterministic(case, fmt):
+    """Repeated calls on the same cache give bit-identical outputs: the
+    schedule's order (atomic item counter, stream-K ranges) and the prefill's
+    pipeline timing must not change any rounding."""
+    name, hq, hkv, d, seqs, win = case
+    w = synthetic.custom_workload(hq, hkv, d, seqs, seed=41, causal=True, sliding_window=win)
+    pk = PagedKV(w, fmt=fmt)
+    pk.populate_history(gen_device="cpu")
+    q, k, v, slots = pk.step_inputs(gen_device="cpu")
+    pk.write(k, v, slots)
+    first = None
+    for _ in range(6):
+        out = torch.full((w.num_q_tokens, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pk.attend(q, out)
+        torch.cuda.synchronize()
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out, first), name
+    assert pk.status.item() == 0
