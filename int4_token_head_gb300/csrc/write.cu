@@ -490,7 +490,7 @@ struct TcGeom {
   // GB300: warps per SM matter more than depth).
   static constexpr int PSTRIDE = 2 * ROWB + 16;  // bytes per staged pair
   static constexpr int WSTAGE = 8 * PSTRIDE;     // one warp's rows of one stage
-  static constexpr int STAGES = D == 192 ? 2 : D == 96 ? 4 : 3;
+  static constexpr int STAGES = D == 96 ? 4 : 2;
   static constexpr int MIN_CTAS = D == 192 ? 3 : 4;
   static constexpr int STAGE_BYTES = WARPS * WSTAGE;
   static constexpr int BFRAG_BYTES = NG * 2 * 32 * 8;
