@@ -127,8 +127,10 @@ __device__ __forceinline__ bool is_decode_kind(int qlen, const Common& c) {
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
 // query rotation: one thread per piece of kPrepPiece(D) consecutive elements
-// of a row (a whole Hadamard block, or 64 elements of a longer one)
-__host__ __device__ constexpr int kPrepPiece(int d) { return (d & -d) < 64 ? (d & -d) : 64; }
+// of a row (a whole 16-element Hadamard block, or 16 elements of a longer
+// one, its later stages by shuffles: more threads in flight per SM than
+// longer pieces, measured faster)
+__host__ __device__ constexpr int kPrepPiece(int d) { return (d & -d) < 16 ? (d & -d) : 16; }
 
 template <typename T>
 __device__ T block_exclusive_scan(T v, T* total, T* sbuf /*[kPrepThreads/32]*/) {
@@ -216,13 +218,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
   }
 
   // query rotation: q' = (I_n (x) H_b) D q * qscale as f16.  A thread holds
-  // E = min(b, 64) consecutive elements of one row (16-byte loads and
+  // E = min(b, 16) consecutive elements of one row (16-byte loads and
   // stores): D is applied as sign-bit XOR masks on the bf16 pairs, the
   // Hadamard stages below E run in registers (packed f32x2), the stages from
   // E to b across the b / E threads of the block (adjacent lanes).
   constexpr int B = Head<D>::b;
   constexpr int E = kPrepPiece(D);
-  constexpr int TPB = B / E;  // threads per Hadamard block: 1, 2 or 4
+  constexpr int TPB = B / E;  // threads per Hadamard block: 1 .. 16
   constexpr int PPR = D / E;  // pieces per row
   __shared__ __align__(16) uint32_t smask[D / 2];
   if constexpr (ROT) {
