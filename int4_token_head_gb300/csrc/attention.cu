@@ -862,6 +862,7 @@ struct RedParams {
   Common c;
   PlanView pv;
   int num_ctas;
+  int cps;  // warps (query columns) per segment: min(dcols, max_query_len * group)
 };
 
 template <int D, bool ROT>
@@ -870,14 +871,17 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   const PlanView& pv = prm.pv;
   constexpr int B = Head<D>::b;
   __shared__ float srow[kDecodeCols][D];
-  const int seg = blockIdx.x;
+  // a warp per (segment, query column): the CTA's dcols warps cover
+  // dcols / cps segments of cps columns each
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = blockIdx.x * (c.dcols / prm.cps) + warp / prm.cps;
+  const int col = warp % prm.cps;
   const int n_dseq = pv.plan[0];
   if (seg >= n_dseq * c.hkv) return;
   const int i = seg / c.hkv, h = seg - i * c.hkv;
   const int seq = pv.dseq[i];
   const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
-  const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (col >= ql * c.group) return;  // ql * group <= dcols
+  if (col >= ql * c.group) return;  // ql * group <= cps
   const int nblk = (c.seq_lens[seq] + 15) / 16;
   const int npos = (nblk - first_block(c, c.seq_lens[seq], ql) + c.np - 1) / c.np;
   const int grp = h / c.hg, hl = h - grp * c.hg;
@@ -925,7 +929,7 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
       if (wstart(w) == p) merge_cta(w);
     }
   }
-  float* r = srow[col];
+  float* r = srow[warp];
   const float inv = 1.f / (Lsum * (ROT ? (float)B : 1.f));
 #pragma unroll
   for (int k = 0; k < PER; k++) r[lane + 32 * k] = acc[k] * inv;
@@ -1470,10 +1474,15 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
           DecParams{c, pv, num_ctas});
     timing_end(kTimedDecode, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
-    const long long rgrid = (long long)a.num_seqs * a.num_kv_heads;
+    // query columns a decode segment can need: q_len * G, at most dcols
+    const long long mcols = (long long)(a.max_query_len > 0 ? a.max_query_len : 1) * c.group;
+    int cps = c.dcols;
+    while (cps > 1 && cps / 2 >= mcols) cps /= 2;  // a divisor of dcols (a power of two)
+    const long long spc = c.dcols / cps;  // segments per CTA
+    const long long rgrid = ((long long)a.num_seqs * a.num_kv_heads + spc - 1) / spc;
     if (rgrid > 0x7fffffff) return KV_INT4_ERR_SIZE;
     timing_begin(kTimedReduce, stream);
-    reduce_kernel<D, ROT><<<(unsigned)rgrid, kDecodeCols * 32, 0, stream>>>(RedParams{c, pv, num_ctas});
+    reduce_kernel<D, ROT><<<(unsigned)rgrid, c.dcols * 32, 0, stream>>>(RedParams{c, pv, num_ctas, cps});
     timing_end(kTimedReduce, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;
   }
