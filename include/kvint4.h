@@ -384,8 +384,20 @@ KVINT4_API int kv_int4_timing_collect(double* ms, int* launches, int* dropped);
 /* kv_int4_status_string -- a static, human-readable name for a KV_INT4_* code. */
 KVINT4_API const char* kv_int4_status_string(int status);
 
-/* kv_int4_version -- the library's ABI version: 2 (kv_int4_rht and the int8_per_token_head entry
- * points kv_int8_write / kv_int8_attention added; the attention entry points take sliding_window). */
+/* kv_int4_selftest_wait -- self-test of the bounded barrier wait that the pipelined kernels use
+ * (the write kernel's copy stages, the prefill's hand-offs between warp roles): one warp waits on
+ * an mbarrier that nothing arrives at, gives up after `iterations` attempts, ORs
+ * KV_INT4_DEV_TIMEOUT into *dev_status and returns; the SM cycles it waited go to *dev_cycles
+ * (nullable).  It never faults or hangs: it exercises the time-out path on a GPU, and its cycles
+ * per attempt bound how long the kernels' own limit (2^20 attempts) can hold a warp.  Device
+ * pointers, enqueued on `stream`.  KV_INT4_ERR_SIZE for iterations < 0, KV_INT4_ERR_NULL without
+ * dev_status. */
+KVINT4_API int kv_int4_selftest_wait(int iterations, int32_t* dev_status, uint64_t* dev_cycles,
+                                     cudaStream_t stream);
+
+/* kv_int4_version -- the library's ABI version: 3 (2: kv_int4_rht and the int8_per_token_head
+ * entry points kv_int8_write / kv_int8_attention, sliding_window in the attention entry points;
+ * 3: the in-slot entry points, kv_int4_attention_noalloc's window argument, kv_int4_selftest_wait). */
 KVINT4_API int kv_int4_version(void);
 
 #ifdef __cplusplus

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "kv_int4_status_string": (ctypes.c_char_p, [c_int]),
     "kv_int4_timing_enable": (c_int, [c_int]),
     "kv_int4_timing_collect": (c_int, [c_void_p, c_void_p, c_void_p]),
+    "kv_int4_selftest_wait": (c_int, [c_int, c_void_p, c_void_p, c_void_p]),
     "kv_int4_version": (c_int, []),
 }
 
@@ -233,6 +234,16 @@ def timing_collect():
     drop = (ctypes.c_int * n)()
     _raise(load().kv_int4_timing_collect(ms, cnt, drop), "kv_int4_timing_collect")
     return {k: (ms[i], cnt[i], drop[i]) for i, k in enumerate(TIMED_KINDS)}
+
+
+def selftest_wait(iterations: int, dev_status: torch.Tensor, dev_cycles: Optional[torch.Tensor] = None, stream=None):
+    """One warp waits on an mbarrier nothing arrives at, gives up after `iterations`
+    attempts and ORs DEV_TIMEOUT into dev_status (int32 [1]); dev_cycles (int64 [1])
+    receives the SM cycles it waited."""
+    _check(dev_status.dtype == torch.int32 and dev_status.is_cuda, "dev_status: int32 CUDA tensor")
+    _check(dev_cycles is None or (dev_cycles.dtype == torch.int64 and dev_cycles.is_cuda), "dev_cycles: int64 CUDA tensor")
+    _raise(load().kv_int4_selftest_wait(int(iterations), _ptr(dev_status), _ptr(dev_cycles), _stream(stream)),
+           "kv_int4_selftest_wait")
 
 
 def attention_workspace_size(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_size) -> int:

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(PKG, "libkvint4.so")
 STAMP = os.path.join(BUILD_DIR, "stamp.txt")
 HEADER = os.path.join(ROOT, "include", "kvint4.h")
 
-SOURCES = ["api.cu", "write.cu", "write_int8.cu", "attention.cu", "rht.cu", "timing.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "write.cu", "write_int8.cu", "attention.cu", "rht.cu", "timing.cu", "noalloc.cu", "selftest.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

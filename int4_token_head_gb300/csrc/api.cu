@@ -70,7 +70,7 @@ using namespace kvint4;
 
 extern "C" {
 
-int kv_int4_version(void) { return 2; }
+int kv_int4_version(void) { return 3; }
 
 const char* kv_int4_status_string(int status) {
   switch (status) {

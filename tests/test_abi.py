@@ -55,7 +55,7 @@ def test_status_strings_and_version(lib):
             s = lib.kv_int4_status_string(code).decode()
             assert s and s != "unknown status"
     assert lib.kv_int4_status_string(999).decode() == "unknown status"
-    assert lib.kv_int4_version() == 2
+    assert lib.kv_int4_version() == 3
 
 
 def test_workspace_size_is_host_only_and_monotone(lib):
@@ -196,3 +196,8 @@ def test_inslot_entry_points_validation(lib):
     assert a(kv=None) == D["KV_INT4_ERR_NULL"]
     assert a(signs=None) == D["KV_INT4_ERR_NULL"]
     assert a(kv=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
+
+
+def test_selftest_wait_validation(lib):
+    assert lib.kv_int4_selftest_wait(-1, FAKE, None, None) == D["KV_INT4_ERR_SIZE"]
+    assert lib.kv_int4_selftest_wait(16, None, None, None) == D["KV_INT4_ERR_NULL"]
