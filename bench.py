@@ -127,9 +127,13 @@ def decode_columns(w) -> int:
     return 4 if cols <= 4 else 8
 
 
-def source_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(paths) -> str:
+    """First 16 hex digits of the SHA-256 of the files' bytes, in order."""
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
@@ -144,8 +148,9 @@ def recorded_traffic(kernel: str, workload: str):
             if "=" in line and not line.startswith("#"):
                 k, v = line.split("=", 1)
                 kv[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "int4_token_head_gb300", "csrc", kv.get("source", "attention.cu"))
-    if kv.get("source_sha") != source_sha(src):
+    names = kv.get("source", "").split()
+    srcs = [os.path.join(ROOT, "int4_token_head_gb300", "csrc", n) for n in names]
+    if not srcs or not all(os.path.exists(p) for p in srcs) or kv.get("source_sha") != source_sha(srcs):
         return None
     try:
         return float(kv["bytes_per_launch"])

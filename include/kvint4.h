@@ -389,9 +389,9 @@ KVINT4_API const char* kv_int4_status_string(int status);
  * an mbarrier that nothing arrives at, gives up after `iterations` attempts, ORs
  * KV_INT4_DEV_TIMEOUT into *dev_status and returns; the SM cycles it waited go to *dev_cycles
  * (nullable).  It never faults or hangs: it exercises the time-out path on a GPU, and its cycles
- * per attempt bound how long the kernels' own limit (2^20 attempts) can hold a warp.  Device
- * pointers, enqueued on `stream`.  KV_INT4_ERR_SIZE for iterations < 0, KV_INT4_ERR_NULL without
- * dev_status. */
+ * per attempt bound how long the kernels' own limit (2^18 attempts, about a second) can hold a
+ * warp.  Device pointers, enqueued on `stream`.  KV_INT4_ERR_SIZE for iterations < 0,
+ * KV_INT4_ERR_NULL without dev_status. */
 KVINT4_API int kv_int4_selftest_wait(int iterations, int32_t* dev_status, uint64_t* dev_cycles,
                                      cudaStream_t stream);
 

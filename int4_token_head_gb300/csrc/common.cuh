@@ -91,8 +91,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Spins on the barrier's phase with an iteration limit; false if the limit
-// was reached (the caller reports it and stops issuing work).
-constexpr int kMaxWaitIters = 1 << 20;
+// was reached (the caller reports it and stops issuing work).  A failing
+// try_wait suspends the warp for a few microseconds (measured on GB300: 7.8 k
+// SM cycles), so the limit holds a stuck warp for about a second.
+constexpr int kMaxWaitIters = 1 << 18;
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   for (int n = 0; n < kMaxWaitIters; n++)
     if (mbar_try_wait(bar, parity)) return true;

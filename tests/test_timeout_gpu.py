@@ -13,7 +13,7 @@ from int4_token_head_gb300.paged import PagedKV
 from tests.helpers import assert_close_attention, oracle_attention, oracle_write_history_and_step
 
 pytestmark = pytest.mark.gpu
-KERNEL_LIMIT = 1 << 20  # attempts of the kernels' bounded waits
+KERNEL_LIMIT = 1 << 18  # attempts of the kernels' bounded waits
 
 
 def _wait(iterations):
@@ -34,7 +34,7 @@ def test_bounded_wait_reports_time_out_and_the_context_stays_usable():
     assert per_attempt * KERNEL_LIMIT / 1e9 < 10.0, per_attempt
     # the full limit itself: the wait ends, reports, and the stream moves on
     status, cycles, wall = _wait(KERNEL_LIMIT)
-    assert status == _lib.DEV_TIMEOUT and wall < 30.0
+    assert status == _lib.DEV_TIMEOUT and wall < 10.0
     print(f"bounded wait: {per_attempt:.0f} SM cycles per attempt; the kernels' limit "
           f"({KERNEL_LIMIT} attempts) held the warp {cycles} cycles, {wall * 1e3:.0f} ms wall")
     # a zero budget gives up at once (and says so)
