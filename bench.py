@@ -333,6 +333,11 @@ def prefill_kernel_name(d: int) -> str:
     return "prefill_ws_kernel" if d <= 192 else "prefill_kernel"
 
 
+def decode_kernel_name(d: int, int8: bool = False) -> str:
+    """INT4 head size 128 has its own decode entry point (128 registers a thread)."""
+    return "decode_kernel_i4d128" if d == 128 and not int8 else "decode_kernel"
+
+
 def int8_decode_bench(w, dev, iters: int):
     """The int8_per_token_head mode on this workload: a second cache (int8
     codes, no rotation) populated through kv_int8_write, then `iters`
@@ -365,7 +370,8 @@ def int8_decode_bench(w, dev, iters: int):
     step_ms = sum(kern[k][0] for k in ("prep", "prefill", "decode", "reduce")) / iters
     del pk
     torch.cuda.empty_cache()
-    return {"kernel": prefill_kernel_name(w.head_size) if dom == "prefill" else "decode_kernel", "ms": round(ms, 5),
+    return {"kernel": prefill_kernel_name(w.head_size) if dom == "prefill" else decode_kernel_name(w.head_size, True),
+            "ms": round(ms, 5),
             "attention_ms": round(step_ms, 5),
             "gbs": round(nbytes / (ms / 1e3) / 1e9, 1) if dom == "decode" else None,
             "cache_bytes_read": nbytes}
@@ -616,7 +622,7 @@ def run_ours(args):
         achieved = algo / launch_s / 1e9 if launch_s else None
         roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
-                    "traffic": recorded_traffic(dom, args.workload), "kernel": "decode_kernel",
+                    "traffic": recorded_traffic(dom, args.workload), "kernel": decode_kernel_name(d),
                     "peak_source": f"{peak_kind} (HBM copy)", "algorithmic_bytes_per_launch": algo}
     else:
         # a dense contraction: QK^T and PV over the visible (query, key) pairs

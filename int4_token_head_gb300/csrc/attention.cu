@@ -829,33 +829,39 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   // decode is sized for single-token queries and longer ones go to prefill.
   const bool any_decode = c.group <= kDecodeCols;
   int dec_occ = 0;
+  // the deeper decode ring serves the separate-scale layout (four heads per
+  // CTA); the in-slot layout's eight-head CTAs read better with the shallower
+  // one (measured on GB300: in-slot decode 2.20 vs 2.63 ms)
+  const bool dec_deep = !inslot && c.hg <= 4;
   if (any_decode) {
-    static bool attr_done[kMaxDevices][2] = {};
-    static int occ_cache[kMaxDevices][2][9] = {};
+    // one cache per kernel: (blocks per position, ring depth)
+    static bool attr_done[kMaxDevices][2][2] = {};
+    static int occ_cache[kMaxDevices][2][2][9] = {};
     auto occupancy = [&](auto kern, int np, int smem_max, int smem) -> int {
       if (smem > kMaxSmem) return 0;  // this ring does not fit
-      if (!attr_done[dev][np - 1]) {
+      if (!attr_done[dev][np - 1][dec_deep]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, min(smem_max, kMaxSmem)) !=
             cudaSuccess)
           return 0;
-        attr_done[dev][np - 1] = true;
+        attr_done[dev][np - 1][dec_deep] = true;
       }
-      if (!occ_cache[dev][np - 1][c.hg]) {
+      if (!occ_cache[dev][np - 1][dec_deep][c.hg]) {
         int o = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.hg * 32, smem) != cudaSuccess || o < 1) return 0;
-        occ_cache[dev][np - 1][c.hg] = o;
+        occ_cache[dev][np - 1][dec_deep][c.hg] = o;
       }
-      return occ_cache[dev][np - 1][c.hg];
+      return occ_cache[dev][np - 1][dec_deep][c.hg];
     };
-    const int occ1 = occupancy(decode_kernel<D, 1, FMT>, 1, DecGeom<D, 1, FMT>::smem_bytes(8), DecGeom<D, 1, FMT>::smem_bytes(c.hg));
+    using E1 = DecodeEntry<D, 1, FMT>;
+    using E2 = DecodeEntry<D, 2, FMT>;
+    const int occ1 = occupancy(E1::kernel(dec_deep), 1, E1::smem(dec_deep, 8), E1::smem(dec_deep, c.hg));
     if (occ1 < 1) return KV_INT4_ERR_CUDA;
     const long long mq = (long long)(a.max_query_len > 0 ? a.max_query_len : 1) * c.group;
     const long long cols = mq <= kDecodeCols ? mq : c.group;
     c.np = 1;
     dec_occ = occ1;
     if (cols <= kDecodeCols / 2) {
-      const int occ2 =
-          occupancy(decode_kernel<D, 2, FMT>, 2, DecGeom<D, 2, FMT>::smem_bytes(8), DecGeom<D, 2, FMT>::smem_bytes(c.hg));
+      const int occ2 = occupancy(E2::kernel(dec_deep), 2, E2::smem(dec_deep, 8), E2::smem(dec_deep, c.hg));
       if (occ2 >= 1 && occ2 >= occ1) {  // 0: the paired ring does not fit
         c.np = 2;
         dec_occ = occ2;
@@ -914,10 +920,10 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     const int threads = c.hg * 32;
     timing_begin(kTimedDecode, stream);
     if (c.np == 2)
-      decode_kernel<D, 2, FMT><<<(unsigned)grid, threads, DecGeom<D, 2, FMT>::smem_bytes(c.hg), stream>>>(
+      DecodeEntry<D, 2, FMT>::kernel(dec_deep)<<<(unsigned)grid, threads, DecodeEntry<D, 2, FMT>::smem(dec_deep, c.hg), stream>>>(
           DecParams{c, pv, num_ctas});
     else
-      decode_kernel<D, 1, FMT><<<(unsigned)grid, threads, DecGeom<D, 1, FMT>::smem_bytes(c.hg), stream>>>(
+      DecodeEntry<D, 1, FMT>::kernel(dec_deep)<<<(unsigned)grid, threads, DecodeEntry<D, 1, FMT>::smem(dec_deep, c.hg), stream>>>(
           DecParams{c, pv, num_ctas});
     timing_end(kTimedDecode, stream);
     if (cudaGetLastError() != cudaSuccess) return KV_INT4_ERR_CUDA;

@@ -13,17 +13,24 @@
 // one softmax pass, one barrier and one V offset correction serve NP blocks.
 // Each column keeps its own running (m, l, o'); the reduce kernel merges the
 // NP columns of a query with the log-sum-exp rule like any other split.
-template <int D, int NP, int FMT>
+template <int D, int NP, int FMT, bool DEEP = false>
 struct DecGeom {
   static constexpr int COLS = kDecodeCols / NP;  // query columns per block
-  // ring of single-block slots: NP consumed per iteration, the rest in flight
-  static constexpr int NS = NP == 1 ? 4 : 2 * NP + 1;
-  static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
   static constexpr int CB = FMT == kFmtInt8 ? D : D / 2;  // code bytes per head vector
+  // 64-byte code rows: V rows unpadded, 16-byte chunk c of row r stored at
+  // chunk c ^ ((r >> 1) & 3), which spreads an ldmatrix piece's 8 rows over
+  // all bank groups; other sizes pad the V row instead
+  static constexpr bool VSWZ = CB == 64;
+  // ring of single-block slots: NP consumed per iteration, the rest in
+  // flight.  The copies in flight per SM set the decode's pace; DEEP (four
+  // heads per CTA, four CTAs per SM) takes one more slot, which the smaller
+  // swizzled slots leave room for
+  static constexpr int NS = NP == 1 ? 4 : 2 * NP + (VSWZ && DEEP ? 2 : 1);
+  static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
   static constexpr int KROW = CB;           // K tile row stride (bytes)
   // V tile row stride: an odd multiple of 16 bytes, so that the 8 rows of
-  // an ldmatrix piece fall in distinct bank groups
-  static constexpr int VROW = (CB / 16) % 2 ? CB : CB + 16;
+  // an ldmatrix piece fall in distinct bank groups (or swizzled, above)
+  static constexpr int VROW = VSWZ || (CB / 16) % 2 ? CB : CB + 16;
   static constexpr int KTILE = 16 * KROW;
   static constexpr int VTILE = 16 * VROW;
   // one head's K and V codes of one block, padded to 64 mod 128 bytes so that
@@ -125,9 +132,10 @@ __device__ __forceinline__ void pv_mma_chunk(float (&oacc)[D / 16][4], int ch, u
 }
 
 // vaddr: shared address of this lane's ldmatrix row in chunk pair 0 (lane l
-// addresses key 8 ((l >> 3) & 1) + (l & 7) of chunk (l >> 4))
+// addresses key 8 ((l >> 3) & 1) + (l & 7) of chunk (l >> 4)); chunk pair p
+// is at vaddr + p * vstep (32 in a padded tile, +-32 by row in a swizzled one)
 template <int D, bool CORR, int FMT>
-__device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], uint32_t vaddr, uint32_t b0, uint32_t b1,
+__device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], uint32_t vaddr, int vstep, uint32_t b0, uint32_t b1,
                                         const uint32_t (&vcorr)[4]) {
   constexpr int CH = (FMT == kFmtInt8 ? D : D / 2) / 16;  // 16-byte chunks per V row
 #pragma unroll
@@ -135,7 +143,7 @@ __device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], uint32_t vaddr
     uint32_t r[4];
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(vaddr + p * 32));
+                 : "r"(vaddr + p * vstep));
     pv_mma_chunk<D, CORR, FMT>(oacc, 2 * p, r[0], r[1], b0, b1, vcorr);
     pv_mma_chunk<D, CORR, FMT>(oacc, 2 * p + 1, r[2], r[3], b0, b1, vcorr);
   }
@@ -143,7 +151,7 @@ __device__ __forceinline__ void pv_mmas(float (&oacc)[D / 16][4], uint32_t vaddr
     uint32_t r[2];
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
                  : "=r"(r[0]), "=r"(r[1])
-                 : "r"(vaddr + (CH / 2) * 32));
+                 : "r"(vaddr + (CH / 2) * vstep));
     pv_mma_chunk<D, CORR, FMT>(oacc, CH - 1, r[0], r[1], b0, b1, vcorr);
   }
 }
@@ -174,9 +182,9 @@ struct DecParams {
 // removes that position's offset, so the running accumulator only ever holds
 // one block's worth of offset per column (accumulating the offset over
 // thousands of keys would cost the fp32 accumulator the signal's low bits).
-template <int D, int NP, int FMT>
-__global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
-  using G = DecGeom<D, NP, FMT>;
+template <int D, int NP, int FMT, bool DEEP>
+__device__ __forceinline__ void decode_body(const DecParams& prm) {
+  using G = DecGeom<D, NP, FMT, DEEP>;
   constexpr bool I8 = FMT == kFmtInt8;
   const Common& c = prm.c;
   const PlanView& pv = prm.pv;
@@ -231,7 +239,8 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
     const int h = rest % HG;
     const int kvr = rest / HG;
     const int kv = kvr / 16, r = kvr % 16;
-    c_saddr[j] = smem_addr(smem) + h * G::HTILE + (kv ? G::KTILE + r * G::VROW : r * G::KROW) + col * 16;
+    const int vcol = G::VSWZ ? col ^ ((r >> 1) & 3) : col;
+    c_saddr[j] = smem_addr(smem) + h * G::HTILE + (kv ? G::KTILE + r * G::VROW + vcol * 16 : r * G::KROW + col * 16);
     c_src[j] = (kv ? c.v_cache : c.k_cache) + r * c.geo.crow + (long long)h * c.geo.chead + col * 16;
   }
   // one 4-byte scale per thread: [K/V][row][h]
@@ -409,8 +418,10 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   const int jb = (cq * NP) >> 2;  // block of this thread's score columns 2cq, 2cq+1
   const int jv = (g * NP) >> 3;   // block of this lane's P'^T column g
   // this lane's ldmatrix row of the V tile in slot 0
-  const uint32_t v_lane = smem_addr(smem) + hl * G::HTILE + G::KTILE +
-                          (((lane >> 3) & 1) * 8 + (lane & 7)) * G::VROW + (lane >> 4) * 16;
+  const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7), vx = G::VSWZ ? (vrow >> 1) & 3 : 0;
+  const uint32_t v_lane =
+      smem_addr(smem) + hl * G::HTILE + G::KTILE + vrow * G::VROW + (((lane >> 4) ^ (vx & 1)) + 2 * (vx >> 1)) * 16;
+  const int vstep = vx >> 1 ? -32 : 32;
   int cs = 0;                     // slot of the iteration's first block
   const int nunits = (int)(P1 - P0);
   // INT4: rows g (even d: offset 1032) and g + 8 (odd d: offset 1152); int8: 1152
@@ -531,13 +542,13 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
 
     // ---- O'^T += V^T P'^T (offset removed per position) ----
     if constexpr (NP == 1) {
-      pv_mmas<D, true, FMT>(oacc, v_lane + slot[0] * SB, b0, b1, vcorr);
+      pv_mmas<D, true, FMT>(oacc, v_lane + slot[0] * SB, vstep, b0, b1, vcorr);
     } else {
 #pragma unroll
       for (int j = 0; j < NP; j++) {
         // block j's probabilities only: the other blocks' columns are zero
         const uint32_t bj0 = jv == j ? b0 : 0u, bj1 = jv == j ? b1 : 0u;
-        pv_mmas<D, false, FMT>(oacc, v_lane + slot[j] * SB, bj0, bj1, vcorr);
+        pv_mmas<D, false, FMT>(oacc, v_lane + slot[j] * SB, vstep, bj0, bj1, vcorr);
       }
 #pragma unroll
       for (int i = 0; i < G::KSTEPS; i++) mma_16816(oacc[i], vcorr, b0, b1);
@@ -558,3 +569,33 @@ __global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
   }
   cp_async_wait<0>();
 }
+
+template <int D, int NP, int FMT>
+__global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
+  decode_body<D, NP, FMT, false>(prm);
+}
+// INT4 head size 128 (the long-context shape): at most 128 registers a
+// thread, so that four 4-warp CTAs (or two 8-warp ones) share an SM
+template <int NP, bool DEEP>
+__global__ void __launch_bounds__(256, 2) decode_kernel_i4d128(DecParams prm) {
+  decode_body<128, NP, kFmtInt4, DEEP>(prm);
+}
+// The decode kernel for a format and head size, with the deeper ring where
+// it has one (`deep`), and its dynamic shared memory for hg heads per CTA.
+template <int D, int NP, int FMT>
+struct DecodeEntry {
+  static constexpr bool HAS_DEEP = FMT == kFmtInt4 && D == 128 && DecGeom<D, NP, FMT, true>::NS != DecGeom<D, NP, FMT>::NS;
+  static void (*kernel(bool deep))(DecParams) {
+    if constexpr (FMT == kFmtInt4 && D == 128) {
+      if constexpr (HAS_DEEP) {
+        if (deep) return decode_kernel_i4d128<NP, true>;
+      }
+      return decode_kernel_i4d128<NP, false>;
+    } else {
+      return decode_kernel<D, NP, FMT>;
+    }
+  }
+  static int smem(bool deep, int hg) {
+    return deep && HAS_DEEP ? DecGeom<D, NP, FMT, true>::smem_bytes(hg) : DecGeom<D, NP, FMT>::smem_bytes(hg);
+  }
+};
