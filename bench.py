@@ -127,6 +127,9 @@ def decode_columns(w) -> int:
     return 4 if cols <= 4 else 8
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context only; `peak` is the measured copy)
+
+
 def source_sha(paths) -> str:
     """First 16 hex digits of the SHA-256 of the files' bytes, in order."""
     h = hashlib.sha256()
@@ -623,7 +626,9 @@ def run_ours(args):
         roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
                     "traffic": recorded_traffic(dom, args.workload), "kernel": decode_kernel_name(d),
-                    "peak_source": f"{peak_kind} (HBM copy)", "algorithmic_bytes_per_launch": algo}
+                    "peak_source": f"{peak_kind} (HBM copy)", "algorithmic_bytes_per_launch": algo,
+                    "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4) if achieved else None,
+                    "nominal_peak": NOMINAL_HBM_GBS}
     else:
         # a dense contraction: QK^T and PV over the visible (query, key) pairs
         seqs = [(ql, kv) for ql, kv in w.seqs if not is_dec(ql)]
