@@ -85,3 +85,26 @@ def test_clock_sampler_parses_nvidia_smi_lines():
                "garbage"]
     c = s.stop()
     assert c["sm_mhz"] == 1925 and c["sm_max_mhz"] == 2070 and c["reasons"] == ["sw_power_cap"]
+
+
+def test_kernel_names_and_recorded_traffic():
+    # the bench names the kernel it times: INT4 head size 128 has its own entry point
+    assert bench.decode_kernel_name(128) == "decode_kernel_i4d128"
+    assert bench.decode_kernel_name(128, int8=True) == "decode_kernel"
+    assert bench.decode_kernel_name(96) == "decode_kernel"
+    assert bench.prefill_kernel_name(192) == "prefill_ws_kernel"
+    assert bench.prefill_kernel_name(256) == "prefill_kernel"
+    # a committed traffic record is reported only for the sources it was taken on
+    rec = bench.recorded_traffic("decode", "long")
+    assert rec is None or rec > 9.0e9
+    assert bench.recorded_traffic("decode", "no-such-workload") is None
+
+
+def test_source_sha_depends_on_every_file(tmp_path):
+    a, b = tmp_path / "a.cuh", tmp_path / "b.cuh"
+    a.write_bytes(b"one")
+    b.write_bytes(b"two")
+    h = bench.source_sha([str(a), str(b)])
+    assert len(h) == 16 and h != bench.source_sha([str(a)])
+    b.write_bytes(b"three")
+    assert bench.source_sha([str(a), str(b)]) != h
