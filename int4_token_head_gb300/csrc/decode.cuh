@@ -23,8 +23,9 @@ struct DecGeom {
   static constexpr bool VSWZ = CB == 64;
   // ring of single-block slots: NP consumed per iteration, the rest in
   // flight.  The copies in flight per SM set the decode's pace; DEEP (four
-  // heads per CTA, four CTAs per SM) takes one more slot, which the smaller
-  // swizzled slots leave room for
+  // heads per CTA, four CTAs per SM, separate 16-byte aligned scales) takes
+  // one more slot, which the smaller swizzled slots leave room for, and
+  // stages a block's scales as 16-byte rows of the group's four heads
   static constexpr int NS = NP == 1 ? 4 : 2 * NP + (VSWZ && DEEP ? 2 : 1);
   static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
   static constexpr int KROW = CB;           // K tile row stride (bytes)
@@ -243,10 +244,12 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
     c_saddr[j] = smem_addr(smem) + h * G::HTILE + (kv ? G::KTILE + r * G::VROW + vcol * 16 : r * G::KROW + col * 16);
     c_src[j] = (kv ? c.v_cache : c.k_cache) + r * c.geo.crow + (long long)h * c.geo.chead + col * 16;
   }
-  // one 4-byte scale per thread: [K/V][row][h]
-  const int s_kv = tid / (16 * HG), s_rem = tid % (16 * HG);
-  const int s_r = s_rem / HG, s_h = s_rem % HG;
-  const uint32_t s_saddr = smem_addr(smem) + HG * G::HTILE + (s_kv * HG + s_h) * 64 + s_r * 4;
+  // scales: DEEP (four heads) one 16-byte row [K/V][row][h] for each of
+  // threads 0..31, else one 4-byte scale [K/V][h][row] per thread
+  const int s_kv = DEEP ? tid >> 4 : tid / (16 * HG), s_rem = DEEP ? tid & 15 : tid % (16 * HG);
+  const int s_r = DEEP ? s_rem : s_rem / HG, s_h = DEEP ? 0 : s_rem % HG;
+  const uint32_t s_saddr = smem_addr(smem) + HG * G::HTILE +
+                           (DEEP ? (s_kv * 16 + s_r) * 16 : (s_kv * HG + s_h) * 64 + s_r * 4);
   const float* s_src = (s_kv ? c.v_scale : c.k_scale) + s_r * c.geo.srow + (long long)s_h * c.geo.shead;
   const uint64_t blk_bytes = (uint64_t)c.geo.cblk, blk_scales = (uint64_t)c.geo.sblk;
 
@@ -267,7 +270,11 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(c_saddr[j] + soff), "l"(src));
       }
       const float* ssrc = s_src + (uint64_t)(uint32_t)blk * blk_scales + (uint64_t)(grp * HG) * c.geo.shead;
-      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s_saddr + soff), "l"(ssrc));
+      if constexpr (DEEP) {
+        if (tid < 32) asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s_saddr + soff), "l"(ssrc));
+      } else {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s_saddr + soff), "l"(ssrc));
+      }
     }
     if (tid == 0) {
       sflag[slot] = ok;
@@ -447,8 +454,9 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
     }
     const uint8_t* mstg = smem + my * SB;
     const bool bok = sflag[my] != 0;
-    const float* sks = reinterpret_cast<const float*>(mstg + HG * G::HTILE + hl * 64);
-    const float* svs = reinterpret_cast<const float*>(mstg + HG * G::HTILE + (HG + hl) * 64);
+    const float* sks = reinterpret_cast<const float*>(mstg + HG * G::HTILE + (DEEP ? hl * 4 : hl * 64));
+    const float* svs = reinterpret_cast<const float*>(mstg + HG * G::HTILE + (DEEP ? 256 + hl * 4 : (HG + hl) * 64));
+    constexpr int SR = DEEP ? 4 : 1;  // scale stride between rows (floats)
 
     // ---- S^T = K Q'^T (biased, x16), one accumulator per block ----
     float sacc[NP][4];
@@ -485,7 +493,7 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
     const int kb0 = cw.fb + cw.kp * NP;
     const int pos0 = (kb0 + jb) * 16 + g, pos1 = pos0 + 8;
     // INT4 scores carry the factor 16 of q' at the low-nibble positions
-    const float ks0 = sks[g] * (I8 ? 1.f : 0.0625f), ks1 = sks[g + 8] * (I8 ? 1.f : 0.0625f);
+    const float ks0 = sks[g * SR] * (I8 ? 1.f : 0.0625f), ks1 = sks[(g + 8) * SR] * (I8 ? 1.f : 0.0625f);
     float s00 = (sa[0] - bias0) * ks0, s01 = (sa[1] - bias1) * ks0;
     float s10 = (sa[2] - bias0) * ks1, s11 = (sa[3] - bias1) * ks1;
     // keys outside a column's visible range [lo, lim) (or in an invalid or
@@ -528,7 +536,7 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
     const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
     l0 += p00 + p10;
     l1 += p01 + p11;
-    const float vs0 = svs[g], vs1 = svs[g + 8];
+    const float vs0 = svs[g * SR], vs1 = svs[(g + 8) * SR];
     float q00 = p00 * vs0, q01 = p01 * vs0, q10 = p10 * vs1, q11 = p11 * vs1;
     if (!full) {  // masked keys may carry unwritten (NaN) scales: select, do not multiply
       q00 = s00 == -INFINITY ? 0.f : q00;
