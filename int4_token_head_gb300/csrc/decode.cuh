@@ -40,7 +40,7 @@ struct DecGeom {
   static constexpr int KW = CB / 16;    // K words per row per thread (quarter row)
   static constexpr int KSTEPS = D / 16; // MMA k-steps of a block's K (and m-tiles of its V)
   static constexpr int CHR = CB / 16;   // 16-byte chunks per code row
-  // per slot: hg head tiles, then scales [K/V][hg][16]
+  // per slot: hg head tiles, then scales [K/V][hg][16] ([K/V][16][hg] with DEEP)
   __host__ __device__ static constexpr int slot_bytes(int hg) { return hg * (HTILE + 128); }
   __host__ __device__ static constexpr int smem_bytes(int hg) { return NS * slot_bytes(hg) + 32; }
   static_assert(HTILE % 16 == 0, "tile alignment");
@@ -588,8 +588,9 @@ template <int NP, bool DEEP>
 __global__ void __launch_bounds__(256, 2) decode_kernel_i4d128(DecParams prm) {
   decode_body<128, NP, kFmtInt4, DEEP>(prm);
 }
-// The decode kernel for a format and head size, with the deeper ring where
-// it has one (`deep`), and its dynamic shared memory for hg heads per CTA.
+// The decode kernel for a format and head size, with the deeper ring and the
+// 16-byte scale rows where it has them (`deep`), and its dynamic shared
+// memory for hg heads per CTA.
 template <int D, int NP, int FMT>
 struct DecodeEntry {
   static constexpr bool HAS_DEEP = FMT == kFmtInt4 && D == 128 && DecGeom<D, NP, FMT, true>::NS != DecGeom<D, NP, FMT>::NS;
