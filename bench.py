@@ -12,15 +12,18 @@ needed between steps).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-prints one JSON line.  Under torchrun (N > 1) every rank runs its own
-replica of the workload (weak scaling, no collective on the data path); the
-timed region is bracketed by a barrier and synchronize on every rank and
-the slowest rank's time is used.
+prints one JSON line.  With N > 1 every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); the timed region is
+bracketed by a barrier and synchronize on every rank and the slowest rank's
+time is used.  Launched without torchrun, `--gpus N` re-runs this script
+under torch.distributed.run with N ranks on this node.
 
 --impl reference times the fp64 CPU oracle on the host cores (rank 0 only)
-on a bounded sample of the same workload: each step is the oracle's write of
-one new token plus its attention for one (sequence, kv head) unit of the
-batch, i.e. 1/num_kv_heads of a decode token.
+on a bounded sample of the same workload: one process per host core, and in
+each step every process does one unit step, the oracle's write of one new
+token plus its attention for one (sequence, kv head) unit of the batch (a
+unit is 1/num_kv_heads of a decode token).  The CPU baseline of our arm is
+the same runner for --cpu-seconds.
 """
 
 from __future__ import annotations
@@ -449,45 +452,149 @@ def inslot_bench(w, dev, pk, q, out, n_chunks: int, iters: int, chunk_tokens: in
 # ---------------------------------------------------------------------------
 # the oracle on host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
-class OracleUnits:
-    """A pool of (sequence, kv head) units of the workload, each with its own
-    oracle-written cache; a step is the oracle's write of the unit's new
-    token plus its attention for the unit's q heads."""
+def _unit_picks(w, n_units: int):
+    """n_units (sequence, kv head) units spread evenly over the batch."""
+    order = [(s, h) for s in range(w.num_seqs) for h in range(w.num_kv_heads)]
+    stride = max(1, len(order) // max(1, n_units))
+    return order[::stride][:n_units]
 
-    def __init__(self, w, n_units: int, gen_device: str):
-        import numpy as np
-        from oracle import kvint4_oracle as O
-        self.O, self.np = O, np
-        self.w = w
-        self.units = []
-        q_all = w.queries(gen_device).float().cpu().numpy()
+
+def _oracle_proc(rank, name, batch, picks, seconds, fixed_steps, warmup, chunk_tokens, gate, results):
+    """One host process of the CPU oracle runner (spawned; never touches a GPU).
+
+    Set-up (untimed): the oracle writes the history of its (sequence, kv
+    head) units into caches of their own.  Timed, after every process has
+    reached the gate: unit steps, each the oracle's write of the unit's new
+    token plus its attention for the unit's q heads (fixed_steps of them, or
+    as many as fit in `seconds`), then, after the gate again, the oracle's
+    write of this process's share of one chunk of new tokens."""
+    import numpy as np
+    import torch
+    torch.set_num_threads(1)
+    from int4_token_head_gb300 import synthetic
+    from oracle import kvint4_oracle as O
+    try:
+        overrides = {"batch": batch} if batch else {}
+        w = synthetic.make_workload(name, **overrides)
+        signs = w.signs.numpy()
+        bs, d, hkv = w.block_size, w.head_size, w.num_kv_heads
+        q_all = w.queries("cpu").float().numpy()
         qsl = w.query_start_loc.numpy()
-        order = [(s, h) for s in range(w.num_seqs) for h in range(w.num_kv_heads)]
-        stride = max(1, len(order) // max(1, n_units))
-        picks = order[::stride][:n_units]
+        units = []
+        drawn = {}
         for s, h in picks:
             ql, L = w.seqs[s]
-            k, v = w.seq_kv(s, gen_device)
-            k = k[:, h:h + 1].float().cpu().numpy()
-            v = v[:, h:h + 1].float().cpu().numpy()
-            nblk = (L + w.block_size - 1) // w.block_size
-            kc = np.full((nblk, w.block_size, 1, w.head_size // 2), 0xA5, np.uint8)
+            if s not in drawn:
+                drawn.clear()
+                k, v = w.seq_kv(s, "cpu")
+                drawn[s] = (k.float().numpy(), v.float().numpy())
+            k, v = drawn[s]
+            k, v = k[:, h:h + 1], v[:, h:h + 1]
+            nblk = (L + bs - 1) // bs
+            kc = np.full((nblk, bs, 1, d // 2), 0xA5, np.uint8)
             vc = kc.copy()
-            ks = np.full((nblk, w.block_size, 1), np.nan, np.float32)
+            ks = np.full((nblk, bs, 1), np.nan, np.float32)
             vs = ks.copy()
-            O.write_cache(k[:L - ql], v[:L - ql], np.arange(L - ql), kc, vc, ks, vs, w.block_size,
-                          w.signs.numpy())
+            O.write_cache(k[:L - ql], v[:L - ql], np.arange(L - ql), kc, vc, ks, vs, bs, signs)
             q = q_all[qsl[s]:qsl[s + 1], h * w.group:(h + 1) * w.group]
-            self.units.append(dict(k_new=k[L - ql:], v_new=v[L - ql:], slots=np.arange(L - ql, L),
-                                   caches=(kc, vc, ks, vs), q=q, L=L, ql=ql, nblk=nblk))
+            units.append((k[L - ql:].copy(), v[L - ql:].copy(), np.arange(L - ql, L), (kc, vc, ks, vs), q, L, ql,
+                          nblk))
+        drawn.clear()
+        scale = 1.0 / math.sqrt(d)
 
-    def step(self, i: int):
-        u = self.units[i % len(self.units)]
-        O, np, w = self.O, self.np, self.w
-        kc, vc, ks, vs = u["caches"]
-        O.write_cache(u["k_new"], u["v_new"], u["slots"], kc, vc, ks, vs, w.block_size, w.signs.numpy())
-        return O.attention_seq(u["q"], kc, vc, ks, vs, np.arange(u["nblk"])[None], [u["L"]], [0, u["ql"]], 0, 1,
-                               w.block_size, 1.0 / math.sqrt(w.head_size), w.causal, w.signs.numpy())
+        def step(i):
+            k_new, v_new, slots, (kc, vc, ks, vs), q, L, ql, nblk = units[i % len(units)]
+            O.write_cache(k_new, v_new, slots, kc, vc, ks, vs, bs, signs)
+            O.attention_seq(q, kc, vc, ks, vs, np.arange(nblk)[None], [L], [0, ql], 0, 1, bs, scale, w.causal, signs)
+
+        for i in range(warmup):
+            step(i)
+        # this process's share of one write chunk: bf16-representable N(0, 1) K/V, random slots
+        rng = np.random.default_rng(1000 + rank)
+        ck = rng.standard_normal((chunk_tokens, hkv, d)).astype(np.float32)
+        cv = rng.standard_normal((chunk_tokens, hkv, d)).astype(np.float32)
+        ck = (ck.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
+        cv = (cv.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
+        nb = max(1, (chunk_tokens + bs - 1) // bs)
+        cache = [np.zeros((nb, bs, hkv, d // 2), np.uint8), np.zeros((nb, bs, hkv, d // 2), np.uint8),
+                 np.zeros((nb, bs, hkv), np.float32), np.zeros((nb, bs, hkv), np.float32)]
+        cslots = rng.permutation(nb * bs)[:chunk_tokens]
+        gate.wait()
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            step(n)
+            n += 1
+            if fixed_steps is not None:
+                if n >= fixed_steps:
+                    break
+            elif time.perf_counter() - t0 >= seconds:
+                break
+        t1 = time.perf_counter()
+        gate.wait()
+        t2 = time.perf_counter()
+        if chunk_tokens:
+            O.write_cache(ck, cv, cslots, *cache, bs, signs)
+        t3 = time.perf_counter()
+        results.put((rank, n, t0, t1, t2, t3, None))
+    except Exception as e:  # reported by the parent
+        try:
+            gate.abort()
+        except Exception:
+            pass
+        results.put((rank, 0, 0.0, 0.0, 0.0, 0.0, repr(e)))
+
+
+def run_oracle_on_host(name, batch, processes, units_per_process, seconds=0.0, fixed_steps=None, warmup=1,
+                       chunk_tokens=65536):
+    """Time the fp64 oracle on `processes` host processes at once (one BLAS
+    thread each; spawned, so safe after CUDA is initialised).  Returns the
+    unit steps and their wall time (first start to last end), their
+    throughput in decode tokens/s (a (sequence, kv head) unit is 1/Hkv of a
+    decode token), and the write of one chunk of chunk_tokens tokens split
+    evenly over the processes, with its wall time and GB/s."""
+    import multiprocessing as mp
+    from int4_token_head_gb300 import synthetic
+    overrides = {"batch": batch} if batch else {}
+    w = synthetic.make_workload(name, **overrides)
+    picks = _unit_picks(w, processes * units_per_process)
+    processes = max(1, min(processes, len(picks)))
+    per = [picks[r::processes] for r in range(processes)]
+    share = [chunk_tokens // processes + (1 if r < chunk_tokens % processes else 0) for r in range(processes)]
+    ctx = mp.get_context("spawn")
+    gate = ctx.Barrier(processes)
+    results = ctx.Queue()
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    os.environ.update({k: "1" for k in keys})
+    try:
+        procs = [ctx.Process(target=_oracle_proc, args=(r, name, batch, per[r], seconds, fixed_steps, warmup,
+                                                        share[r], gate, results), daemon=True)
+                 for r in range(processes)]
+        for p in procs:
+            p.start()
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    out = [results.get(timeout=1800) for _ in range(processes)]
+    for p in procs:
+        p.join(60)
+    errs = [o[6] for o in out if o[6]]
+    if errs:
+        raise RuntimeError(f"oracle process failed: {errs[0]}")
+    steps = sum(o[1] for o in out)
+    wall = max(o[3] for o in out) - min(o[2] for o in out)
+    wwall = max(o[5] for o in out) - min(o[4] for o in out)
+    d, hkv = w.head_size, w.num_kv_heads
+    wbytes = chunk_tokens * (2 * hkv * d * 2 + 2 * hkv * (d // 2 + 4) + 8)
+    return {"w": w, "processes": processes, "units": len(picks), "unit_steps": steps, "wall_s": wall,
+            "steps_per_process": min(o[1] for o in out),
+            "tokens_per_s": steps / hkv / wall, "total_units": w.num_seqs * hkv,
+            "write_chunk": {"tokens": chunk_tokens, "s": round(wwall, 3),
+                            "gbs": round(wbytes / wwall / 1e9, 4) if wwall > 0 else None}}
 
 
 def host_cores() -> int:
@@ -497,25 +604,16 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def time_oracle(w, gen_device, max_seconds: float, min_steps: int = 3, fixed_steps=None, warmup: int = 1,
-                n_units: int = 2):
-    pool = OracleUnits(w, n_units, gen_device)
-    for i in range(warmup):
-        pool.step(i)
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        pool.step(n)
-        n += 1
-        el = time.perf_counter() - t0
-        if fixed_steps is not None:
-            if n >= fixed_steps:
-                break
-        elif n >= min_steps and el >= max_seconds:
-            break
-    el = time.perf_counter() - t0
-    tokens = n / w.num_kv_heads
-    return tokens / el, n, el, pool
+def oracle_sample_text(r) -> str:
+    w = r["w"]
+    step_s = r["total_units"] / (r["unit_steps"] / r["wall_s"])
+    return (f"{r['processes']} processes at once (one per host core, 1 BLAS thread each) on {r['units']} of the "
+            f"{r['total_units']} (sequence, kv head) units of this batch; a unit step is the oracle's write of the "
+            f"unit's new token + attention for its {w.group} q heads over up to {w.max_seq_len} keys (1 unit = "
+            f"1/{w.num_kv_heads} decode token); {r['unit_steps']} unit steps in {r['wall_s']:.1f} s, so one whole "
+            f"step ({r['total_units']} units) would take {step_s:.1f} s; the write of one "
+            f"{r['write_chunk']['tokens']}-token chunk took {r['write_chunk']['s']} s = "
+            f"{r['write_chunk']['gbs']} GB/s")
 
 
 # ---------------------------------------------------------------------------
@@ -661,11 +759,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int4 codes, f16 mma / f32 accumulate, f32 rotation",
         "data": "synthetic (seeded N(0,1) bf16 K/V/Q; no dataset or weights)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-                   "global_batch": w.num_seqs * world, "seq_len": w.max_seq_len,
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "l2": "inputs larger than L2 (cache %.2f GB), no flush" % (
-                       (pk.k_cache.numel() * 2 + pk.k_scale.numel() * 8) / 1e9)},
+        "config": bench_config(args, w, world),
         "roofline": roofline,
         "kv_read_gbs": round(attn_bytes / (attn_ms / 1e3) / 1e9, 1) if attn_ms else None,
         "write": write_info,
@@ -679,11 +773,11 @@ def run_ours(args):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, n, el, _ = time_oracle(w, str(dev), max_seconds=args.cpu_seconds)
-        result["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                                  "sample": f"{n} (sequence, kv head) units of this batch, each the oracle's "
-                                            f"write of one new token + attention for its {w.group} q heads "
-                                            f"over {w.max_seq_len} keys; {el:.1f} s; 1 unit = 1/{w.num_kv_heads} token"}
+        r = run_oracle_on_host(args.workload, args.batch, host_cores(), units_per_process=2,
+                               seconds=args.cpu_seconds, warmup=1)
+        result["cpu_baseline"] = {"value": round(r["tokens_per_s"], 3), "unit": UNIT, "cores": r["processes"],
+                                  "kind": "oracle", "sample": oracle_sample_text(r),
+                                  "write_chunk_gbs": r["write_chunk"]["gbs"]}
     if rank == 0:
         print(json.dumps(result), flush=True)
 
@@ -692,29 +786,55 @@ def run_ours(args):
 # reference arm: the oracle on host cores
 # ---------------------------------------------------------------------------
 def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores (rank 0 only),
+    each step one unit step (write of a new token + attention of one
+    (sequence, kv head) unit) in every host process at once."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import torch
-    from int4_token_head_gb300 import synthetic
-    overrides = {"batch": args.batch} if args.batch else {}
-    w = synthetic.make_workload(args.workload, **overrides)
-    gen = "cuda" if torch.cuda.is_available() else "cpu"
-    v, n, el, _ = time_oracle(w, gen, max_seconds=0, fixed_steps=args.steps, warmup=args.warmup, n_units=4)
+    r = run_oracle_on_host(args.workload, args.batch, host_cores(), units_per_process=1, fixed_steps=args.steps,
+                           warmup=args.warmup)
+    w = r["w"]
+    v = r["tokens_per_s"]
     result = {
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / n * 1e3, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["wall_s"] / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 K/V/Q; no dataset or weights)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-                   "global_batch": w.num_seqs, "seq_len": w.max_seq_len, "parallelism": "host cores"},
-        "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                         "sample": f"each step: the oracle's write of one new token + attention for one "
-                                   f"(sequence, kv head) unit ({w.group} q heads over {w.max_seq_len} keys), "
-                                   f"cycling over 4 units; 1 unit = 1/{w.num_kv_heads} token"},
+        "config": bench_config(args, w, world),
+        "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": r["processes"], "kind": "oracle",
+                         "sample": oracle_sample_text(r), "write_chunk_gbs": r["write_chunk"]["gbs"]},
         "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(result), flush=True)
+
+
+def bench_config(args, w, world):
+    """The workload description both arms print (identical for the same arguments)."""
+    cache_gb = w.num_blocks * w.block_size * w.num_kv_heads * (w.head_size + 8) / 1e9
+    return {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+            "global_batch": w.num_seqs * world, "seq_len": w.max_seq_len,
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "collectives": "none on the data path (replicas; a barrier and a max over ranks around the timing)",
+            "l2": "inputs larger than L2 (cache %.2f GB), no flush" % cache_gb}
+
+
+def launch_replicas(n: int, argv) -> int:
+    """`--gpus N` without a surrounding launcher: run this script under
+    torch.distributed.run with N ranks on this node (one replica per GPU)."""
+    import socket
+    if "--impl" not in argv or argv[argv.index("--impl") + 1] != "reference":
+        import torch
+        if torch.cuda.device_count() < n:
+            print(f"bench.py --gpus {n} needs {n} visible GPUs; {torch.cuda.device_count()} found", file=sys.stderr)
+            return 2
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
 
 
 def main(argv=None):
@@ -728,7 +848,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--write-chunks", type=int, default=16, help="65,536-token chunks in the bulk write measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    argv = list(sys.argv[1:] if argv is None else argv)
     args = ap.parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus, argv))
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

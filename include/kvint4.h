@@ -8,7 +8,12 @@
  *   says otherwise.  The library allocates no device memory, keeps no
  *   per-call state and never synchronises the device; each call only enqueues
  *   kernels on `stream` (a cudaStream_t passed as void*; NULL is the legacy
- *   default stream) and returns.  Calls are thread-safe.
+ *   default stream) and returns.  Calls are thread-safe: host threads may
+ *   call any entry point concurrently (the launch configuration each kernel
+ *   needs is computed once per device and CUDA context, under a lock, and
+ *   again after a cudaDeviceReset).  The one exception is
+ *   kv_int4_attention_noalloc, whose calls share a device array and must not
+ *   overlap on the GPU (see its note).
  * - "bf16" arguments are arrays of IEEE bfloat16 (2 bytes per element).
  * - A head vector has `head_size` = d elements; b = d & -d is the largest
  *   power-of-two divisor of d and n = d / b.  Supported head sizes: 64, 96,
@@ -52,7 +57,9 @@ extern "C" {
 #define KV_INT4_ERR_HEADS 3         /* num_q_heads % num_kv_heads != 0, a head count <= 0, or a group
                                        (num_q_heads / num_kv_heads) above 64 */
 #define KV_INT4_ERR_BLOCK_SIZE 4    /* block_size != 16 */
-#define KV_INT4_ERR_ALIGN 5         /* a pointer or stride breaks the 16-byte alignment rule */
+#define KV_INT4_ERR_ALIGN 5         /* a pointer or stride breaks its alignment rule (16 bytes for
+                                       K/V/Q/out and code caches, 8 for slot_mapping, 4 for scale
+                                       caches and int32 metadata) */
 #define KV_INT4_ERR_WORKSPACE 6     /* workspace NULL or smaller than kv_int4_attention_workspace_size() */
 #define KV_INT4_ERR_SIZE 7          /* a negative count, or a size that overflows the index types */
 #define KV_INT4_ERR_CUDA 8          /* a CUDA call or kernel launch failed */
@@ -62,8 +69,9 @@ extern "C" {
 /* device-side status bits (ORed into *dev_status) */
 #define KV_INT4_DEV_BAD_SLOT 1      /* slot_mapping entry >= num_blocks * block_size */
 #define KV_INT4_DEV_BAD_BLOCK 2     /* block_table entry outside [0, num_blocks) */
-#define KV_INT4_DEV_BAD_SEQ 4       /* q_len < 0, q_len > seq_len, seq_len > max_blocks_per_seq * block_size,
-                                       or query_start_loc outside [0, num_q_tokens] */
+#define KV_INT4_DEV_BAD_SEQ 4       /* q_len < 0, q_len > seq_len, q_len > max_query_len,
+                                       seq_len > max_blocks_per_seq * block_size, or query_start_loc
+                                       outside [0, num_q_tokens] */
 #define KV_INT4_DEV_BAD_SIGNS 8     /* a sign entry other than +1 / -1 */
 #define KV_INT4_DEV_TIMEOUT 16      /* a wait for staged input exceeded its iteration limit: the kernel
                                        stopped early and its outputs are incomplete (not expected to occur) */
@@ -90,9 +98,11 @@ extern "C" {
  * k, v: bf16, element (t, h, i) at k[t*k_token_stride + h*head_size + i];
  *   heads and elements contiguous.  Strides are in elements and must be
  *   multiples of 8; k, v must be 16-byte aligned.
- * slot_mapping: int64 [num_tokens].  signs: int8 [head_size], each +1 or -1
- *   (the random diagonal D, shared by K, V, Q and all heads).
- * Caches: as above, 16-byte aligned.  num_tokens == 0 is a no-op.
+ * slot_mapping: int64 [num_tokens], 8-byte aligned.  signs: int8
+ *   [head_size], each +1 or -1 (the random diagonal D, shared by K, V, Q and
+ *   all heads).
+ * Caches: as above; code caches 16-byte aligned, scale caches 4-byte
+ *   aligned.  num_tokens == 0 is a no-op.
  */
 KVINT4_API int kv_int4_write(const void* k, int64_t k_token_stride,
                   const void* v, int64_t v_token_stride,
@@ -186,8 +196,10 @@ KVINT4_API size_t kv_int4_attention_workspace_size(int num_seqs, int num_q_token
  * out: bf16, same layout with out_token_stride.
  * block_table: int32 [num_seqs][max_blocks_per_seq].  seq_lens: int32
  *   [num_seqs].  query_start_loc: int32 [num_seqs+1], non-decreasing from 0
- *   to num_q_tokens.  max_query_len / max_seq_len: upper bounds of the
- *   per-sequence values (used only to size launches).
+ *   to num_q_tokens.  These three and the scale caches are 4-byte aligned.
+ *   max_query_len / max_seq_len: upper bounds of the per-sequence values
+ *   (used only to size launches); a sequence whose q_len exceeds
+ *   max_query_len is treated as invalid metadata (below).
  * signs: int8 [head_size], the same D that the cache was written with.
  * workspace: >= kv_int4_attention_workspace_size(...) bytes, 256-byte aligned.
  * Sequences whose metadata is invalid are skipped (their output rows are not
@@ -255,8 +267,9 @@ KVINT4_API int kv_int8_attention(const void* q, int64_t q_token_stride,
  * nothing (no cudaMalloc, cudaFree or allocating library call).
  *
  * The first call on a device (with that device current) looks up the array's
- * device address and keeps it; that call may load the library's device code
- * on the device, so make it before any stream capture begins.
+ * device address and keeps it (a call after a cudaDeviceReset looks it up
+ * again); that call may load the library's device code on the device, so
+ * make it before any stream capture begins.
  *
  * All calls on a device share the one array, which keeps the last call's
  * contents; nothing in it needs clearing (each call rewrites what it reads).
@@ -390,14 +403,15 @@ KVINT4_API const char* kv_int4_status_string(int status);
  * KV_INT4_DEV_TIMEOUT into *dev_status and returns; the SM cycles it waited go to *dev_cycles
  * (nullable).  It never faults or hangs: it exercises the time-out path on a GPU, and its cycles
  * per attempt bound how long the kernels' own limit (2^18 attempts, about a second) can hold a
- * warp.  Device pointers, enqueued on `stream`.  KV_INT4_ERR_SIZE for iterations < 0,
+ * warp.  Device pointers, enqueued on `stream` (a cudaStream_t passed as void*).  KV_INT4_ERR_SIZE for iterations < 0,
  * KV_INT4_ERR_NULL without dev_status. */
 KVINT4_API int kv_int4_selftest_wait(int iterations, int32_t* dev_status, uint64_t* dev_cycles,
-                                     cudaStream_t stream);
+                                     void* stream);
 
-/* kv_int4_version -- the library's ABI version: 3 (2: kv_int4_rht and the int8_per_token_head
+/* kv_int4_version -- the library's ABI version: 4 (2: kv_int4_rht and the int8_per_token_head
  * entry points kv_int8_write / kv_int8_attention, sliding_window in the attention entry points;
- * 3: the in-slot entry points, kv_int4_attention_noalloc's window argument, kv_int4_selftest_wait). */
+ * 3: the in-slot entry points, kv_int4_attention_noalloc's window argument, kv_int4_selftest_wait;
+ * 4: kv_int4_selftest_wait takes its stream as void*, like every other entry point). */
 KVINT4_API int kv_int4_version(void);
 
 #ifdef __cplusplus

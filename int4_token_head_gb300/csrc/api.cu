@@ -2,7 +2,10 @@
 // on the caller's stream.  Nothing here allocates device memory or
 // synchronises the device.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "../../include/kvint4.h"
 #include "internal.h"
@@ -17,14 +20,40 @@ int current_device() {
 }
 
 int sm_count(int dev) {
-  static int cache[kMaxDevices] = {};
+  static std::atomic<int> cache[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return 1;
-  if (!cache[dev]) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
+}
+
+// The two driver calls are reached through the runtime's entry-point query,
+// so the library links the static runtime only.
+uint64_t current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -63,6 +92,7 @@ bool workspace_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_k
 
 static bool head_size_ok(int d) { return d == 64 || d == 96 || d == 128 || d == 192 || d == 256; }
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+static bool aligned(const void* p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
 
 }  // namespace kvint4
 
@@ -70,7 +100,7 @@ using namespace kvint4;
 
 extern "C" {
 
-int kv_int4_version(void) { return 3; }
+int kv_int4_version(void) { return 4; }
 
 const char* kv_int4_status_string(int status) {
   switch (status) {
@@ -79,7 +109,9 @@ const char* kv_int4_status_string(int status) {
     case KV_INT4_ERR_HEAD_SIZE: return "unsupported head_size (expected 64, 96, 128, 192 or 256)";
     case KV_INT4_ERR_HEADS: return "invalid head counts (num_q_heads must be a positive multiple of num_kv_heads, at most 64 times it)";
     case KV_INT4_ERR_BLOCK_SIZE: return "unsupported block_size (expected 16)";
-    case KV_INT4_ERR_ALIGN: return "a pointer is not 16-byte aligned or a token stride is not a multiple of 8 elements";
+    case KV_INT4_ERR_ALIGN:
+      return "a pointer breaks its alignment rule (16 bytes for K/V/Q/out and code caches, 8 for slot_mapping, "
+             "4 for scale caches and int32 metadata) or a token stride is not a multiple of 8 elements";
     case KV_INT4_ERR_WORKSPACE: return "workspace is NULL or smaller than kv_int4_attention_workspace_size()";
     case KV_INT4_ERR_SIZE: return "a count is negative or a size overflows the index types";
     case KV_INT4_ERR_CUDA: return "a CUDA call or kernel launch failed";
@@ -101,6 +133,7 @@ static int validate_write(const void* k, int64_t ks, const void* v, int64_t vs, 
   if (!k || !v || !slots || !kc || !vc || !ksc || !vsc || (need_signs && !signs)) return KV_INT4_ERR_NULL;
   if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc) || (ks % 8) || (vs % 8) || ks < 0 || vs < 0)
     return KV_INT4_ERR_ALIGN;
+  if (!aligned(slots, 8) || !aligned(ksc, 4) || !aligned(vsc, 4)) return KV_INT4_ERR_ALIGN;
   if ((int64_t)num_tokens * 2 * hkv >= (1ll << 31)) return KV_INT4_ERR_SIZE;
   return KV_INT4_OK;
 }
@@ -216,6 +249,9 @@ static int do_attention(const void* q, int64_t q_token_stride, const uint8_t* k_
     return !workspace ? KV_INT4_ERR_WORKSPACE : KV_INT4_ERR_NULL;
   if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || (q_token_stride % 8) ||
       (out_token_stride % 8) || q_token_stride < 0 || out_token_stride < 0 || ((uintptr_t)workspace & 255u))
+    return KV_INT4_ERR_ALIGN;
+  if (!aligned(k_scale_cache, 4) || !aligned(v_scale_cache, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(query_start_loc, 4) || !aligned(dev_status, 4))
     return KV_INT4_ERR_ALIGN;
   if ((int64_t)max_blocks_per_seq * block_size >= (1ll << 31) || (int64_t)num_q_tokens * num_q_heads >= (1ll << 31))
     return KV_INT4_ERR_SIZE;

@@ -90,6 +90,7 @@ struct Common {
   const int32_t* qsl;
   int num_seqs;
   int num_q_tokens;
+  int max_qlen;  // the caller's max_query_len: launch sizes assume no q_len above it
   int hq;
   int hkv;
   int group;
@@ -173,7 +174,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
         const int q0 = c.qsl[s], q1 = c.qsl[s + 1];
         L = c.seq_lens[s];
         ql = q1 - q0;
-        const bool bad = q0 < 0 || q1 > c.num_q_tokens || ql < 0 || L < ql ||
+        // a q_len above max_query_len would fall outside the launches sized
+        // from it (decode columns, the prefill launch, the reduce segments)
+        const bool bad = q0 < 0 || q1 > c.num_q_tokens || ql < 0 || L < ql || ql > c.max_qlen ||
                          (long long)L > (long long)c.max_blocks * 16;
         if (bad) {
           flag(c.status, KV_INT4_DEV_BAD_SEQ);
@@ -721,17 +724,14 @@ __global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PrePa
 // ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
+// sets the kernel's shared-memory limit and gives its CTAs per SM
 template <typename K>
-static bool configure(K kern, int smem, int threads, int* occ_out, bool* done, int* occ_cache) {
-  if (!*done) {
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return false;
-    int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem) != cudaSuccess || o < 1) return false;
-    *occ_cache = o;
-    *done = true;
-  }
-  *occ_out = *occ_cache;
+static bool configure(K kern, int smem, int threads, int* occ_out) {
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return false;
+  int o = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem) != cudaSuccess || o < 1) return false;
+  *occ_out = o;
   return true;
 }
 
@@ -739,28 +739,24 @@ static bool configure(K kern, int smem, int threads, int* occ_out, bool* done, i
 // answers 1 for any such kernel, so the count is taken from the kernel's
 // registers and shared memory and the TMEM columns each CTA holds
 template <typename K>
-static bool configure_tmem(K kern, int smem, int threads, int tmem_cols, int* occ_out, bool* done, int* occ_cache) {
-  if (!*done) {
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return false;
-    cudaFuncAttributes fa;
-    int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
-      return false;
-    const int warps = (threads + 31) / 32;
-    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocated per warp in 256-register units
-    const int by_regs = regs_sm / (regs_warp * ((warps + 3) / 4 * 4));  // and per group of four warps
-    const int by_smem = smem_sm / (smem + fa.sharedSizeBytes + reserved);
-    const int by_tmem = 512 / tmem_cols;
-    const int o = min(by_regs, min(by_smem, by_tmem));
-    if (o < 1) return false;
-    *occ_cache = o;
-    *done = true;
-  }
-  *occ_out = *occ_cache;
+static bool configure_tmem(K kern, int smem, int threads, int tmem_cols, int* occ_out) {
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return false;
+  cudaFuncAttributes fa;
+  int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
+    return false;
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocated per warp in 256-register units
+  const int by_regs = regs_sm / (regs_warp * ((warps + 3) / 4 * 4));  // and per group of four warps
+  const int by_smem = smem_sm / (smem + fa.sharedSizeBytes + reserved);
+  const int by_tmem = 512 / tmem_cols;
+  const int o = min(by_regs, min(by_smem, by_tmem));
+  if (o < 1) return false;
+  *occ_out = o;
   return true;
 }
 
@@ -785,6 +781,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   c.qsl = a.query_start_loc;
   c.num_seqs = a.num_seqs;
   c.num_q_tokens = a.num_q_tokens;
+  c.max_qlen = a.max_query_len;
   c.hq = a.num_q_heads;
   c.hkv = a.num_kv_heads;
   c.group = a.num_q_heads / a.num_kv_heads;
@@ -837,23 +834,18 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
                         (reinterpret_cast<uintptr_t>(a.v_scale) & 15) == 0 && (a.geo.srow * 4) % 16 == 0 &&
                         (a.geo.sblk * 4) % 16 == 0 && a.geo.shead == 1;
   if (any_decode) {
-    // one cache per kernel: (blocks per position, ring depth)
-    static bool attr_done[kMaxDevices][2][2] = {};
-    static int occ_cache[kMaxDevices][2][2][9] = {};
+    // one cache per kernel and head group: (blocks per position, ring depth, hg)
+    static PerContext<int> occ_cache[2][2][9];
     auto occupancy = [&](auto kern, int np, int smem_max, int smem) -> int {
       if (smem > kMaxSmem) return 0;  // this ring does not fit
-      if (!attr_done[dev][np - 1][dec_deep]) {
+      int o = 0;
+      const bool ok = occ_cache[np - 1][dec_deep][c.hg].get(dev, [&](int* v) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, min(smem_max, kMaxSmem)) !=
             cudaSuccess)
-          return 0;
-        attr_done[dev][np - 1][dec_deep] = true;
-      }
-      if (!occ_cache[dev][np - 1][dec_deep][c.hg]) {
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.hg * 32, smem) != cudaSuccess || o < 1) return 0;
-        occ_cache[dev][np - 1][dec_deep][c.hg] = o;
-      }
-      return occ_cache[dev][np - 1][dec_deep][c.hg];
+          return false;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, c.hg * 32, smem) == cudaSuccess && *v >= 1;
+      }, &o);
+      return ok ? o : 0;
     };
     using E1 = DecodeEntry<D, 1, FMT>;
     using E2 = DecodeEntry<D, 2, FMT>;
@@ -889,12 +881,13 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   // 2. prefill
   const bool may_prefill = c.group > c.dcols || (long long)a.max_query_len * c.group > c.dcols;
   if (may_prefill) {
-    static bool done[kMaxDevices] = {};
-    static int occ_c[kMaxDevices] = {};
+    static PerContext<int> occ_c;
     int occ = 0;
     if constexpr (kTcPrefill) {
       using G = WsGeom<D, FMT>;
-      if (!configure_tmem(prefill_ws_kernel<D, FMT>, G::SMEM, G::THREADS, G::TMEM_COLS, &occ, &done[dev], &occ_c[dev]))
+      if (!occ_c.get(dev, [](int* o) {
+            return configure_tmem(prefill_ws_kernel<D, FMT>, G::SMEM, G::THREADS, G::TMEM_COLS, o);
+          }, &occ))
         return KV_INT4_ERR_CUDA;
       long long grid = (long long)sms * occ;
       if (grid > L.max_prefill_items) grid = L.max_prefill_items;
@@ -904,7 +897,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
       timing_end(kTimedPrefill, stream);
     } else {
       using G = PreGeom<D, FMT>;
-      if (!configure(prefill_kernel<D, FMT>, G::SMEM, G::THREADS, &occ, &done[dev], &occ_c[dev]))
+      if (!occ_c.get(dev, [](int* o) { return configure(prefill_kernel<D, FMT>, G::SMEM, G::THREADS, o); }, &occ))
         return KV_INT4_ERR_CUDA;
       long long grid = (long long)sms * occ;
       if (grid > L.max_prefill_items) grid = L.max_prefill_items;

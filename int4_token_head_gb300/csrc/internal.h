@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace kvint4 {
 
 constexpr int kMaxDevices = 64;
@@ -14,6 +16,45 @@ constexpr int kMaxDevices = 64;
 int current_device();
 // cached multiprocessor count of device `dev`
 int sm_count(int dev);
+// A unique id of the calling thread's current CUDA context (0 when there is
+// none yet or the driver cannot say).  cudaDeviceReset replaces a device's
+// primary context, and with it every function attribute set and every
+// address taken in the old one.
+uint64_t current_context_id();
+
+// A launch setting (a function attribute set, an occupancy, a symbol
+// address) computed once per device and CUDA context and shared by all host
+// threads.  The first caller in a new context computes it under the lock;
+// a failed computation caches nothing.
+template <typename T>
+class PerContext {
+ public:
+  template <typename Make>
+  bool get(int dev, Make&& make, T* out) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    const uint64_t ctx = current_context_id();
+    std::lock_guard<std::mutex> lock(mutex_);
+    Slot& s = slot_[dev];
+    if (!s.valid || s.ctx != ctx) {
+      T v{};
+      if (!make(&v)) return false;
+      s.value = v;
+      s.ctx = ctx;
+      s.valid = true;
+    }
+    *out = s.value;
+    return true;
+  }
+
+ private:
+  struct Slot {
+    bool valid = false;
+    uint64_t ctx = 0;
+    T value{};
+  };
+  std::mutex mutex_;
+  Slot slot_[kMaxDevices];
+};
 
 // Where the codes and the scale of (slot, kv head) live.  A slot is
 // (block, row) = (slot / 16, slot % 16); codes start at

@@ -12,8 +12,10 @@
 //
 // Set-up: the first call on a device, with that device current, asks the
 // runtime for the array's device address (cudaGetSymbolAddress) and keeps it
-// for later calls on that device.  That first call may load the library's
-// device code on the device, so make it before any stream capture begins.
+// for later calls on that device (and looks it up again after a
+// cudaDeviceReset, which gives the device a new context).  That first call
+// may load the library's device code on the device, so make it before any
+// stream capture begins.
 //
 // Sharing: every call on a device uses the same array, and the array keeps
 // whatever the previous call left there.  The attention kernels never read a
@@ -25,8 +27,6 @@
 
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/kvint4.h"
 #include "internal.h"
 
@@ -36,20 +36,15 @@ namespace {
 // The whole workspace of kv_int4_attention_noalloc, per device.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[KV_INT4_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_setup_mutex;
-void* g_scratch_address[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on device `dev` (which must be current).
+// Device address of g_noalloc_scratch on device `dev` (which must be
+// current), looked up once per device and CUDA context: after a
+// cudaDeviceReset the array lives in a new context, possibly elsewhere.
 int scratch_address(int dev, void** out) {
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_address[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) return KV_INT4_ERR_CUDA;
-    g_scratch_address[dev] = p;
-  }
-  *out = g_scratch_address[dev];
-  return KV_INT4_OK;
+  static PerContext<void*> address;
+  const bool ok = address.get(dev, [](void** p) {
+    return cudaGetSymbolAddress(p, g_noalloc_scratch) == cudaSuccess && *p != nullptr;
+  }, out);
+  return ok ? KV_INT4_OK : KV_INT4_ERR_CUDA;
 }
 
 }  // namespace

@@ -229,15 +229,16 @@ int launch_reg(const RhtArgs& a, cudaStream_t stream) {
 template <bool INV, bool F32>
 int launch_smem(const RhtArgs& a, int d, cudaStream_t stream) {
   const int smem = kRhtWarps * d * (int)sizeof(float);
-  static bool attr_done[kMaxDevices] = {};
+  static PerContext<int> attr;
   const int dev = current_device();
   if (dev < 0) return KV_INT4_ERR_CUDA;
-  if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(rht_smem_kernel<INV, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kRhtWarps * kRhtMaxSmemHead * (int)sizeof(float)) != cudaSuccess)
-      return KV_INT4_ERR_CUDA;
-    attr_done[dev] = true;
-  }
+  int set = 0;
+  if (!attr.get(dev, [](int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(rht_smem_kernel<INV, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kRhtWarps * kRhtMaxSmemHead * (int)sizeof(float)) == cudaSuccess;
+      }, &set))
+    return KV_INT4_ERR_CUDA;
   rht_smem_kernel<INV, F32><<<(unsigned)grid_for(a.rows, dev), kRhtWarps * 32, smem, stream>>>(a, d);
   return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
 }

@@ -36,10 +36,10 @@ __global__ void __launch_bounds__(32) selftest_wait_kernel(int iterations, int32
 }  // namespace kvint4
 
 extern "C" KVINT4_API int kv_int4_selftest_wait(int iterations, int32_t* dev_status, uint64_t* dev_cycles,
-                                                cudaStream_t stream) {
+                                                void* stream) {
   if (iterations < 0) return KV_INT4_ERR_SIZE;
   if (!dev_status) return KV_INT4_ERR_NULL;
-  kvint4::selftest_wait_kernel<<<1, 32, 0, stream>>>(iterations, dev_status,
+  kvint4::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(iterations, dev_status,
                                                     reinterpret_cast<unsigned long long*>(dev_cycles));
   return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
 }

@@ -756,36 +756,25 @@ static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
   using G = WriteGeom<D>;
   auto kern = write_kernel<D, PREROT>;
   const int dev = current_device();
-  static bool configured[kMaxDevices] = {};
-  if (!configured[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM) != cudaSuccess)
-      return KV_INT4_ERR_CUDA;
-    configured[dev] = true;
-  }
-  static int occ[kMaxDevices] = {};
-  if (!occ[dev]) {
-    int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, G::NT, G::SMEM) != cudaSuccess || o < 1) return KV_INT4_ERR_CUDA;
-    occ[dev] = o;
-  }
+  // each kernel's shared-memory limit and CTAs per SM, set once per device context
+  auto setup = [](auto k, int threads, int smem, int* o) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(o, k, threads, smem) == cudaSuccess && *o >= 1;
+  };
+  static PerContext<int> occ_cache;
+  int occ = 0;
+  if (!occ_cache.get(dev, [&](int* o) { return setup(kern, G::NT, G::SMEM, o); }, &occ)) return KV_INT4_ERR_CUDA;
   if constexpr (!PREROT && D <= 192) {
     using T = TcGeom<D>;
     if (2 * a.num_kv_heads <= T::UT) {
       auto tckern = write_kernel_tc<D>;
-      static bool tc_done[kMaxDevices] = {};
-      static int tc_occ[kMaxDevices] = {};
-      if (!tc_done[dev]) {
-        if (cudaFuncSetAttribute(tckern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) != cudaSuccess)
-          return KV_INT4_ERR_CUDA;
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tckern, T::NT, T::SMEM) != cudaSuccess || o < 1)
-          return KV_INT4_ERR_CUDA;
-        tc_occ[dev] = o;
-        tc_done[dev] = true;
-      }
+      static PerContext<int> tc_occ_cache;
+      int tc_occ = 0;
+      if (!tc_occ_cache.get(dev, [&](int* o) { return setup(tckern, T::NT, T::SMEM, o); }, &tc_occ))
+        return KV_INT4_ERR_CUDA;
       const int tt = T::UT / (2 * a.num_kv_heads);
       const int64_t tiles = ((int64_t)a.num_tokens + tt - 1) / tt;
-      const int64_t tcap = (int64_t)sm_count(dev) * tc_occ[dev];
+      const int64_t tcap = (int64_t)sm_count(dev) * tc_occ;
       const int grid = (int)(tiles < tcap ? tiles : tcap);
       timing_begin(kTimedWrite, stream);
       tckern<<<grid, T::NT, T::SMEM, stream>>>(
@@ -796,15 +785,16 @@ static int launch_write_t(const WriteArgs& a, cudaStream_t stream) {
       return cudaGetLastError() == cudaSuccess ? KV_INT4_OK : KV_INT4_ERR_CUDA;
     }
   }
-  const int64_t cap = (int64_t)sm_count(dev) * occ[dev];
+  const int64_t cap = (int64_t)sm_count(dev) * occ;
   if (2 * a.num_kv_heads <= G::UT) {
     auto tkern = write_kernel_tok<D, PREROT>;
-    static bool tconfigured[kMaxDevices] = {};
-    if (!tconfigured[dev]) {
-      if (cudaFuncSetAttribute(tkern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM) != cudaSuccess)
-        return KV_INT4_ERR_CUDA;
-      tconfigured[dev] = true;
-    }
+    static PerContext<int> tok_attr;
+    int set = 0;
+    if (!tok_attr.get(dev, [&](int* v) {
+          *v = 1;
+          return cudaFuncSetAttribute(tkern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM) == cudaSuccess;
+        }, &set))
+      return KV_INT4_ERR_CUDA;
     const int tt = G::UT / (2 * a.num_kv_heads);
     const int64_t tiles = ((int64_t)a.num_tokens + tt - 1) / tt;
     const int grid = (int)(tiles < cap ? tiles : cap);

@@ -61,3 +61,32 @@ def assert_close_attention(got, ref, atol=5e-2, rtol=5e-2, min_corr=0.9999, what
 
 def f32_bits(x):
     return np.asarray(x, np.float32).view(np.uint32)
+
+
+def check_sampled_end_to_end(w, q, out, seqs, heads):
+    """End to end on sampled rows: the oracle writes the sampled sequences'
+    K/V itself (drawn on the GPU, copied to the host), attends, and every
+    sampled (sequence, q head) row of the GPU output must be within atol =
+    rtol = 5e-2; the rows together must correlate >= 0.9999 (single 96- or
+    128-element rows are too short for a meaningful correlation bar)."""
+    qn = q.float().cpu().numpy()
+    scale = 1.0 / math.sqrt(w.head_size)
+    signs = w.signs.numpy()
+    gots, refs = [], []
+    for s in seqs:
+        ql, L = w.seqs[s]
+        k, v = w.seq_kv(s, "cuda")
+        k = k.float().cpu().numpy()
+        v = v.float().cpu().numpy()
+        q0 = int(w.query_start_loc[s])
+        for h in heads:
+            kvh = h // w.group
+            kc, ksc = O.quantize(O.rotate_for_cache(k[:, kvh], signs))
+            vc, vsc = O.quantize(O.rotate_for_cache(v[:, kvh], signs))
+            k_hat = O.dequantize_original(kc, ksc, signs)
+            v_hat = O.dequantize_original(vc, vsc, signs)
+            refs.append(O.attention_head(qn[q0:q0 + ql, h], k_hat, v_hat, L - ql, scale, w.causal,
+                                         w.sliding_window).ravel())
+            gots.append(out[q0:q0 + ql, h].float().cpu().numpy().ravel())
+    return assert_close_attention(np.concatenate(gots), np.concatenate(refs),
+                                  what=f"{w.name} sampled end to end")

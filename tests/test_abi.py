@@ -55,7 +55,7 @@ def test_status_strings_and_version(lib):
             s = lib.kv_int4_status_string(code).decode()
             assert s and s != "unknown status"
     assert lib.kv_int4_status_string(999).decode() == "unknown status"
-    assert lib.kv_int4_version() == 3
+    assert lib.kv_int4_version() == 4
 
 
 def test_workspace_size_is_host_only_and_monotone(lib):
@@ -94,6 +94,9 @@ def test_write_validation(lib):
     assert _write(lib, kc=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
     assert _write(lib, ks=8 * 128 + 4) == D["KV_INT4_ERR_ALIGN"]
     assert _write(lib, nt=1 << 28, hkv=8) == D["KV_INT4_ERR_SIZE"]
+    assert _write(lib, slots=ctypes.c_void_p(0x10004)) == D["KV_INT4_ERR_ALIGN"]   # int64 slots: 8 bytes
+    assert _write(lib, ksc=ctypes.c_void_p(0x10002)) == D["KV_INT4_ERR_ALIGN"]    # f32 scales: 4 bytes
+    assert _write(lib, vsc=ctypes.c_void_p(0x10001)) == D["KV_INT4_ERR_ALIGN"]
     # the prerotated variant takes no signs
     r = lib.kv_int4_write_prerotated(FAKE, 1024, FAKE, 1024, FAKE, 0, FAKE, FAKE, FAKE, FAKE, 4, 16, 8, 128,
                                      None, None)
@@ -130,6 +133,8 @@ def test_attention_validation(lib):
     assert _attn(lib, out=FAKE_ODD) == D["KV_INT4_ERR_ALIGN"]
     assert _attn(lib, ws=ctypes.c_void_p(0x10010)) == D["KV_INT4_ERR_ALIGN"]
     assert _attn(lib, qs=32 * 128 + 2) == D["KV_INT4_ERR_ALIGN"]
+    for arg in ("ksc", "vsc", "bt", "sl", "qsl", "status"):
+        assert _attn(lib, **{arg: ctypes.c_void_p(0x10002)}) == D["KV_INT4_ERR_ALIGN"], arg
     assert _attn(lib, ns=-3) == D["KV_INT4_ERR_SIZE"]
     assert _attn(lib, win=-1) == D["KV_INT4_ERR_SIZE"]
     assert _attn(lib, ns=0, win=4096) == D["KV_INT4_OK"]

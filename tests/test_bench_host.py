@@ -67,6 +67,30 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == bench.UNIT and d["metric"] == bench.METRIC
     assert d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert "processes at once" in d["cpu_baseline"]["sample"] and d["cpu_baseline"]["write_chunk_gbs"] > 0
+    # the same workload description as our arm prints for the same arguments
+    args = bench.argparse.Namespace(workload="tiny", batch=0)
+    from int4_token_head_gb300 import synthetic
+    assert d["config"] == bench.bench_config(args, synthetic.make_workload("tiny"), 1)
+
+
+def test_gpus_flag_launches_ranks_itself():
+    """`bench.py --gpus 2` without torchrun starts two ranks itself; for the
+    reference arm rank 0 alone prints the line, which reports both ranks."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "tiny", "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
+                       timeout=600, env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["config"]["parallelism"] == "replicas x2"
+
+
+def test_gpus_flag_without_enough_gpus_fails_cleanly():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       capture_output=True, text=True, timeout=300, env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode != 0 and "needs 2 visible GPUs" in r.stderr
 
 
 def test_reference_arm_nonzero_rank_exits_quietly():
