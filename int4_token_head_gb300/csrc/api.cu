@@ -70,7 +70,7 @@ bool workspace_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_k
   L->plan = off;
   off = align256(off + 64 * sizeof(int32_t));
   L->dseq = off;
-  off = align256(off + (size_t)S * sizeof(int32_t));
+  off = align256(off + (size_t)S * 4 * sizeof(int32_t));
   L->dprefix = off;
   off = align256(off + (size_t)(S + 1) * sizeof(int64_t));
   L->max_prefill_items = (T / tile_tokens + S) * Hkv;

@@ -46,7 +46,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct PlanView {
   int32_t* plan;      // [0] n_dseq, [1] n_prefill_items, [2] prefill work counter, [3] n_pseq
-  int32_t* dseq;
+  int4* dseq;         // decode sequences in order: (sequence id, seq_len, first query token, q_len)
   int64_t* dprefix;
   int2* ptab;         // prefill sequences in order: (seq id, index of its first item); [n_pseq].y = items
   __half* qrot;
@@ -60,7 +60,7 @@ static PlanView plan_view(void* ws, const WorkspaceLayout& L) {
   uint8_t* b = static_cast<uint8_t*>(ws);
   PlanView v;
   v.plan = reinterpret_cast<int32_t*>(b + L.plan);
-  v.dseq = reinterpret_cast<int32_t*>(b + L.dseq);
+  v.dseq = reinterpret_cast<int4*>(b + L.dseq);
   v.dprefix = reinterpret_cast<int64_t*>(b + L.dprefix);
   v.ptab = reinterpret_cast<int2*>(b + L.pitems);
   v.qrot = reinterpret_cast<__half*>(b + L.qrot);
@@ -110,6 +110,12 @@ struct Common {
   int dcols;        // decode: query columns per block (8 / np); longer queries go to prefill
   long long max_items;  // capacity of the prefill item list
 };
+
+// floor(n / d) for 0 <= n, 0 < d: one 32-bit division when both fit (the
+// usual case for schedule arithmetic), the 64-bit routine otherwise
+__device__ __forceinline__ long long div_nn(long long n, long long d) {
+  return ((n | d) >> 31) == 0 ? (long long)((uint32_t)n / (uint32_t)d) : n / d;
+}
 
 // first key position visible to the query at position qpos
 __device__ __forceinline__ int window_lo(const Common& c, int qpos) {
@@ -169,9 +175,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
     long long dpre = 0, n_items = 0;
     for (int base = 0; base < c.num_seqs; base += kPrepThreads) {
       const int s = base + threadIdx.x;
-      int kind = 0, nblk = 0, ntiles = 0, ql = 0, L = 0;
+      int kind = 0, nblk = 0, ntiles = 0, ql = 0, L = 0, q0 = 0;
       if (s < c.num_seqs) {
-        const int q0 = c.qsl[s], q1 = c.qsl[s + 1];
+        q0 = c.qsl[s];
+        const int q1 = c.qsl[s + 1];
         L = c.seq_lens[s];
         ql = q1 - q0;
         // a q_len above max_query_len would fall outside the launches sized
@@ -194,7 +201,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
       const int ex_p = block_exclusive_scan<int>(kind == 2, &tot_p, s_i32);
       const long long ex_c = block_exclusive_scan<long long>((long long)ntiles * c.hkv, &tot_c, s_i64);
       if (kind == 1) {
-        pv.dseq[n_dseq + ex_a] = s;
+        pv.dseq[n_dseq + ex_a] = make_int4(s, L, q0, ql);
         pv.dprefix[n_dseq + ex_a] = dpre + ex_b;
       } else if (kind == 2) {
         // the prefill kernel expands (tile, kv head) items from this table
@@ -329,16 +336,16 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   const int n_dseq = pv.plan[0];
   if (seg >= n_dseq * c.hkv) return;
   const int i = seg / c.hkv, h = seg - i * c.hkv;
-  const int seq = pv.dseq[i];
-  const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+  const int4 di = pv.dseq[i];  // (sequence, seq_len, first query token, q_len)
+  const int q0 = di.z, ql = di.w;
   if (col >= ql * c.group) return;  // ql * group <= cps
-  const int nblk = (c.seq_lens[seq] + 15) / 16;
-  const int npos = (nblk - first_block(c, c.seq_lens[seq], ql) + c.np - 1) / c.np;
+  const int nblk = (di.y + 15) / 16;
+  const int npos = (nblk - first_block(c, di.y, ql) + c.np - 1) / c.np;
   const int grp = h / c.hg, hl = h - grp * c.hg;
   const long long Tu = pv.dprefix[n_dseq] * c.ng;
   const long long sbeg = pv.dprefix[i] * c.ng + (long long)grp * npos, send = sbeg + npos;
   const int W = prm.num_ctas;
-  auto wstart = [&](long long w) { return Tu * w / W; };
+  auto wstart = [&](long long w) { return div_nn(Tu * w, W); };
 
   constexpr int PER = D / 32;
   float acc[PER];
@@ -368,14 +375,14 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
     const long long slot = w * c.hg + hl;
     merge_slot(pv.warp_o + slot * kDecodeCols * D, pv.warp_ml + slot * kDecodeCols * 2);
   };
-  const long long w_first = ((sbeg + 1) * W + Tu - 1) / Tu;  // first CTA starting after sbeg
-  const long long w_end = (send * W + Tu - 1) / Tu;          // first CTA starting at or after send
+  const long long w_first = div_nn((sbeg + 1) * W + Tu - 1, Tu);  // first CTA starting after sbeg
+  const long long w_end = div_nn(send * W + Tu - 1, Tu);          // first CTA starting at or after send
   if (w_end - w_first <= send - sbeg - 1) {
     for (long long w = w_first; w < w_end; w++)
       if (wstart(w + 1) > wstart(w)) merge_cta(w);
   } else {
     for (long long p = sbeg + 1; p < send; p++) {
-      const long long w = ((p + 1) * W + Tu - 1) / Tu - 1;  // last CTA starting at or before p
+      const long long w = div_nn((p + 1) * W + Tu - 1, Tu) - 1;  // last CTA starting at or before p
       if (wstart(w) == p) merge_cta(w);
     }
   }
@@ -866,6 +873,13 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     c.np = 1;
   }
   c.dcols = kDecodeCols / c.np;
+  // the decode launch's CTAs
+  int dec_grid = 0;
+  if (any_decode) {
+    long long grid = (long long)sms * dec_occ;
+    if (grid * c.hg > kMaxDecodeWarps) grid = kMaxDecodeWarps / c.hg;
+    dec_grid = (int)grid;
+  }
 
   // 1. prep
   {
@@ -910,9 +924,8 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   }
   // 3. decode + 4. reduce
   if (any_decode) {
-    long long grid = (long long)sms * dec_occ;
-    if (grid * c.hg > kMaxDecodeWarps) grid = kMaxDecodeWarps / c.hg;
-    const int num_ctas = (int)grid;
+    const long long grid = dec_grid;
+    const int num_ctas = dec_grid;
     const int threads = c.hg * 32;
     timing_begin(kTimedDecode, stream);
     if (c.np == 2)

@@ -58,12 +58,13 @@ struct DecWalk {
   int seq;    // sequence id
 };
 
+// one 16-byte record per decode sequence, written by the prep kernel
 template <int NP>
 __device__ __forceinline__ void walk_load(DecWalk& w, const Common& c, const PlanView& pv) {
-  w.seq = pv.dseq[w.i];
-  const int L = c.seq_lens[w.seq];
-  w.nblk = (L + 15) / 16;
-  w.fb = first_block(c, L, c.qsl[w.seq + 1] - c.qsl[w.seq]);
+  const int4 di = pv.dseq[w.i];  // (sequence, seq_len, first query token, q_len)
+  w.seq = di.x;
+  w.nblk = (di.y + 15) / 16;
+  w.fb = first_block(c, di.y, di.w);
   w.npos = (w.nblk - w.fb + NP - 1) / NP;
 }
 template <int NP>
@@ -203,6 +204,7 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
   const int R = prm.num_ctas;
   const long long P0 = Tu * blockIdx.x / R, P1 = Tu * (blockIdx.x + 1) / R;
   if (P0 >= P1) return;
+  const int nunits = (int)(P1 - P0);
 
   // locate P0: largest i with dprefix[i] * ng <= P0 (32-ary search, per warp)
   int lo = 0, hi = n_dseq;  // invariant: key(lo) <= P0 < key(hi)
@@ -284,18 +286,42 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
 
   // producer: one block per call into the next ring slot, the next block id
   // loaded one call ahead; one commit group per call (empty past the range)
-  long long ppos = P0;
+  int ppos = 0;
   int pj = 0, ps = 0;
-  int pblk = block_at(pw, 0);
+  // the prologue's block ids, loaded together when its NS - NP blocks lie in
+  // the first segment (one latency instead of one per block): this serves
+  // short ranges; the DEEP ring's CTAs run long ranges and keep the registers
+  constexpr int PRO = DEEP ? 1 : G::NS - NP;
+  static_assert(PRO <= 4, "prologue depth");
+  int pro[4];
+  const int pro_n = PRO > 1 && pw.kp + (PRO + NP - 1) / NP <= pw.npos && (PRO + NP - 1) / NP <= nunits ? PRO : 1;
+#pragma unroll
+  for (int j = 0; j < 4; j++)
+    if (j < pro_n) {
+      const int kb = pw.fb + pw.kp * NP + j;
+      pro[j] = kb < pw.nblk ? c.block_table[(long long)pw.seq * c.max_blocks + kb] : kAbsent;
+    }
+  if (pro_n == 1) pro[0] = block_at(pw, 0);
+  int pro_left = pro_n - 1;  // prefetched ids after the current one, shifted down pro[1..3]
+  int pblk = pro[0];
   auto produce = [&]() {
-    if (ppos < P1) {
+    if (ppos < nunits) {
       issue(pblk, pw.grp, ps);
       ps = ps + 1 == G::NS ? 0 : ps + 1;
       if (++pj == NP) {
         pj = 0;
-        if (++ppos < P1) walk_next<NP>(pw, c, pv);
+        if (++ppos < nunits) walk_next<NP>(pw, c, pv);
       }
-      if (ppos < P1) pblk = block_at(pw, pj);
+      if (ppos < nunits) {
+        if (pro_left > 0) {
+          pblk = pro[1];
+          pro[1] = pro[2];
+          pro[2] = pro[3];
+          --pro_left;
+        } else {
+          pblk = block_at(pw, pj);
+        }
+      }
     }
     cp_async_commit();
   };
@@ -313,11 +339,9 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
   bool first_piece = cw.kp == 0;
 
   auto begin_segment = [&]() {
-    const int seq = cw.seq;
     const int head = cw.grp * HG + hl;
-    const int q0 = c.qsl[seq];
-    const int ql = c.qsl[seq + 1] - q0;
-    const int L = c.seq_lens[seq];
+    const int4 di = pv.dseq[cw.i];  // (sequence, seq_len, first query token, q_len)
+    const int q0 = di.z, ql = di.w, L = di.y;
     const int ctx = L - ql;
     // B fragments of this lane's column g, which holds query column g % COLS
     const int n = g & (G::COLS - 1);
@@ -430,7 +454,6 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
       smem_addr(smem) + hl * G::HTILE + G::KTILE + vrow * G::VROW + (((lane >> 4) ^ (vx & 1)) + 2 * (vx >> 1)) * 16;
   const int vstep = vx >> 1 ? -32 : 32;
   int cs = 0;                     // slot of the iteration's first block
-  const int nunits = (int)(P1 - P0);
   // INT4: rows g (even d: offset 1032) and g + 8 (odd d: offset 1152); int8: 1152
   const uint32_t vcorr[4] = {I8 ? kF16x2_M1152 : kF16x2_M1032, kF16x2_M1152, I8 ? kF16x2_M1152 : kF16x2_M1032,
                              kF16x2_M1152};
@@ -578,8 +601,14 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
   cp_async_wait<0>();
 }
 
+// Register ceilings (allocated in steps of 8 a thread) for four 4-warp CTAs
+// per SM up to head size 96, three at 128 (int8) and 192 (INT4); int8 at 192
+// and both formats at 256 keep the compiler's choice (two CTAs, no spills).
+__host__ __device__ constexpr int decode_max_regs(int d, int fmt) {
+  return d <= 96 ? 128 : (d <= 128 || (d <= 192 && fmt == kFmtInt4)) ? 168 : 255;
+}
 template <int D, int NP, int FMT>
-__global__ void __launch_bounds__(256) decode_kernel(DecParams prm) {
+__global__ void __maxnreg__(decode_max_regs(D, FMT)) decode_kernel(DecParams prm) {
   decode_body<D, NP, FMT, false>(prm);
 }
 // INT4 head size 128 (the long-context shape): at most 128 registers a

@@ -142,7 +142,7 @@ struct AttnArgs {
 // Workspace layout, shared by the size query and the launcher.
 struct WorkspaceLayout {
   size_t plan;          // int32 counters + per-seq schedule
-  size_t dseq;          // int32 [num_seqs] decode-sequence list
+  size_t dseq;          // int4 [num_seqs] decode sequences: (sequence id, seq_len, first query token, q_len)
   size_t dprefix;       // int64 [num_seqs + 1] block prefix over decode sequences
   size_t pitems;        // int2 [num_seqs + 1] prefill sequence table (region sized for max_prefill_items int4)
   size_t qrot;          // f16 [num_q_tokens][Hq][d] rotated, pre-scaled queries

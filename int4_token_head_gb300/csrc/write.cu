@@ -716,10 +716,11 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
         for (int t = 0; t < 2; t++) {
           const uint32_t pw = pk[t][q][rr];
           const float2 tq = f2fma(make_float2(__uint_as_float(pw * 65536u), __uint_as_float(pw & 0xffff0000u)), r2, magic2);
-          bytes[t] = (__float_as_uint(tq.y) * 16u + __float_as_uint(tq.x)) ^ 0x88u;  // (c_lo & 15) | (c_hi & 15) << 4
+          bytes[t] = __float_as_uint(tq.y) * 16u + __float_as_uint(tq.x);  // (c_lo + 8) | (c_hi + 8) << 4 (mod 16)
         }
-        // outputs 4cq..4cq+3 of group q = bytes 8q + 2cq, 8q + 2cq + 1
-        *reinterpret_cast<uint16_t*>(orow + 8 * q + 2 * cq) = (uint16_t)__byte_perm(bytes[0], bytes[1], 0x0040);
+        // outputs 4cq..4cq+3 of group q = bytes 8q + 2cq, 8q + 2cq + 1; the xor
+        // turns the four offset-binary nibbles into two's complement at once
+        *reinterpret_cast<uint16_t*>(orow + 8 * q + 2 * cq) = (uint16_t)(__byte_perm(bytes[0], bytes[1], 0x0040) ^ 0x8888u);
       }
       if (cq == 0 && r_slot[rr] >= 0) (r_kv[rr] ? v_scale : k_scale)[scale_off(geo, r_slot[rr], r_h[rr])] = sc;
     }
