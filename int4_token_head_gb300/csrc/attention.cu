@@ -302,7 +302,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
       uint32_t o[4];
 #pragma unroll
       for (int k = 0; k < 4; k++) {
-        const float2 y = __fmul2_rn(make_float2(x[8 * v + 2 * k], x[8 * v + 2 * k + 1]), qs);
+        // INT4: each 8-element group in the nibble order of the code words,
+        // (0, 4), (1, 5), (2, 6), (3, 7): the order the attention kernels'
+        // K tiles and fragments use, so that they read q' as stored
+        const float2 y = ROT ? __fmul2_rn(make_float2(x[8 * v + k], x[8 * v + k + 4]), qs)
+                             : __fmul2_rn(make_float2(x[8 * v + 2 * k], x[8 * v + 2 * k + 1]), qs);
         o[k] = pack_f16x2(y.x, y.y);
       }
       reinterpret_cast<uint4*>(dst)[v] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -558,12 +562,16 @@ __global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PrePa
           const uint32_t x = bok ? x0 : 0x88888888u;
           const uint32_t p0 = nib_to_f16x2(x), p1 = nib_to_f16x2(x >> 4), p2 = nib_to_f16x2(x >> 8),
                          p3 = nib_to_f16x2(x >> 12);
-          // p_k = (element k, element k+4) -> natural order 0..7
-          uint4 o;
-          o.x = __byte_perm(p0, p1, 0x5410);
-          o.y = __byte_perm(p2, p3, 0x5410);
-          o.z = __byte_perm(p0, p1, 0x7632);
-          o.w = __byte_perm(p2, p3, 0x7632);
+          // p_k = (element k, element k+4): K rows stay in this nibble order
+          // (q' is stored in it), V rows, whose dims are the output's, go to
+          // natural order 0..7
+          uint4 o = make_uint4(p0, p1, p2, p3);
+          if (which) {
+            o.x = __byte_perm(p0, p1, 0x5410);
+            o.y = __byte_perm(p2, p3, 0x5410);
+            o.z = __byte_perm(p0, p1, 0x7632);
+            o.w = __byte_perm(p2, p3, 0x7632);
+          }
           *reinterpret_cast<uint4*>(dst + w * 8) = o;
         } else {
           // four int8 codes: 0x64uu (u = c + 128) is 1024 + u, minus 1152 is c, exactly

@@ -352,15 +352,15 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
       const __half2 x16 = __float2half2_rn(16.f);
 #pragma unroll
       for (int w = 0; w < G::KW; w++) {
+        // q' is stored in nibble order: v = (e0, e4), (e1, e5), (e2, e6), (e3, e7)
         uint4 v = make_uint4(0, 0, 0, 0);
         if (colok) v = *reinterpret_cast<const uint4*>(qrow + 8 * (cq * G::KW + w));
-        uint32_t lo0 = __byte_perm(v.x, v.z, 0x5410), lo1 = __byte_perm(v.y, v.w, 0x5410);
-        __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&lo0), x16);
-        __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&lo1), x16);
+        __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&v.x), x16);
+        __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&v.z), x16);
         qb[2 * w][0] = *reinterpret_cast<uint32_t*>(&h0);
-        qb[2 * w][1] = __byte_perm(v.x, v.z, 0x7632);
+        qb[2 * w][1] = v.y;
         qb[2 * w + 1][0] = *reinterpret_cast<uint32_t*>(&h1);
-        qb[2 * w + 1][1] = __byte_perm(v.y, v.w, 0x7632);
+        qb[2 * w + 1][1] = v.w;
       }
     } else {
       // k-step s of this lane's quarter: dimensions cq D/4 + 4s + {0, 1} and + {2, 3}

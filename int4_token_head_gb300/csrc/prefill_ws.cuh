@@ -29,9 +29,9 @@
 //     and stages the bf16 rows over the Q' and K tiles for coalesced stores.
 // INT4 tiles keep each 8-element group in nibble order (elements 0,4,1,5,
 // 2,6,3,7: the two nibble lanes of a 32-bit word per f16x2, no byte
-// shuffles); Q' is stored with the same permutation, which leaves Q' K^T
-// unchanged, and the epilogue undoes it on O (its columns are V's dims) by
-// register renaming.
+// shuffles); the prep kernel stores Q' with the same permutation, which
+// leaves Q' K^T unchanged, and the epilogue undoes it on O (its columns are
+// V's dims) by register renaming.
 // Shared-memory operands: K-major tiles are [D/64 blocks][rows][128 bytes]
 // with the 16-byte chunk index XORed by row % 8 (1024-byte atoms; leading
 // byte offset unused, stride byte offset 1024); the V tiles use the same
@@ -222,27 +222,35 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
     regs_inc<160>();
     // phase bits of the barriers the role waits on (one completion per wait)
     uint32_t ph_sfull = 0, ph_odone = 0;
+    // the next item: (prefill sequence, tile in descending order of work, kv
+    // head, blocks), claimed and looked up by thread 0 when the current item's
+    // last PV is complete, so that the claim's atomic and search overlap the
+    // epilogue (claimed any earlier, items would wait behind busy CTAs)
+    auto claim = [&]() -> int4 {
+      const int itn = *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1);
+      int4 it = make_int4(-1, 0, 0, 0);
+      if (itn < n_items) {
+        int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pv.ptab[mid].y <= itn) lo = mid;
+          else hi = mid;
+        }
+        const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
+        const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
+        const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
+        const int t = ntiles - 1 - r / c.hkv;
+        const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
+        it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
+      }
+      return it;
+    };
+    int4 next_item = make_int4(-1, 0, 0, 0);
+    if (tid == 0) next_item = claim();
 #pragma unroll 1
     while (true) {
       if (tid == 0) {
-        // next item: (prefill sequence, tile in descending order of work, kv head)
-        const int itn = *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1);
-        int4 it = make_int4(-1, 0, 0, 0);
-        if (itn < n_items) {
-          int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (pv.ptab[mid].y <= itn) lo = mid;
-            else hi = mid;
-          }
-          const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
-          const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
-          const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
-          const int t = ntiles - 1 - r / c.hkv;
-          const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
-          it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
-        }
-        sitem[0] = it.x; sitem[1] = it.y; sitem[2] = it.z; sitem[3] = it.w;
+        sitem[0] = next_item.x; sitem[1] = next_item.y; sitem[2] = next_item.z; sitem[3] = next_item.w;
       }
       __syncthreads();
       const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
@@ -277,19 +285,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
           }
         }
         cp_async_commit();
-        cp_async_wait<0>();
-        if constexpr (FMT == kFmtInt4) {
-          // each thread reorders the chunks it copied into the tiles' nibble
-          // order: (q0, q4), (q1, q5), (q2, q6), (q3, q7)
-#pragma unroll 4
-          for (int u = tid; u < nrows * CPR; u += 256) {
-            const int rr = u / CPR, ch = u - rr * CPR;
-            uint4* pq = reinterpret_cast<uint4*>(sQ + sw128(ROWS, rr, ch));
-            const uint4 v = *pq;
-            *pq = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
-                             __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
-          }
-        }
+        cp_async_wait<0>();  // (INT4 q' arrives in the tiles' nibble order)
       }
       fence_proxy_async_smem();  // Q' is read by the tensor cores
       q_sync();
@@ -406,6 +402,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
       // ---- epilogue: normalise, inverse rotation (INT4), bf16 store ----
       ws_wait(bar(ODONE), ph_odone, abort_flag, c.status);
       ph_odone ^= 1;
+      if (tid == 0) next_item = claim();
       tc_fence_after();
       const bool live = l_run > 0.f;  // a row that saw no usable key is written as zeros
       const float inv = live ? 1.f / (l_run * (ROT ? (float)B : 1.f)) : 0.f;
