@@ -76,6 +76,8 @@ bool workspace_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_k
   L->max_prefill_items = (T / tile_tokens + S) * Hkv;
   L->pitems = off;
   off = align256(off + (size_t)L->max_prefill_items * 4 * sizeof(int32_t));
+  L->plist = off;
+  off = align256(off + (size_t)L->max_prefill_items * 2 * sizeof(int32_t));
   L->qrot = off;
   off = align256(off + (size_t)T * Hq * D * 2);
   L->direct_o = off;

@@ -49,6 +49,7 @@ struct PlanView {
   int4* dseq;         // decode sequences in order: (sequence id, seq_len, first query token, q_len)
   int64_t* dprefix;
   int2* ptab;         // prefill sequences in order: (seq id, index of its first item); [n_pseq].y = items
+  int2* plist;        // prefill (sequence, tile) pairs, longest first; pair i gives items i Hkv .. i Hkv + Hkv - 1
   __half* qrot;
   float* direct_o;
   float* direct_ml;
@@ -63,6 +64,7 @@ static PlanView plan_view(void* ws, const WorkspaceLayout& L) {
   v.dseq = reinterpret_cast<int4*>(b + L.dseq);
   v.dprefix = reinterpret_cast<int64_t*>(b + L.dprefix);
   v.ptab = reinterpret_cast<int2*>(b + L.pitems);
+  v.plist = reinterpret_cast<int2*>(b + L.plist);
   v.qrot = reinterpret_cast<__half*>(b + L.qrot);
   v.direct_o = reinterpret_cast<float*>(b + L.direct_o);
   v.direct_ml = reinterpret_cast<float*>(b + L.direct_ml);
@@ -127,6 +129,22 @@ __device__ __forceinline__ int first_block(const Common& c, int L, int ql) { ret
 
 __device__ __forceinline__ bool is_decode_kind(int qlen, const Common& c) {
   return c.group <= c.dcols && qlen * c.group <= c.dcols;
+}
+
+// keys that prefill tile t of a sequence (kv length L, q_len qn) attends:
+// up to its last query's causal horizon, or all
+__device__ __forceinline__ int prefill_tile_keys(const Common& c, int L, int qn, int t) {
+  return c.causal ? L - qn + min(qn, (t + 1) * c.tile_tokens) : L;
+}
+// prefill item itn in the prep kernel's longest-first order: (sequence, kv
+// head, tile, 16-key blocks), or sequence -1 past the last item
+__device__ __forceinline__ int4 prefill_item(const Common& c, const PlanView& pv, int itn, int n_items) {
+  if (itn >= n_items) return make_int4(-1, 0, 0, 0);
+  const int pi = itn / c.hkv;
+  const int2 st = pv.plist[pi];
+  const int qa = c.qsl[st.x], qn = c.qsl[st.x + 1] - qa;
+  const int keys = prefill_tile_keys(c, c.seq_lens[st.x], qn, st.y);
+  return make_int4(st.x, itn - pi * c.hkv, st.y, (keys + 15) / 16);
 }
 
 // ---------------------------------------------------------------------------
@@ -223,6 +241,45 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Common c, PlanView p
       pv.plan[1] = over ? 0 : (int)n_items;
       pv.plan[2] = 0;
       pv.plan[3] = n_pseq;
+    }
+    // the prefill (sequence, tile) pairs, longest first: a counting sort over
+    // buckets of 16-key blocks (descending), so that the longest items start
+    // first and the shortest fill the end of the launch (within a bucket the
+    // order is arbitrary; every item computes the same rows either way)
+    constexpr int kBuckets = 2048;
+    __shared__ int hist[kBuckets];
+    if (n_pseq > 0 && n_items <= c.max_items && n_items <= INT_MAX) {
+      int sh = 0;
+      while ((((long long)c.max_blocks + 1) >> sh) >= kBuckets) sh++;
+      auto bucket = [&](int nkb) { return kBuckets - 1 - min(kBuckets - 1, nkb >> sh); };
+      for (int i = threadIdx.x; i < kBuckets; i += kPrepThreads) hist[i] = 0;
+      __syncthreads();  // the sequence table and the histogram
+      for (int p = threadIdx.x; p < n_pseq; p += kPrepThreads) {
+        const int sq = pv.ptab[p].x, qn = c.qsl[sq + 1] - c.qsl[sq], Ls = c.seq_lens[sq];
+        const int nt = (qn + c.tile_tokens - 1) / c.tile_tokens;
+        for (int t = 0; t < nt; t++) atomicAdd(&hist[bucket((prefill_tile_keys(c, Ls, qn, t) + 15) / 16)], 1);
+      }
+      __syncthreads();
+      // exclusive prefix over the buckets: thread j owns buckets [8j, 8j + 8)
+      constexpr int PER = kBuckets / kPrepThreads;
+      int mine = 0;
+#pragma unroll
+      for (int i = 0; i < PER; i++) mine += hist[threadIdx.x * PER + i];
+      int total;
+      int run = block_exclusive_scan<int>(mine, &total, s_i32);
+#pragma unroll
+      for (int i = 0; i < PER; i++) {
+        const int hb = hist[threadIdx.x * PER + i];
+        hist[threadIdx.x * PER + i] = run;
+        run += hb;
+      }
+      __syncthreads();
+      for (int p = threadIdx.x; p < n_pseq; p += kPrepThreads) {
+        const int sq = pv.ptab[p].x, qn = c.qsl[sq + 1] - c.qsl[sq], Ls = c.seq_lens[sq];
+        const int nt = (qn + c.tile_tokens - 1) / c.tile_tokens;
+        for (int t = 0; t < nt; t++)
+          pv.plist[atomicAdd(&hist[bucket((prefill_tile_keys(c, Ls, qn, t) + 15) / 16)], 1)] = make_int2(sq, t);
+      }
     }
     return;
   }
@@ -456,28 +513,13 @@ __global__ void __launch_bounds__(PreGeom<D, FMT>::THREADS) prefill_kernel(PrePa
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
   for (int i = tid; i < D; i += G::THREADS) ssign[i] = (ROT && c.signs[i] < 0) ? -1.f : 1.f;
-  const int n_items = pv.plan[1], n_pseq = pv.plan[3];
+  const int n_items = pv.plan[1];
 
 #pragma unroll 1
   while (true) {
     if (tid == 0) {
-      // next item: (prefill sequence, tile in descending order of work, kv head)
-      const int itn = atomicAdd(&pv.plan[2], 1);
-      int4 it = make_int4(-1, 0, 0, 0);
-      if (itn < n_items) {
-        int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (pv.ptab[mid].y <= itn) lo = mid;
-          else hi = mid;
-        }
-        const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
-        const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
-        const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
-        const int t = ntiles - 1 - r / c.hkv;
-        const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
-        it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
-      }
+      // next item, longest first: (prefill sequence, kv head, tile, blocks)
+      const int4 it = prefill_item(c, pv, atomicAdd(&pv.plan[2], 1), n_items);
       sitem[0] = it.x; sitem[1] = it.y; sitem[2] = it.z; sitem[3] = it.w;
     }
     __syncthreads();

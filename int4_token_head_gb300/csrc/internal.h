@@ -145,6 +145,7 @@ struct WorkspaceLayout {
   size_t dseq;          // int4 [num_seqs] decode sequences: (sequence id, seq_len, first query token, q_len)
   size_t dprefix;       // int64 [num_seqs + 1] block prefix over decode sequences
   size_t pitems;        // int2 [num_seqs + 1] prefill sequence table (region sized for max_prefill_items int4)
+  size_t plist;         // int2 [max_prefill_items] prefill (sequence-table index, tile) pairs, longest first
   size_t qrot;          // f16 [num_q_tokens][Hq][d] rotated, pre-scaled queries
   size_t direct_o;      // f32 [num_seqs][Hkv][8][d]
   size_t direct_ml;     // f32 [num_seqs][Hkv][8][2]

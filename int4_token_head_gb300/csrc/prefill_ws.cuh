@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
   // registers: the launch gives 128 a thread to all four warpgroups (65,536);
   // the softmax warpgroups take 168, the dequant/MMA ones keep 88
   // (2 x 128 x 168 + 2 x 128 x 88 = 65,536: the increase can always be met)
-  const int n_items = pv.plan[1], n_pseq = pv.plan[3];
+  const int n_items = pv.plan[1];
   // each role runs its own item loop (the same items, the same CTA-wide
   // barriers), so that the register budget set for its warpgroups covers
   // only its own code
@@ -222,28 +222,12 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
     regs_inc<160>();
     // phase bits of the barriers the role waits on (one completion per wait)
     uint32_t ph_sfull = 0, ph_odone = 0;
-    // the next item: (prefill sequence, tile in descending order of work, kv
-    // head, blocks), claimed and looked up by thread 0 when the current item's
+    // the next item, longest first: (prefill sequence, kv head, tile,
+    // blocks), claimed and looked up by thread 0 when the current item's
     // last PV is complete, so that the claim's atomic and search overlap the
     // epilogue (claimed any earlier, items would wait behind busy CTAs)
     auto claim = [&]() -> int4 {
-      const int itn = *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1);
-      int4 it = make_int4(-1, 0, 0, 0);
-      if (itn < n_items) {
-        int lo = 0, hi = n_pseq;  // ptab[lo].y <= itn < ptab[hi].y
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (pv.ptab[mid].y <= itn) lo = mid;
-          else hi = mid;
-        }
-        const int s = pv.ptab[lo].x, r = itn - pv.ptab[lo].y;
-        const int qa = c.qsl[s], qn = c.qsl[s + 1] - qa, Ls = c.seq_lens[s];
-        const int ntiles = (qn + c.tile_tokens - 1) / c.tile_tokens;
-        const int t = ntiles - 1 - r / c.hkv;
-        const int keys = c.causal ? Ls - qn + min(qn, (t + 1) * c.tile_tokens) : Ls;
-        it = make_int4(s, r % c.hkv, t, (keys + 15) / 16);
-      }
-      return it;
+      return prefill_item(c, pv, *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1), n_items);
     };
     int4 next_item = make_int4(-1, 0, 0, 0);
     if (tid == 0) next_item = claim();
