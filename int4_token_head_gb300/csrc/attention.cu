@@ -413,40 +413,82 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
 #pragma unroll
   for (int k = 0; k < PER; k++) acc[k] = 0.f;
   float M = -INFINITY, Lsum = 0.f;
-  // a piece's columns col, col + dcols, ... hold the same query over
-  // disjoint key blocks
-  auto merge_slot = [&](const float* o_base, const float* ml_base) {
-    for (int sub = 0; sub < c.np; sub++) {
-      const int cc = col + sub * c.dcols;
-      const float* ow = o_base + cc * D;
-      const float mw = ml_base[cc * 2], lw = ml_base[cc * 2 + 1];
-      const float Mn = fmaxf(M, mw);
-      const float Mu = Mn == -INFINITY ? 0.f : Mn;
-      const float a = fast_exp2(M - Mu), b = fast_exp2(mw - Mu);
-#pragma unroll
-      for (int k = 0; k < PER; k++) acc[k] = acc[k] * a + ow[lane + 32 * k] * b;
-      Lsum = Lsum * a + lw * b;
-      M = Mn;
-    }
+  // The pieces (the direct slot of the piece that starts the segment, then
+  // every CTA whose non-empty range starts strictly inside it) are merged a
+  // chunk at a time: all of a chunk's loads are issued before any of its
+  // arithmetic (the chunk's largest maximum first, then every piece weighted
+  // by 2^(m - that maximum)), so a segment's pieces cost one or two memory
+  // round trips instead of one each.  A piece's columns col, col + dcols, ...
+  // hold the same query over disjoint key blocks.
+  constexpr int CH = 4;  // pieces per chunk
+  int64_t chunk[CH];     // piece slots: -1 the direct slot, else the CTA slot index
+  int nch = 0;
+  auto o_of = [&](int64_t sl) {
+    return sl < 0 ? pv.direct_o + (long long)seg * kDecodeCols * D : pv.warp_o + sl * kDecodeCols * D;
   };
-  merge_slot(pv.direct_o + (long long)seg * kDecodeCols * D, pv.direct_ml + (long long)seg * kDecodeCols * 2);
+  auto ml_of = [&](int64_t sl) {
+    return sl < 0 ? pv.direct_ml + (long long)seg * kDecodeCols * 2 : pv.warp_ml + sl * kDecodeCols * 2;
+  };
+  auto merge_chunk = [&]() {
+    float mw[CH][2], lw[CH][2], ov[CH][2][PER];
+#pragma unroll
+    for (int j = 0; j < CH; j++) {
+#pragma unroll
+      for (int sub = 0; sub < 2; sub++) {
+        const bool use = j < nch && sub < c.np;
+        const int cc = col + sub * c.dcols;
+        const float* ml = ml_of(use ? chunk[j] : -1);
+        const float* o = o_of(use ? chunk[j] : -1);
+        mw[j][sub] = use ? ml[cc * 2] : -INFINITY;
+        lw[j][sub] = use ? ml[cc * 2 + 1] : 0.f;
+#pragma unroll
+        for (int k = 0; k < PER; k++) ov[j][sub][k] = use ? o[cc * D + lane + 32 * k] : 0.f;
+      }
+    }
+    float Mc = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < CH; j++) Mc = fmaxf(Mc, fmaxf(mw[j][0], mw[j][1]));
+    const float Mn = fmaxf(M, Mc);
+    const float Mu = Mn == -INFINITY ? 0.f : Mn;
+    const float a = fast_exp2(M - Mu);
+#pragma unroll
+    for (int k = 0; k < PER; k++) acc[k] *= a;
+    Lsum *= a;
+#pragma unroll
+    for (int j = 0; j < CH; j++) {
+#pragma unroll
+      for (int sub = 0; sub < 2; sub++) {
+        const float wgt = fast_exp2(mw[j][sub] - Mu);  // 0 for an unused entry
+#pragma unroll
+        for (int k = 0; k < PER; k++) acc[k] += ov[j][sub][k] * wgt;
+        Lsum += lw[j][sub] * wgt;
+      }
+    }
+    M = Mn;
+    nch = 0;
+  };
+  auto add_piece = [&](int64_t sl) {
+#pragma unroll
+    for (int j = 0; j < CH; j++)
+      if (j == nch) chunk[j] = sl;  // a register, not local memory
+    if (++nch == CH) merge_chunk();
+  };
+  add_piece(-1);
   // the other pieces: CTAs whose non-empty range starts strictly inside the
   // segment.  Walk the CTAs or the positions, whichever are fewer.
-  auto merge_cta = [&](long long w) {
-    const long long slot = w * c.hg + hl;
-    merge_slot(pv.warp_o + slot * kDecodeCols * D, pv.warp_ml + slot * kDecodeCols * 2);
-  };
+  auto add_cta = [&](long long w) { add_piece(w * c.hg + hl); };
   const long long w_first = div_nn((sbeg + 1) * W + Tu - 1, Tu);  // first CTA starting after sbeg
   const long long w_end = div_nn(send * W + Tu - 1, Tu);          // first CTA starting at or after send
   if (w_end - w_first <= send - sbeg - 1) {
     for (long long w = w_first; w < w_end; w++)
-      if (wstart(w + 1) > wstart(w)) merge_cta(w);
+      if (wstart(w + 1) > wstart(w)) add_cta(w);
   } else {
     for (long long p = sbeg + 1; p < send; p++) {
       const long long w = div_nn((p + 1) * W + Tu - 1, Tu) - 1;  // last CTA starting at or before p
-      if (wstart(w) == p) merge_cta(w);
+      if (wstart(w) == p) add_cta(w);
     }
   }
+  if (nch > 0) merge_chunk();
   float* r = srow[warp];
   const float inv = 1.f / (Lsum * (ROT ? (float)B : 1.f));
 #pragma unroll
