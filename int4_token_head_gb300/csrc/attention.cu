@@ -925,10 +925,10 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   // decode is sized for single-token queries and longer ones go to prefill.
   const bool any_decode = c.group <= kDecodeCols;
   int dec_occ = 0;
-  // the deeper decode ring serves the separate-scale layout with four heads
-  // per CTA and 16-byte aligned scale rows; the in-slot layout's eight-head
-  // CTAs read better with the shallower one (measured on GB300: in-slot
-  // decode 2.20 vs 2.63 ms)
+  // the 16-byte scale rows (and at INT4 d = 128 the deeper decode ring)
+  // serve the separate-scale layout with four heads per CTA and 16-byte
+  // aligned scale rows; the in-slot layout's eight-head CTAs read better with
+  // the shallower ring (measured on GB300: in-slot decode 2.20 vs 2.63 ms)
   const bool dec_deep = !inslot && c.hg == 4 && (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0 &&
                         (reinterpret_cast<uintptr_t>(a.v_scale) & 15) == 0 && (a.geo.srow * 4) % 16 == 0 &&
                         (a.geo.sblk * 4) % 16 == 0 && a.geo.shead == 1;

@@ -607,9 +607,9 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
 __host__ __device__ constexpr int decode_max_regs(int d, int fmt) {
   return d <= 96 ? 128 : (d <= 128 || (d <= 192 && fmt == kFmtInt4)) ? 168 : 255;
 }
-template <int D, int NP, int FMT>
+template <int D, int NP, int FMT, bool DEEP = false>
 __global__ void __maxnreg__(decode_max_regs(D, FMT)) decode_kernel(DecParams prm) {
-  decode_body<D, NP, FMT, false>(prm);
+  decode_body<D, NP, FMT, DEEP>(prm);
 }
 // INT4 head size 128 (the long-context shape): at most 128 registers a
 // thread, so that four 4-warp CTAs (or two 8-warp ones) share an SM
@@ -617,12 +617,15 @@ template <int NP, bool DEEP>
 __global__ void __launch_bounds__(256, 2) decode_kernel_i4d128(DecParams prm) {
   decode_body<128, NP, kFmtInt4, DEEP>(prm);
 }
-// The decode kernel for a format and head size, with the deeper ring and the
-// 16-byte scale rows where it has them (`deep`), and its dynamic shared
-// memory for hg heads per CTA.
+// The decode kernel for a format and head size, with the 16-byte scale rows
+// (and, for 64-byte code rows, the deeper ring) where it has them (`deep`),
+// and its dynamic shared memory for hg heads per CTA.  INT4 head size 128
+// takes them with paired blocks, where the deeper ring changes the slot
+// count; the other INT4 head sizes take the scale rows alone.
 template <int D, int NP, int FMT>
 struct DecodeEntry {
-  static constexpr bool HAS_DEEP = FMT == kFmtInt4 && D == 128 && DecGeom<D, NP, FMT, true>::NS != DecGeom<D, NP, FMT>::NS;
+  static constexpr bool HAS_DEEP =
+      FMT == kFmtInt4 && (D != 128 || DecGeom<D, NP, FMT, true>::NS != DecGeom<D, NP, FMT>::NS);
   static void (*kernel(bool deep))(DecParams) {
     if constexpr (FMT == kFmtInt4 && D == 128) {
       if constexpr (HAS_DEEP) {
@@ -630,7 +633,10 @@ struct DecodeEntry {
       }
       return decode_kernel_i4d128<NP, false>;
     } else {
-      return decode_kernel<D, NP, FMT>;
+      if constexpr (HAS_DEEP) {
+        if (deep) return decode_kernel<D, NP, FMT, true>;
+      }
+      return decode_kernel<D, NP, FMT, false>;
     }
   }
   static int smem(bool deep, int hg) {

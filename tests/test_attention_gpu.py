@@ -48,6 +48,9 @@ CASES = [
     ("decode_d192_g4", 16, 4, 192, [(1, 500), (1, 17)], True),
     ("decode_d64_g8", 16, 2, 64, [(1, 90), (1, 250)], True),
     ("decode_d256_g2", 4, 2, 256, [(1, 77), (1, 160)], True),
+    ("decode_d64_four_heads_per_cta", 16, 4, 64, [(1, 90), (1, 250), (1, 7)], True),
+    ("decode_d256_four_heads_per_cta", 8, 4, 256, [(1, 77), (1, 160)], True),
+    ("decode_d96_spec_q2", 8, 8, 96, [(2, 70), (1, 33)], True),
     ("spec_q2_g4_decode_path", 8, 2, 128, [(2, 50), (2, 2), (1, 40)], True),
     ("q3_g4_prefill_path", 8, 2, 128, [(3, 50), (3, 3)], True),
     ("prefill_d128_g4", 16, 4, 128, [(40, 40), (70, 100), (5, 5)], True),
