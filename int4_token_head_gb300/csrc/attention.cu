@@ -108,6 +108,7 @@ struct Common {
   int tile_tokens;  // prefill: query tokens per 64-row tile
   int hg;           // decode: kv heads per CTA (largest divisor of hkv <= 8)
   int ng;           // decode: head groups per sequence (hkv / hg)
+  int nl;           // decode: lanes (a divisor of ng): CTA r serves the head groups = r mod nl
   int np;           // decode: 16-key blocks per schedule position (1 or 2)
   int dcols;        // decode: query columns per block (8 / np); longer queries go to prefill
   long long max_items;  // capacity of the prefill item list
@@ -403,9 +404,11 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   const int nblk = (di.y + 15) / 16;
   const int npos = (nblk - first_block(c, di.y, ql) + c.np - 1) / c.np;
   const int grp = h / c.hg, hl = h - grp * c.hg;
-  const long long Tu = pv.dprefix[n_dseq] * c.ng;
-  const long long sbeg = pv.dprefix[i] * c.ng + (long long)grp * npos, send = sbeg + npos;
-  const int W = prm.num_ctas;
+  // the lane of the segment's head group, and the group's place in its lane
+  const int gpl = c.ng / c.nl, lane_g = grp % c.nl, gs = grp / c.nl;
+  const long long Tu = pv.dprefix[n_dseq] * gpl;
+  const long long sbeg = pv.dprefix[i] * gpl + (long long)gs * npos, send = sbeg + npos;
+  const int W = prm.num_ctas / c.nl;  // the lane's CTAs
   auto wstart = [&](long long w) { return div_nn(Tu * w, W); };
 
   constexpr int PER = D / 32;
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   add_piece(-1);
   // the other pieces: CTAs whose non-empty range starts strictly inside the
   // segment.  Walk the CTAs or the positions, whichever are fewer.
-  auto add_cta = [&](long long w) { add_piece(w * c.hg + hl); };
+  auto add_cta = [&](long long w) { add_piece((w * c.nl + lane_g) * c.hg + hl); };
   const long long w_first = div_nn((sbeg + 1) * W + Tu - 1, Tu);  // first CTA starting after sbeg
   const long long w_end = div_nn(send * W + Tu - 1, Tu);          // first CTA starting at or after send
   if (w_end - w_first <= send - sbeg - 1) {
@@ -917,6 +920,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
       break;
     }
   c.ng = a.num_kv_heads / c.hg;
+  c.nl = 1;
   if (c.group > kPrefillRows) return KV_INT4_ERR_HEADS;
 
   // decode configuration: blocks per schedule position and the kernel's
@@ -970,6 +974,18 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   if (any_decode) {
     long long grid = (long long)sms * dec_occ;
     if (grid * c.hg > kMaxDecodeWarps) grid = kMaxDecodeWarps / c.hg;
+    // lanes: the CTAs of all (or as many as divide evenly) head groups walk
+    // the same positions side by side, so the groups' slices of a block's
+    // code and scale rows are read together and each cache line leaves DRAM
+    // once (measured on GB300, Phi-3 shape, 32 kv heads in 8 groups: DRAM
+    // reads 1.79x the cache bytes when a CTA walks its groups one after the
+    // other)
+    for (int l = (int)(grid < c.ng ? grid : c.ng); l >= 1; l--)
+      if (c.ng % l == 0) {
+        c.nl = l;
+        break;
+      }
+    grid = grid / c.nl * c.nl;
     dec_grid = (int)grid;
   }
 

@@ -47,10 +47,11 @@ struct DecGeom {
   static_assert(WAIT >= 0 && NS <= 8, "slot ring");
 };
 
-// Walk over the decode units (sequence i, head group grp, position kp).
+// Walk over a lane's decode units (sequence i, head group grp, position kp).
 struct DecWalk {
   int i;      // index into the decode-sequence list
-  int grp;    // head group
+  int grp;    // head group (= lane mod nl)
+  int lane;   // the CTA's lane
   int kp;     // position within the sequence
   int npos;   // positions of the sequence
   int nblk;   // 16-key blocks of the sequence
@@ -71,8 +72,8 @@ template <int NP>
 __device__ __forceinline__ void walk_next(DecWalk& w, const Common& c, const PlanView& pv) {
   if (++w.kp == w.npos) {
     w.kp = 0;
-    if (++w.grp == c.ng) {
-      w.grp = 0;
+    if ((w.grp += c.nl) >= c.ng) {
+      w.grp = w.lane;
       ++w.i;
       walk_load<NP>(w, c, pv);
     }
@@ -164,8 +165,13 @@ struct DecParams {
   int num_ctas;
 };
 
-// Work decomposition: stream-K over the flattened (decode sequence, head
-// group, position) units; CTA r takes units [T*r/R, T*(r+1)/R).  A CTA has
+// Work decomposition: nl lanes (nl divides the head-group count; as a rule
+// every group has its own lane), CTA r in lane r mod nl.  Each lane runs
+// stream-K over its flattened (decode sequence, head group, position) units:
+// the lane's k-th CTA takes units [T*k/R, T*(k+1)/R) of its T, with R the
+// lane's CTAs.  The lanes' ranges line up, so the CTAs that read the
+// different head groups' slices of one block do so at about the same time
+// and the cache lines they share are read from DRAM once.  A CTA has
 // one warp per kv head of the group; for every block all its threads copy
 // the block's codes and scales of the group's heads -- contiguous runs of the
 // cache -- into per-head padded tiles, and each warp then computes its own
@@ -200,18 +206,22 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
 
   const int n_dseq = pv.plan[0];
   if (n_dseq == 0) return;
-  const long long Tu = pv.dprefix[n_dseq] * c.ng;
-  const int R = prm.num_ctas;
-  const long long P0 = Tu * blockIdx.x / R, P1 = Tu * (blockIdx.x + 1) / R;
+  // lane blockIdx.x mod nl: its head groups, the lane's (blockIdx.x / nl)-th
+  // share of their units
+  const int gpl = c.ng / c.nl;  // head groups per lane
+  const int my_lane = blockIdx.x % c.nl, rr = blockIdx.x / c.nl;
+  const long long Tu = pv.dprefix[n_dseq] * gpl;
+  const int R = prm.num_ctas / c.nl;
+  const long long P0 = Tu * rr / R, P1 = Tu * (rr + 1) / R;
   if (P0 >= P1) return;
   const int nunits = (int)(P1 - P0);
 
-  // locate P0: largest i with dprefix[i] * ng <= P0 (32-ary search, per warp)
+  // locate P0: largest i with dprefix[i] * gpl <= P0 (32-ary search, per warp)
   int lo = 0, hi = n_dseq;  // invariant: key(lo) <= P0 < key(hi)
   while (hi - lo > 1) {
     const long long span = hi - lo;
     const int probe = lo + (int)((span * lane) / 32);
-    const bool le = lane == 0 || pv.dprefix[probe] * c.ng <= P0;
+    const bool le = lane == 0 || pv.dprefix[probe] * gpl <= P0;
     const unsigned m = __ballot_sync(0xffffffffu, le);
     const int last = 31 - __clz(m);
     const int nlo = lo + (int)((span * last) / 32);
@@ -221,11 +231,13 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
   }
   DecWalk cw;
   cw.i = lo;
+  cw.lane = my_lane;
   walk_load<NP>(cw, c, pv);
   {
-    const long long off = P0 - pv.dprefix[cw.i] * c.ng;
-    cw.grp = (int)(off / cw.npos);
-    cw.kp = (int)(off - (long long)cw.grp * cw.npos);
+    const long long off = P0 - pv.dprefix[cw.i] * gpl;
+    const int gs = (int)(off / cw.npos);
+    cw.grp = gs * c.nl + my_lane;
+    cw.kp = (int)(off - (long long)gs * cw.npos);
   }
   DecWalk pw = cw;
 
