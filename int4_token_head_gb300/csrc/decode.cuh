@@ -24,9 +24,10 @@ struct DecGeom {
   // ring of single-block slots: NP consumed per iteration, the rest in
   // flight.  The copies in flight per SM set the decode's pace; DEEP (four
   // heads per CTA, four CTAs per SM, separate 16-byte aligned scales) takes
-  // one more slot, which the smaller swizzled slots leave room for, and
-  // stages a block's scales as 16-byte rows of the group's four heads
-  static constexpr int NS = NP == 1 ? 4 : 2 * NP + (VSWZ && DEEP ? 2 : 1);
+  // one more slot where the slots are small enough to keep four CTAs per SM
+  // (swizzled 64-byte rows, or rows of at most 48 bytes), and stages a
+  // block's scales as 16-byte rows of the group's four heads
+  static constexpr int NS = NP == 1 ? 4 : 2 * NP + (DEEP && (VSWZ || CB <= 48) ? 2 : 1);
   static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
   static constexpr int KROW = CB;           // K tile row stride (bytes)
   // V tile row stride: an odd multiple of 16 bytes, so that the 8 rows of
