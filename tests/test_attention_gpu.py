@@ -61,6 +61,12 @@ CASES = [
     ("mixed_any_order", 16, 4, 192, [(1, 300), (60, 60), (1, 45), (25, 200), (1, 1)], True),
     ("noncausal_prefill", 8, 2, 128, [(20, 60), (7, 7)], False),
     ("decode_g16_prefill_kernel", 32, 2, 128, [(1, 100), (1, 33)], True),
+    # decode lanes: head-group counts that are not powers of two (3 groups of
+    # four heads, 7 groups of one), and more groups than CTAs, where each lane
+    # walks several groups (609 groups of four heads: 203 lanes of 3)
+    ("decode_three_head_groups", 12, 12, 128, [(1, 90), (1, 300), (1, 5)], True),
+    ("decode_seven_head_groups", 14, 7, 64, [(1, 120), (1, 33)], True),
+    ("decode_groups_beyond_grid", 2436, 2436, 64, [(1, 20), (1, 37)], True),
 ]
 
 
