@@ -300,8 +300,12 @@ KVINT4_API int kv_int4_attention_noalloc(const void* q, int64_t q_token_stride,
  * per-token-head KV slots).  Reading taken: with CB code bytes per head
  * vector (head_size / 2 for INT4, head_size for int8) a slot is
  *   P = kv_int4_inslot_slot_bytes(head_size, int8) = round_up(CB + 4, 16) bytes:
- * codes at [0, CB), the f32 scale at [CB, CB + 4), padding after (never read
- * or written); the cache is uint8 [num_blocks][2 (K, V)][block_size]
+ * codes at [0, CB), the f32 scale at [CB, CB + 4), padding after (CB is a
+ * multiple of 16, so the scale and the padding are the slot's last 16
+ * bytes: a write stores them together, the scale then zeros, so that it
+ * writes whole DRAM sectors; attention never reads the padding, and the
+ * padding of slots no write touches keeps its bytes); the cache is uint8
+ * [num_blocks][2 (K, V)][block_size]
  * [num_kv_heads][P], 16-byte aligned: the codes of token slot s, kv head h,
  * half kv (0: K, 1: V) start at byte
  *   (((s / 16) * 2 + kv) * 16 + s % 16) * num_kv_heads * P + h * P

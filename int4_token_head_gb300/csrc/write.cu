@@ -242,7 +242,7 @@ write_kernel(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* _
         uint4* dst = reinterpret_cast<uint4*>(cache + code_off(geo, slot, h) + (blk * B + jj * SEG) / 2);
 #pragma unroll
         for (int q = 0; q < SEG / 32; q++) dst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-        if (j == 0) (kv ? v_scale : k_scale)[scale_off(geo, slot, h)] = sc;
+        if (j == 0) store_scale((kv ? v_scale : k_scale) + scale_off(geo, slot, h), geo, sc);
       }
     }
     __syncthreads();  // the stage (and the absmax buffer) may now be overwritten
@@ -449,7 +449,7 @@ write_kernel_tok(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_
         uint4* dst = reinterpret_cast<uint4*>(u_cache + code_off(geo, slot, u_h) + (blk * B + jj * SEG) / 2);
 #pragma unroll
         for (int q = 0; q < SEG / 32; q++) dst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-        if (j == 0) u_scale[scale_off(geo, slot, u_h)] = sc;
+        if (j == 0) store_scale(u_scale + scale_off(geo, slot, u_h), geo, sc);
       }
     }
     __syncthreads();  // the stage (and the absmax buffer) may now be overwritten
@@ -722,7 +722,7 @@ write_kernel_tc(const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t
         // turns the four offset-binary nibbles into two's complement at once
         *reinterpret_cast<uint16_t*>(orow + 8 * q + 2 * cq) = (uint16_t)(__byte_perm(bytes[0], bytes[1], 0x0040) ^ 0x8888u);
       }
-      if (cq == 0 && r_slot[rr] >= 0) (r_kv[rr] ? v_scale : k_scale)[scale_off(geo, r_slot[rr], r_h[rr])] = sc;
+      if (cq == 0 && r_slot[rr] >= 0) store_scale((r_kv[rr] ? v_scale : k_scale) + scale_off(geo, r_slot[rr], r_h[rr]), geo, sc);
     }
     __syncwarp();
     // 16-byte stores: the quad of rows g, g + 8 stores those rows' chunks

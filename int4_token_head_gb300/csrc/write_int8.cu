@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kI8Warps * 32) write_int8_kernel(I8Args a) {
       const bool kv = unit[u] >= a.hkv;
       const int h = kv ? unit[u] - a.hkv : unit[u];
       *reinterpret_cast<uint4*>((kv ? a.v_cache : a.k_cache) + code_off(a.geo, slot, h) + 16 * c) = codes;
-      if (c == 0) (kv ? a.v_scale : a.k_scale)[scale_off(a.geo, slot, h)] = sc;
+      if (c == 0) store_scale((kv ? a.v_scale : a.k_scale) + scale_off(a.geo, slot, h), a.geo, sc);
     }
   }
 }

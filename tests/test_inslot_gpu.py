@@ -4,8 +4,10 @@ f32 scale in every P-byte slot) for both formats, through the C ABI.
 The layout only moves bytes, so the in-slot paths must reproduce the
 separate-layout paths exactly: writes byte for byte (after the oracle's
 to_inslot packing of the separate caches), attention bit for bit on the
-same cache contents (same kernels, same schedule).  The padding bytes of
-every slot are never written."""
+same cache contents (same kernels, same schedule).  A write stores a slot's
+scale and the padding after it as the slot's last 16 bytes (the scale, then
+zeros); the padding of slots no write touched keeps its bytes, and
+attention never reads padding (the attention cases fill it with PAD)."""
 
 import math
 
@@ -20,6 +22,15 @@ from tests.helpers import assert_close_attention, oracle_attention, oracle_write
 
 pytestmark = pytest.mark.gpu
 PAD = 0xEE
+
+
+def _written_padding_zeroed(want, slots, cb):
+    """The in-slot cache a write leaves: want (built with PAD padding) with
+    the padding of every written slot (both halves, every head) zeroed."""
+    for s_ in np.asarray(slots):
+        if s_ >= 0:
+            want[s_ // 16, :, s_ % 16, :, cb + 4:] = 0
+    return want
 
 
 @pytest.mark.parametrize("int8", [False, True])
@@ -51,6 +62,7 @@ def test_inslot_write_matches_separate_write(d, hkv, int8):
     torch.cuda.synchronize()
     assert status.item() == 0
     want = O.to_inslot(kc.cpu().numpy(), vc.cpu().numpy(), ks.cpu().numpy(), vs.cpu().numpy(), fill=PAD)
+    want = _written_padding_zeroed(want, slots.cpu().numpy(), cb)
     assert np.array_equal(ins.cpu().numpy(), want)
 
 
@@ -69,7 +81,8 @@ def test_inslot_int8_write_matches_the_oracle():
                                        fill=PAD)).cuda()
     _lib.write_inslot(k.cuda(), v.cuda(), slots.cuda(), ins, int8=True)
     torch.cuda.synchronize()
-    assert np.array_equal(ins.cpu().numpy(), O.to_inslot(kc, vc, ks, vs, fill=PAD))
+    want = _written_padding_zeroed(O.to_inslot(kc, vc, ks, vs, fill=PAD), slots.numpy(), d)
+    assert np.array_equal(ins.cpu().numpy(), want)
 
 
 ATT_CASES = [
