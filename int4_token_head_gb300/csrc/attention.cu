@@ -389,7 +389,6 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   const Common& c = prm.c;
   const PlanView& pv = prm.pv;
   constexpr int B = Head<D>::b;
-  __shared__ float srow[kDecodeCols][D];
   // a warp per (segment, query column): the CTA's dcols warps cover
   // dcols / cps segments of cps columns each
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -492,29 +491,42 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
     }
   }
   if (nch > 0) merge_chunk();
-  float* r = srow[warp];
+  // normalise, then D (I_n (x) H_b) (.) / b in registers: element e = lane +
+  // 32 k of the head vector is acc[k] of lane e % 32, and a butterfly stage of
+  // span hs pairs e with e ^ hs (Sylvester order) -- across lanes by warp
+  // shuffles for spans below 32, across this lane's registers above
   const float inv = 1.f / (Lsum * (ROT ? (float)B : 1.f));
 #pragma unroll
-  for (int k = 0; k < PER; k++) r[lane + 32 * k] = acc[k] * inv;
-  __syncwarp();
+  for (int k = 0; k < PER; k++) acc[k] *= inv;
   if constexpr (ROT) {
-#pragma unroll 1
-    for (int hh = 1; hh < B; hh <<= 1) {
-      for (int p = lane; p < D / 2; p += 32) {
-        const int ii = (p / hh) * 2 * hh + (p % hh);
-        const float a = r[ii], b = r[ii + hh];
-        r[ii] = a + b;
-        r[ii + hh] = a - b;
+#pragma unroll
+    for (int hs = 1; hs < (B < 32 ? B : 32); hs <<= 1) {
+      const bool upper = (lane & hs) != 0;
+#pragma unroll
+      for (int k = 0; k < PER; k++) {
+        const float o = __shfl_xor_sync(0xffffffffu, acc[k], hs);
+        acc[k] = upper ? o - acc[k] : acc[k] + o;
       }
-      __syncwarp();
+    }
+#pragma unroll
+    for (int hs = 32; hs < B; hs <<= 1) {
+      const int hk = hs / 32;
+#pragma unroll
+      for (int k = 0; k < PER; k++)
+        if (!(k & hk)) {
+          const float a = acc[k], b = acc[k + hk];
+          acc[k] = a + b;
+          acc[k + hk] = a - b;
+        }
     }
   }
   const int j = col / c.group, jj = col - j * c.group;
   uint16_t* dst = c.out + (long long)(q0 + j) * c.out_stride + (long long)(h * c.group + jj) * D;
-  for (int p = lane; p < D / 2; p += 32) {
-    const float x0 = (ROT && c.signs[2 * p] < 0) ? -r[2 * p] : r[2 * p];
-    const float x1 = (ROT && c.signs[2 * p + 1] < 0) ? -r[2 * p + 1] : r[2 * p + 1];
-    reinterpret_cast<uint32_t*>(dst)[p] = pack_bf16x2_rn(x0, x1);
+#pragma unroll
+  for (int k = 0; k < PER; k++) {
+    const int e = lane + 32 * k;
+    const float x = (ROT && c.signs[e] < 0) ? -acc[k] : acc[k];
+    dst[e] = (uint16_t)(pack_bf16x2_rn(x, 0.f) & 0xffffu);  // coalesced: a warp writes 64 contiguous bytes per k
   }
 }
 
