@@ -919,11 +919,12 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
   // staging ring fits in shared memory (int8 tiles are twice as large).
   // Four 4-warp CTAs per SM beat two 8-warp ones (independent barrier
   // domains; measured on GB300: long-context decode 0.76 vs 0.73 of the HBM
-  // peak); the in-slot layout keeps up to 8, its unaligned slots read
-  // better in longer contiguous runs
+  // peak), for the in-slot layout too since the head-group lanes put the
+  // CTAs reading one row's slots side by side (long-context in-slot decode
+  // 2.226 -> 2.200 ms, Phi-3 46.6 -> 43.3 us against eight-head CTAs)
   constexpr int kMaxSmem = 227 * 1024;
   const bool inslot = a.geo.chead != (FMT == kFmtInt8 ? D : D / 2);
-  int hg_cap = inslot ? 8 : 4;
+  int hg_cap = 4;
   while (hg_cap > 1 && DecGeom<D, 1, FMT>::smem_bytes(hg_cap) > kMaxSmem) hg_cap--;
   c.hg = 1;
   for (int h = hg_cap; h >= 1; h--)
