@@ -90,3 +90,25 @@ def check_sampled_end_to_end(w, q, out, seqs, heads):
             gots.append(out[q0:q0 + ql, h].float().cpu().numpy().ravel())
     return assert_close_attention(np.concatenate(gots), np.concatenate(refs),
                                   what=f"{w.name} sampled end to end")
+
+
+def upload_cache(pk, caches):
+    """Copy host (numpy) cache arrays into a PagedKV's device caches."""
+    for dst, src in zip((pk.k_cache, pk.v_cache, pk.k_scale, pk.v_scale), caches):
+        dst.copy_(torch.from_numpy(src))
+
+
+def attend_on_oracle_cache(w):
+    """The oracle writes the cache; the GPU attends over those same bytes.
+    Returns (GPU output, oracle output, device status)."""
+    from int4_token_head_gb300.paged import PagedKV
+    caches = oracle_write_history_and_step(w)
+    pk = PagedKV(w)
+    upload_cache(pk, caches)
+    q = w.queries("cpu")
+    out = torch.full((w.num_q_tokens, w.num_q_heads, w.head_size), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    pk.attend(q.cuda(), out)
+    torch.cuda.synchronize()
+    ref = oracle_attention(w, q, caches)
+    return out.float().cpu().numpy(), ref, int(pk.status.item())

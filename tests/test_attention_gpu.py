@@ -18,27 +18,14 @@ import torch
 from oracle import kvint4_oracle as O
 from int4_token_head_gb300 import _lib, synthetic
 from int4_token_head_gb300.paged import PagedKV
-from tests.helpers import assert_close_attention, corr, oracle_attention, oracle_write_history_and_step
+from tests.helpers import (assert_close_attention, attend_on_oracle_cache, corr, oracle_attention,
+                           oracle_write_history_and_step, upload_cache)
 
 pytestmark = pytest.mark.gpu
 
 
-def _upload(pk, caches):
-    for dst, src in zip((pk.k_cache, pk.v_cache, pk.k_scale, pk.v_scale), caches):
-        dst.copy_(torch.from_numpy(src))
-
-
-def _attend_on_oracle_cache(w):
-    caches = oracle_write_history_and_step(w)
-    pk = PagedKV(w)
-    _upload(pk, caches)
-    q = w.queries("cpu")
-    out = torch.full((w.num_q_tokens, w.num_q_heads, w.head_size), float("nan"), dtype=torch.bfloat16,
-                     device="cuda")
-    pk.attend(q.cuda(), out)
-    torch.cuda.synchronize()
-    ref = oracle_attention(w, q, caches)
-    return out.float().cpu().numpy(), ref, int(pk.status.item())
+_upload = upload_cache
+_attend_on_oracle_cache = attend_on_oracle_cache
 
 
 CASES = [
