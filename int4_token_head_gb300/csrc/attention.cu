@@ -106,9 +106,9 @@ struct Common {
   int64_t out_stride;
   int32_t* status;
   int tile_tokens;  // prefill: query tokens per 64-row tile
-  int hg;           // decode: kv heads per CTA (largest divisor of hkv <= 8)
+  int hg;           // decode: kv heads per CTA (largest divisor of hkv <= 4)
   int ng;           // decode: head groups per sequence (hkv / hg)
-  int nl;           // decode: lanes (a divisor of ng): CTA r serves the head groups = r mod nl
+  int nl;           // decode: lanes (a divisor of ng): CTA r serves the head groups g with g mod nl = r mod nl
   int np;           // decode: 16-key blocks per schedule position (1 or 2)
   int dcols;        // decode: query columns per block (8 / np); longer queries go to prefill
   long long max_items;  // capacity of the prefill item list

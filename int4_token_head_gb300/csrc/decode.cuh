@@ -51,7 +51,7 @@ struct DecGeom {
 // Walk over a lane's decode units (sequence i, head group grp, position kp).
 struct DecWalk {
   int i;      // index into the decode-sequence list
-  int grp;    // head group (= lane mod nl)
+  int grp;    // head group (grp mod nl = lane)
   int lane;   // the CTA's lane
   int kp;     // position within the sequence
   int npos;   // positions of the sequence
