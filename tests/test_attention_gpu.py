@@ -175,6 +175,25 @@ def test_bad_block_and_bad_sequence_are_reported_not_trapped():
     assert torch.all(out[1:3] == 7.0)  # rows of the invalid sequence untouched
 
 
+def test_sequences_without_queries_and_an_empty_batch():
+    """Sequences with q_len = 0 (one of them with no keys at all) contribute
+    no rows and leave the other sequences' rows exact; a batch with no
+    sequences (or no query tokens) enqueues nothing and returns OK."""
+    w = synthetic.custom_workload(8, 2, 128, [(0, 50), (1, 40), (0, 0), (3, 30), (0, 17)], seed=23)
+    got, ref, status = attend_on_oracle_cache(w)
+    assert status == 0
+    assert_close_attention(got, ref, what="sequences without queries")
+    pk = PagedKV(w)
+    q = torch.empty((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    none = torch.empty((0,), dtype=torch.int32, device="cuda")
+    _lib.attention(q, pk.k_cache, pk.v_cache, pk.k_scale, pk.v_scale, pk.block_table[:0], none,
+                   torch.zeros(1, dtype=torch.int32, device="cuda"), 0, 0, pk.softmax_scale, True, pk.signs, out,
+                   pk.workspace, dev_status=pk.status)
+    torch.cuda.synchronize()
+    assert pk.status.item() == 0
+
+
 @pytest.mark.parametrize("hq,hkv", [(8, 2), (4, 2)])
 def test_understated_max_query_len_is_reported_not_dropped(hq, hkv):
     """max_query_len sizes the launches (decode columns, whether a prefill
