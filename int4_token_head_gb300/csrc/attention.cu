@@ -109,7 +109,7 @@ struct Common {
   int hg;           // decode: kv heads per CTA (largest divisor of hkv <= 4)
   int ng;           // decode: head groups per sequence (hkv / hg)
   int nl;           // decode: lanes (a divisor of ng): CTA r serves the head groups g with g mod nl = r mod nl
-  int np;           // decode: 16-key blocks per schedule position (1 or 2)
+  int np;           // decode: 16-key blocks per schedule position (1, 2 or 4)
   int dcols;        // decode: query columns per block (8 / np); longer queries go to prefill
   long long max_items;  // capacity of the prefill item list
 };
@@ -420,8 +420,10 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
   // chunk at a time: all of a chunk's loads are issued before any of its
   // arithmetic (the chunk's largest maximum first, then every piece weighted
   // by 2^(m - that maximum)), so a segment's pieces cost one or two memory
-  // round trips instead of one each.  A piece's columns col, col + dcols, ...
-  // hold the same query over disjoint key blocks.
+  // round trips instead of one each.  With two blocks per position a
+  // piece's columns col and col + dcols hold the same query over disjoint key
+  // blocks; with four the decode merged them into column col.
+  const int nsub = c.np == 2 ? 2 : 1;
   constexpr int CH = 4;  // pieces per chunk
   int64_t chunk[CH];     // piece slots: -1 the direct slot, else the CTA slot index
   int nch = 0;
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kDecodeCols * 32) reduce_kernel(RedParams prm)
     for (int j = 0; j < CH; j++) {
 #pragma unroll
       for (int sub = 0; sub < 2; sub++) {
-        const bool use = j < nch && sub < c.np;
+        const bool use = j < nch && sub < nsub;
         const int cc = col + sub * c.dcols;
         const float* ml = ml_of(use ? chunk[j] : -1);
         const float* o = o_of(use ? chunk[j] : -1);
@@ -951,7 +953,7 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
                         (a.geo.sblk * 4) % 16 == 0 && a.geo.shead == 1;
   if (any_decode) {
     // one cache per kernel and head group: (blocks per position, ring depth, hg)
-    static PerContext<int> occ_cache[2][2][9];
+    static PerContext<int> occ_cache[4][2][9];
     auto occupancy = [&](auto kern, int np, int smem_max, int smem) -> int {
       if (smem > kMaxSmem) return 0;  // this ring does not fit
       int o = 0;
@@ -976,6 +978,20 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
       if (occ2 >= 1 && occ2 >= occ1) {  // 0: the paired ring does not fit
         c.np = 2;
         dec_occ = occ2;
+        // four blocks per position when every block needs at most 2 columns
+        // (one query per kv head: Phi-3's shape): the position's fixed work
+        // serves twice the keys.  INT4 with four-head CTAs and 16-byte scale
+        // rows only: the other instances of the four-block kernel spill
+        if constexpr (FMT == kFmtInt4) {
+          if (cols <= kDecodeCols / 4 && dec_deep) {
+            using E4 = DecodeEntry<D, 4, FMT>;
+            const int occ4 = occupancy(E4::kernel(true), 4, E4::smem(true, 8), E4::smem(true, c.hg));
+            if (occ4 >= 1 && occ4 >= occ2) {
+              c.np = 4;
+              dec_occ = occ4;
+            }
+          }
+        }
       }
     }
   } else {
@@ -1049,7 +1065,11 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
     const int num_ctas = dec_grid;
     const int threads = c.hg * 32;
     timing_begin(kTimedDecode, stream);
-    if (c.np == 2)
+    if (c.np == 4) {
+      if constexpr (FMT == kFmtInt4)
+        DecodeEntry<D, 4, FMT>::kernel(true)<<<(unsigned)grid, threads, DecodeEntry<D, 4, FMT>::smem(true, c.hg), stream>>>(
+            DecParams{c, pv, num_ctas});
+    } else if (c.np == 2)
       DecodeEntry<D, 2, FMT>::kernel(dec_deep)<<<(unsigned)grid, threads, DecodeEntry<D, 2, FMT>::smem(dec_deep, c.hg), stream>>>(
           DecParams{c, pv, num_ctas});
     else

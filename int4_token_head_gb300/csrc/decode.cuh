@@ -12,7 +12,8 @@
 // [j * COLS, (j + 1) * COLS) (COLS = 8 / NP >= the sequence's q_len * G), so
 // one softmax pass, one barrier and one V offset correction serve NP blocks.
 // Each column keeps its own running (m, l, o'); the reduce kernel merges the
-// NP columns of a query with the log-sum-exp rule like any other split.
+// NP columns of a query with the log-sum-exp rule like any other split
+// (with NP = 4 the piece's flush merges them first).
 template <int D, int NP, int FMT, bool DEEP = false>
 struct DecGeom {
   static constexpr int COLS = kDecodeCols / NP;  // query columns per block
@@ -27,7 +28,7 @@ struct DecGeom {
   // one more slot where the slots are small enough to keep four CTAs per SM
   // (swizzled 64-byte rows, or rows of at most 48 bytes), and stages a
   // block's scales as 16-byte rows of the group's four heads
-  static constexpr int NS = NP == 1 ? 4 : 2 * NP + (DEEP && (VSWZ || CB <= 48) ? 2 : 1);
+  static constexpr int NS = NP == 1 ? 4 : NP == 4 ? 8 : 2 * NP + (DEEP && (VSWZ || CB <= 48) ? 2 : 1);
   static constexpr int WAIT = NS - 2 * NP;  // copy groups that may stay pending at a wait
   static constexpr int KROW = CB;           // K tile row stride (bytes)
   // V tile row stride: an odd multiple of 16 bytes, so that the 8 rows of
@@ -418,6 +419,35 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
       a0 += __shfl_xor_sync(0xffffffffu, a0, o);
       a1 += __shfl_xor_sync(0xffffffffu, a1, o);
     }
+    // with four blocks per position the piece's blocks hold the same queries
+    // in columns c, c + 2, c + 4, c + 6 (lanes whose cq differs): merge them
+    // here with the log-sum-exp rule, so that only columns 0 and 1 leave the
+    // CTA and the reduce reads one partial per piece instead of four (with
+    // two blocks the reduce merges the pair: the extra code here measured
+    // 1631 -> 1641 us on the long-context decode)
+    float mm0 = m0, mm1 = m1;
+    if constexpr (NP == 4) {
+#pragma unroll
+      for (int x = G::COLS / 2; x < 4; x <<= 1) {
+        const float p0 = __shfl_xor_sync(0xffffffffu, mm0, x), p1 = __shfl_xor_sync(0xffffffffu, mm1, x);
+        const float n0 = fmaxf(mm0, p0), n1 = fmaxf(mm1, p1);
+        const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+        const float sa0 = fast_exp2(mm0 - u0), sb0 = fast_exp2(p0 - u0);
+        const float sa1 = fast_exp2(mm1 - u1), sb1 = fast_exp2(p1 - u1);
+        a0 = a0 * sa0 + __shfl_xor_sync(0xffffffffu, a0, x) * sb0;
+        a1 = a1 * sa1 + __shfl_xor_sync(0xffffffffu, a1, x) * sb1;
+#pragma unroll
+        for (int i = 0; i < G::KSTEPS; i++) {
+          oacc[i][0] = oacc[i][0] * sa0 + __shfl_xor_sync(0xffffffffu, oacc[i][0], x) * sb0;
+          oacc[i][2] = oacc[i][2] * sa0 + __shfl_xor_sync(0xffffffffu, oacc[i][2], x) * sb0;
+          oacc[i][1] = oacc[i][1] * sa1 + __shfl_xor_sync(0xffffffffu, oacc[i][1], x) * sb1;
+          oacc[i][3] = oacc[i][3] * sa1 + __shfl_xor_sync(0xffffffffu, oacc[i][3], x) * sb1;
+        }
+        mm0 = n0;
+        mm1 = n1;
+      }
+    }
+    if (NP == 4 && cq > 0) return;  // columns 2 .. 7 are merged into columns 0 and 1
     float* dst_o;
     float* dst_ml;
     if (first_piece) {
@@ -451,9 +481,9 @@ __device__ __forceinline__ void decode_body(const DecParams& prm) {
       }
     }
     if (g == 0) {
-      dst_ml[(2 * cq) * 2 + 0] = m0;
+      dst_ml[(2 * cq) * 2 + 0] = mm0;
       dst_ml[(2 * cq) * 2 + 1] = a0;
-      dst_ml[(2 * cq + 1) * 2 + 0] = m1;
+      dst_ml[(2 * cq + 1) * 2 + 0] = mm1;
       dst_ml[(2 * cq + 1) * 2 + 1] = a1;
     }
   };
@@ -638,9 +668,14 @@ __global__ void __launch_bounds__(256, 2) decode_kernel_i4d128(DecParams prm) {
 template <int D, int NP, int FMT>
 struct DecodeEntry {
   static constexpr bool HAS_DEEP =
-      FMT == kFmtInt4 && (D != 128 || DecGeom<D, NP, FMT, true>::NS != DecGeom<D, NP, FMT>::NS);
+      FMT == kFmtInt4 && (D != 128 || NP == 4 || DecGeom<D, NP, FMT, true>::NS != DecGeom<D, NP, FMT>::NS);
   static void (*kernel(bool deep))(DecParams) {
-    if constexpr (FMT == kFmtInt4 && D == 128) {
+    if constexpr (NP == 4) {  // launched with four-head CTAs and 16-byte scale rows only
+      static_assert(HAS_DEEP, "four blocks per position: INT4");
+      (void)deep;
+      if constexpr (D == 128) return decode_kernel_i4d128<NP, true>;
+      else return decode_kernel<D, NP, FMT, true>;
+    } else if constexpr (FMT == kFmtInt4 && D == 128) {
       if constexpr (HAS_DEEP) {
         if (deep) return decode_kernel_i4d128<NP, true>;
       }
