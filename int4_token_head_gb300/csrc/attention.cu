@@ -981,12 +981,15 @@ static int launch_attention_t(const AttnArgs& a, cudaStream_t stream) {
         // four blocks per position when every block needs at most 2 columns
         // (one query per kv head: Phi-3's shape): the position's fixed work
         // serves twice the keys.  INT4 with four-head CTAs and 16-byte scale
-        // rows only: the other instances of the four-block kernel spill
+        // rows only (the other instances of the four-block kernel spill),
+        // while at least three CTAs fit per SM (measured on GB300 at d = 128,
+        // G = 1 and 2, three CTAs of the eight-slot ring against four of the
+        // six-slot one: 1-3 % faster; d = 192 and 256 would drop to two)
         if constexpr (FMT == kFmtInt4) {
           if (cols <= kDecodeCols / 4 && dec_deep) {
             using E4 = DecodeEntry<D, 4, FMT>;
             const int occ4 = occupancy(E4::kernel(true), 4, E4::smem(true, 8), E4::smem(true, c.hg));
-            if (occ4 >= 1 && occ4 >= occ2) {
+            if (occ4 >= 1 && (occ4 >= occ2 || occ4 >= 3)) {
               c.np = 4;
               dec_occ = occ4;
             }
