@@ -5,14 +5,18 @@
 // (query token x q head of one kv group) in two halves of 128, the MMA's M;
 // 64 keys (four cache blocks) per step.  Sixteen warps in three roles, each
 // role running its own item loop so that a register budget can be set per
-// warpgroup (softmax 160 a thread, the others 96):
-//   * dequant warps (8-14): stage the step's code rows and scales with
-//     cp.async into one of two staging buffers (block ids loaded a step
-//     ahead), dequantise K into one of two f16 tiles (one where shared
-//     memory is short) and V into one of two, exactly (an INT4 nibble u
-//     becomes the f16 pattern 0x6400 | u = 1024 + u, an int8 byte u the
-//     pattern 0x64uu), and copy the step's K/V scales, block flags and the
-//     V-scale vote into a three-entry ring;
+// warpgroup (softmax 160 a thread, the others 96); the roles meet only at
+// mbarriers, so that the next item starts while the current one's epilogue
+// runs:
+//   * dequant warps (8-14): claim the next item (longest first) and pass it
+//     to the other roles through a two-entry ring; stage the step's code rows
+//     and scales with cp.async into one of two staging buffers (block ids
+//     loaded a step ahead), load the item's Q' rows once every score MMA of
+//     the previous item is complete, dequantise K into one of two f16 tiles
+//     (one where shared memory is short) and V into one of two, exactly (an
+//     INT4 nibble u becomes the f16 pattern 0x6400 | u = 1024 + u, an int8
+//     byte u the pattern 0x64uu), and copy the step's K/V scales, block flags
+//     and the V-scale vote into a three-entry ring;
 //   * MMA warp (15, lane 0 issues): S_h = Q_h K^T into TMEM columns
 //     [64h, 64h + 64); O_h += P_h V with P_h read from TMEM (the A operand
 //     of the MMA may live in tensor memory) into columns
@@ -26,7 +30,8 @@
 //     else tau = 0 (the exact running max); P' = p * v_scale is written back
 //     as f16 pairs over the row's S columns.  The epilogue normalises O,
 //     applies D (I_n (x) H_b) (.) / b in registers (packed f32x2 butterflies)
-//     and stages the bf16 rows over the Q' and K tiles for coalesced stores.
+//     and writes each thread's bf16 row straight from registers, leaving
+//     shared memory to the next item.
 // INT4 tiles keep each 8-element group in nibble order (elements 0,4,1,5,
 // 2,6,3,7: the two nibble lanes of a 32-bit word per f16x2, no byte
 // shuffles); the prep kernel stores Q' with the same permutation, which
@@ -42,7 +47,10 @@
 // wait at once, so a fault in the pipeline costs one time-out, not one
 // per step).  Each comes in a pair, per K/V tile or per half, so that no
 // barrier can complete twice before its waiter has seen the first:
+//   ifull[e] (dequant -> MMA, softmax)  item ring entry e written
+//   ifree[e] (MMA, softmax -> dequant)  item ring entry e read
 //   kfull[b] (dequant -> MMA)  K tile b and the step's ring entry written
+//                              (for an item's first step also its Q' rows)
 //   vfull[b] (dequant -> MMA)  V tile b written
 //   kfree[b] (MMA commit -> dequant) S0 and S1 that read K tile b complete
 //   vfree[b] (MMA commit -> dequant) PV0 and PV1 that read V tile b complete
@@ -50,7 +58,12 @@
 //   pfull[h] (softmax h -> MMA) P_h in TMEM, O_h rescaled if it had to be
 //   odone    (MMA commit -> softmax) the item's last PV complete
 // The ring entry of step j is rewritten at step j + 3, after S of step
-// j + 1 completed, which follows both halves' P of step j.
+// j + 1 completed, which follows both halves' P of step j.  Across items:
+// the next item's Q' rows and K tiles are written once the previous item's
+// last S is complete (kfree), its V tiles and first ring entries once the
+// previous item's last PV is (vfree: every P, so every softmax read of the
+// ring, came before it); its first PV overwrites O only after its first P,
+// which the softmax warps write after their epilogue's last TMEM load.
 
 constexpr int kWsRows = 256;  // query rows per item
 
@@ -79,9 +92,10 @@ struct WsGeom {
   static constexpr int RING = 2 * NK * 4 + 32;        // K scales, V scales, 4 block flags, 2 votes
   static constexpr int NRING = 3;                     // ring entries: step j's is rewritten at step j + 3
   static constexpr int TMEM_COLS = 128 + 2 * D <= 256 ? 256 : 512;
-  static constexpr int NBARS = 14;
+  static constexpr int NBARS = 18;
+  // item ring [2][4], abort flag, TMEM base
   static constexpr int fixed_bytes(int kbuf) {
-    return 1024 + QBYTES + (kbuf + 2) * KVBYTES + 2 * STG + NRING * RING + D * 4 + NBARS * 8 + 32;
+    return 1024 + QBYTES + (kbuf + 2) * KVBYTES + 2 * STG + NRING * RING + D * 4 + NBARS * 8 + 48;
   }
   // two K tiles (dequantise K(j + 1) while S(j) runs) where shared memory allows
   static constexpr int KBUF = fixed_bytes(2) <= 227 * 1024 ? 2 : 1;
@@ -150,10 +164,6 @@ __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.a
 
 // named barrier over the dequant warps only
 __device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 1, 224;\n" ::: "memory"); }
-// named barrier over the softmax warps and the MMA warp: the item's Q' tile is written
-__device__ __forceinline__ void q_sync() { asm volatile("bar.sync 2, 288;\n" ::: "memory"); }
-// named barrier over the softmax warps
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 3, 256;\n" ::: "memory"); }
 
 template <int D, int FMT>
 __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
@@ -175,15 +185,15 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
   uint8_t* const ring = stg + 2 * G::STG;     // two entries: K scales [64], V scales [64], flags [4], votes [2]
   float* const ssign = reinterpret_cast<float*>(ring + G::NRING * G::RING);
   uint64_t* const bars = reinterpret_cast<uint64_t*>(ssign + D);
-  int* const sitem = reinterpret_cast<int*>(bars + G::NBARS);  // item [4], abort flag
-  uint32_t* const tslot = reinterpret_cast<uint32_t*>(sitem + 6);
-  volatile int* const abort_flag = sitem + 4;
+  int* const sitem = reinterpret_cast<int*>(bars + G::NBARS);  // item ring [2][4], abort flag
+  uint32_t* const tslot = reinterpret_cast<uint32_t*>(sitem + 10);
+  volatile int* const abort_flag = sitem + 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // barrier indices
   // two of each pair: per K/V tile (full, free) or per half (S, P); every
   // barrier is waited once per completion, in order
-  enum { KFULL = 0, VFULL = 2, KFREE = 4, VFREE = 6, SFULL = 8, PFULL = 10, ODONE = 12, DRAIN = 13 };
+  enum { KFULL = 0, VFULL = 2, KFREE = 4, VFREE = 6, SFULL = 8, PFULL = 10, ODONE = 12, DRAIN = 13, IFULL = 14, IFREE = 16 };
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
   for (int i = tid; i < D; i += G::THREADS) ssign[i] = (ROT && c.signs[i] < 0) ? -1.f : 1.f;
   if (tid == 0) {
@@ -201,6 +211,10 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
     mbar_init(bar(PFULL + 1), 4);
     mbar_init(bar(ODONE), 1);
     mbar_init(bar(DRAIN), 1);
+    mbar_init(bar(IFULL), 1);
+    mbar_init(bar(IFULL + 1), 1);
+    mbar_init(bar(IFREE), 9);  // the eight softmax warps and the MMA warp
+    mbar_init(bar(IFREE + 1), 9);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -210,35 +224,34 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
   tc_fence_after();
   const uint32_t tmem = *tslot;
   // registers: the launch gives 128 a thread to all four warpgroups (65,536);
-  // the softmax warpgroups take 168, the dequant/MMA ones keep 88
-  // (2 x 128 x 168 + 2 x 128 x 88 = 65,536: the increase can always be met)
+  // the softmax warpgroups take 160, the dequant/MMA ones keep 96
+  // (2 x 128 x 160 + 2 x 128 x 96 = 65,536: the increase can always be met)
   const int n_items = pv.plan[1];
-  // each role runs its own item loop (the same items, the same CTA-wide
-  // barriers), so that the register budget set for its warpgroups covers
-  // only its own code
+  // each role runs its own item loop (the same items, handed over through
+  // the item ring), so that the register budget set for its warpgroups
+  // covers only its own code
   static_assert(G::THREADS == 512, "four warpgroups");
+  auto item_at = [&](int e) { return make_int4(sitem[4 * e], sitem[4 * e + 1], sitem[4 * e + 2], sitem[4 * e + 3]); };
+  // a consumer's wait for ring entry e, warp-uniform (a wait that gives up
+  // on the abort flag may do so in some lanes only)
+  auto take_item = [&](int e, uint32_t& ph, int4& item) {
+    const bool ok = __all_sync(0xffffffffu, ws_wait(bar(IFULL + e), (ph >> e) & 1, abort_flag, c.status));
+    ph ^= 1u << e;
+    if (!ok) return false;
+    item = item_at(e);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(IFREE + e));
+    return item.x >= 0;
+  };
   if (warp < 8) {
     // ======================= softmax warpgroups =======================
     regs_inc<160>();
     // phase bits of the barriers the role waits on (one completion per wait)
-    uint32_t ph_sfull = 0, ph_odone = 0;
-    // the next item, longest first: (prefill sequence, kv head, tile,
-    // blocks), claimed and looked up by thread 0 when the current item's
-    // last PV is complete, so that the claim's atomic and search overlap the
-    // epilogue (claimed any earlier, items would wait behind busy CTAs)
-    auto claim = [&]() -> int4 {
-      return prefill_item(c, pv, *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1), n_items);
-    };
-    int4 next_item = make_int4(-1, 0, 0, 0);
-    if (tid == 0) next_item = claim();
+    uint32_t ph_sfull = 0, ph_odone = 0, ph_ifull = 0;
 #pragma unroll 1
-    while (true) {
-      if (tid == 0) {
-        sitem[0] = next_item.x; sitem[1] = next_item.y; sitem[2] = next_item.z; sitem[3] = next_item.w;
-      }
-      __syncthreads();
-      const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
-      if (item.x < 0) break;
+    for (int itc = 0;; itc++) {
+      int4 item;
+      if (!take_item(itc & 1, ph_ifull, item)) break;
       const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
       const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
       const int L = c.seq_lens[seq], ctx = L - ql;
@@ -252,27 +265,6 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
       const int r = tid;  // row of the item (half hf holds rows [128 hf, 128 hf + 128))
       const int j = (int)c.gdiv.div((uint32_t)r);  // token of the row within the item
       const bool rok = r < nrows;
-      constexpr int CPR = D / 8;  // 16-byte chunks of a row (Q' and the output)
-      {
-        // Q' rows of the item, consecutive threads on consecutive 16-byte
-        // chunks (the rows of one token's group are contiguous)
-#pragma unroll 4
-        for (int u = tid; u < ROWS * CPR; u += 256) {
-          const int rr = u / CPR, ch = u - rr * CPR;
-          uint8_t* d = sQ + sw128(ROWS, rr, ch);
-          if (rr < nrows) {
-            const int tj = (int)c.gdiv.div((uint32_t)rr), tjj = rr - tj * c.group;
-            cp_async16(d, reinterpret_cast<const uint8_t*>(
-                              pv.qrot + ((long long)(q0 + tok0 + tj) * c.hq + h * c.group + tjj) * D) + ch * 16);
-          } else {
-            *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        cp_async_commit();
-        cp_async_wait<0>();  // (INT4 q' arrives in the tiles' nibble order)
-      }
-      fence_proxy_async_smem();  // Q' is read by the tensor cores
-      q_sync();
       const int qp = ctx + tok0 + (rok ? j : 0);
       const int lim = c.causal ? min(L, qp + 1) : L;
       const int lo = window_lo(c, qp);
@@ -386,17 +378,34 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
       // ---- epilogue: normalise, inverse rotation (INT4), bf16 store ----
       ws_wait(bar(ODONE), ph_odone, abort_flag, c.status);
       ph_odone ^= 1;
-      if (tid == 0) next_item = claim();
       tc_fence_after();
       const bool live = l_run > 0.f;  // a row that saw no usable key is written as zeros
       const float inv = live ? 1.f / (l_run * (ROT ? (float)B : 1.f)) : 0.f;
-      // the output rows are staged as bf16 over the Q' and K tiles (every
-      // MMA of the item is complete) at a padded stride, then written out
-      // with consecutive threads on consecutive 16-byte chunks
-      constexpr int OSTR = 2 * D + 16;
-      static_assert(ROWS * OSTR <= G::QBYTES + G::KVBYTES, "output staging");
-      uint8_t* const orow = sQ + r * OSTR;
-      auto put8 = [&](int col, const float (&y)[8]) {
+      // The output leaves straight from registers (shared memory is left to
+      // the next item, whose Q' and first tiles load meanwhile).  A thread
+      // holds its row, and the rows of a lane quad are the group's q heads of
+      // one token (contiguous when the group has four heads): where a whole
+      // 64-column group is transformed at once, the quad transposes its
+      // 32-byte units so that each store instruction writes a full 128-byte
+      // run per quad; elsewhere a thread stores its own row 32 bytes at a time.
+      uint16_t* const orow =
+          c.out + (long long)(q0 + tok0 + (rok ? j : 0)) * c.out_stride + (long long)(h * c.group + (rok ? r - j * c.group : 0)) * D;
+      const int qi = lane & 3;  // position in the lane quad
+      // the output rows start on 32-byte boundaries (else two 16-byte stores)
+      const bool al32 = ((reinterpret_cast<uintptr_t>(c.out) | (uintptr_t)(c.out_stride * 2) | (uintptr_t)(D * 2)) & 31) == 0;
+      auto st32 = [&](uint16_t* dst, const uint4& a, const uint4& b) {
+        if (al32) {
+          asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(dst), "r"(a.x), "r"(a.y), "r"(a.z),
+                       "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                       : "memory");
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = a;
+          reinterpret_cast<uint4*>(dst)[1] = b;
+        }
+      };
+      // bf16 words of the 8 outputs from column col: normalised, signs
+      // applied, zeros for a row that saw no usable key
+      auto cvt8 = [&](int col, const float* y) {
         const float4 s0 = *reinterpret_cast<const float4*>(ssign + col);
         const float4 s1 = *reinterpret_cast<const float4*>(ssign + col + 4);
         const float2 iv = make_float2(inv, inv);
@@ -406,12 +415,25 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
         const float2 z3 = __fmul2_rn(__fmul2_rn(make_float2(y[6], y[7]), iv), make_float2(s1.z, s1.w));
         const uint4 w = make_uint4(pack_bf16x2_rn(z0.x, z0.y), pack_bf16x2_rn(z1.x, z1.y), pack_bf16x2_rn(z2.x, z2.y),
                                    pack_bf16x2_rn(z3.x, z3.y));
-        *reinterpret_cast<uint4*>(orow + col * 2) = live ? w : make_uint4(0, 0, 0, 0);
+        return live ? w : make_uint4(0, 0, 0, 0);
+      };
+      // 16 outputs from column col (a multiple of 16) of this thread's row
+      auto put16 = [&](int col, const float (&y)[16]) {
+        const uint4 a = cvt8(col, y), b = cvt8(col + 8, y + 8);
+        if (rok) st32(orow + col, a, b);
       };
       // TMEM column slot of natural element i within a chunk: INT4 columns are
       // in nibble order, so elements i and i + 4 (i % 8 < 4) sit in slots s, s + 1
       auto slot = [](int i) { return FMT == kFmtInt4 ? (i & ~7) + (i & 3) * 2 + ((i >> 2) & 1) : i; };
       constexpr int CHUNK = (ROT && B > 32) ? (B > 64 ? 64 : B) : 32;  // columns transformed in registers
+      constexpr bool QUAD = CHUNK == 64 && !(ROT && B > 64);              // whole 64-column groups stored here
+      // the quad's rows (lane quad position t): output row, or null past the item's rows
+      uint16_t* qrow[4];
+#pragma unroll
+      for (int t = 0; t < 4; t++) {
+        const unsigned long long pr = rok ? reinterpret_cast<unsigned long long>(orow) : 0ull;
+        qrow[t] = reinterpret_cast<uint16_t*>(__shfl_sync(0xffffffffu, pr, (lane & ~3) | t));
+      }
 #pragma unroll 1
       for (int base = 0; base < D; base += CHUNK) {
         float o[CHUNK];  // TMEM column order
@@ -453,13 +475,49 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
           for (int i = 0; i < CHUNK; i++) nat[i] = o[slot(i)];
 #pragma unroll
           for (int cc = 0; cc < CHUNK / 32; cc++) tmem_st32(tO + base + cc * 32, *reinterpret_cast<float(*)[32]>(nat + cc * 32));
+        } else if constexpr (QUAD) {
+          // u[t]: 32-byte unit t (columns base + 16 t ..) of this thread's row
+          uint4 u[4][2];
+#pragma unroll
+          for (int t = 0; t < 4; t++) {
+            float y[16];
+#pragma unroll
+            for (int e = 0; e < 16; e++) y[e] = o[slot(16 * t + e)];
+            u[t][0] = cvt8(base + 16 * t, y);
+            u[t][1] = cvt8(base + 16 * t + 8, y + 8);
+          }
+          // 4 x 4 transpose over the quad (row = quad position, column =
+          // unit), by two exchanges with the partners at xor 1 and xor 2:
+          // afterwards u[t] is unit qi of the quad's row t
+#pragma unroll
+          for (int x = 1; x <= 2; x <<= 1) {
+            const bool hi = (qi & x) != 0;
+#pragma unroll
+            for (int a = 0; a < 4; a++) {
+              if (a & x) continue;  // pairs (a, a + x)
+#pragma unroll
+              for (int k = 0; k < 2; k++) {
+                const uint4 snd = hi ? u[a][k] : u[a + x][k];
+                uint4 rcv;
+                rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, x);
+                rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, x);
+                rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, x);
+                rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, x);
+                if (hi) u[a][k] = rcv;
+                else u[a + x][k] = rcv;
+              }
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < 4; t++)
+            if (qrow[t] != nullptr) st32(qrow[t] + base + 16 * qi, u[t][0], u[t][1]);
         } else {
 #pragma unroll
-          for (int i = 0; i < CHUNK; i += 8) {
-            float y[8];
+          for (int i = 0; i < CHUNK; i += 16) {
+            float y[16];
 #pragma unroll
-            for (int e = 0; e < 8; e++) y[e] = o[slot(i + e)];
-            put8(base + i, y);
+            for (int e = 0; e < 16; e++) y[e] = o[slot(i + e)];
+            put16(base + i, y);
           }
         }
       }
@@ -474,53 +532,77 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
             tmem_ld32(tO + base + q, a);
             tmem_ld32(tO + base + 64 + q, b2);
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              float y0[8], y1[8];
+            for (int i = 0; i < 32; i += 16) {
+              float y0[16], y1[16];
 #pragma unroll
-              for (int e = 0; e < 8; e++) {
+              for (int e = 0; e < 16; e++) {
                 y0[e] = a[i + e] + b2[i + e];
                 y1[e] = a[i + e] - b2[i + e];
               }
-              put8(base + q + i, y0);
-              put8(base + 64 + q + i, y1);
+              put16(base + q + i, y0);
+              put16(base + 64 + q + i, y1);
             }
           }
         }
       }
-      softmax_sync();  // every row is staged
-#pragma unroll 4
-      for (int u = tid; u < nrows * CPR; u += 256) {
-        const int rr = u / CPR, ch = u - rr * CPR;
-        const int tj = (int)c.gdiv.div((uint32_t)rr), tjj = rr - tj * c.group;
-        *reinterpret_cast<uint4*>(c.out + (long long)(q0 + tok0 + tj) * c.out_stride + (long long)(h * c.group + tjj) * D +
-                                  ch * 8) = *reinterpret_cast<const uint4*>(sQ + rr * OSTR + ch * 16);
-      }
-      // item end: every role is done with TMEM, the tiles and the ring
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
     }
   } else {
     // ==================== dequant and MMA warpgroups ====================
     regs_dec<96>();
     uint32_t ph_kfull = 0, ph_vfull = 0, ph_kfree = 0, ph_vfree = 0, ph_pfull = 0;
+    if (warp < 15) {
+      // ================= dequant warps =================
+      const int dt = tid - 256;
+      uint32_t ph_ifree = 0;
+      int prev_steps = 0;  // steps of the previous item
+      // the previous item's MMA completions that its step loop did not wait
+      // for: the S of its last KBUF steps (and with them every S, so every
+      // read of its Q' and K tiles), the last PV of each V tile (and with it
+      // every P, so every softmax read of its ring entries)
+      auto wait_kfree_tail = [&](int ns) {
+        for (int st = ns - G::KBUF < 0 ? 0 : ns - G::KBUF; st < ns; st++) {
+          ws_wait(bar(KFREE + (st & 1)), (ph_kfree >> (st & 1)) & 1, abort_flag, c.status);
+          ph_kfree ^= 1u << (st & 1);
+        }
+      };
+      auto wait_vfree_tail = [&](int ns) {
+        for (int b = 0; b < 2 && b < ns; b++) {
+          ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
+          ph_vfree ^= 1u << b;
+        }
+      };
 #pragma unroll 1
-    while (true) {
-      __syncthreads();
-      const int4 item = make_int4(sitem[0], sitem[1], sitem[2], sitem[3]);
-      if (item.x < 0) break;
-      const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
-      const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
-      const int L = c.seq_lens[seq], ctx = L - ql;
-      const int tok0 = tile * c.tile_tokens;
-      const int ntok = min(c.tile_tokens, ql - tok0);
-      const int nrows = ntok * c.group;
-      const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
-      const int nsteps = (nkb - kb0 + 3) / 4;
-      (void)nrows;
-      if (warp < 15) {
-        // ================= dequant warps =================
-        const int dt = tid - 256;
+      for (int itc = 0;; itc++) {
+        const int e = itc & 1;
+        if (dt == 0) {
+          // claim the next item and publish it in ring entry e, whose
+          // previous item (itc - 2) every consumer has read
+          if (itc >= 2) {
+            ws_wait(bar(IFREE + e), (ph_ifree >> e) & 1, abort_flag, c.status);
+            ph_ifree ^= 1u << e;
+          }
+          const int4 it = prefill_item(c, pv, *abort_flag ? n_items : atomicAdd(&pv.plan[2], 1), n_items);
+          sitem[4 * e] = it.x;
+          sitem[4 * e + 1] = it.y;
+          sitem[4 * e + 2] = it.z;
+          sitem[4 * e + 3] = it.w;
+          mbar_arrive(bar(IFULL + e));
+        }
+        dq_sync();
+        const int4 item = item_at(e);
+        if (item.x < 0) {
+          wait_kfree_tail(prev_steps);
+          wait_vfree_tail(prev_steps);
+          break;
+        }
+        const int seq = item.x, h = item.y, tile = item.z, nkb = item.w;
+        const int q0 = c.qsl[seq], ql = c.qsl[seq + 1] - q0;
+        const int L = c.seq_lens[seq], ctx = L - ql;
+        const int tok0 = tile * c.tile_tokens;
+        const int ntok = min(c.tile_tokens, ql - tok0);
+        const int nrows = ntok * c.group;
+        const int kb0 = window_lo(c, ctx + tok0) >> 4;  // blocks before the earliest row's window are skipped
+        const int nsteps = (nkb - kb0 + 3) / 4;
         // staging is done by the first 128 dequant threads: thread (block b4,
         // K/V, row) copies one code row and its scale; the block id of a step
         // is loaded a step before its copies are issued
@@ -573,16 +655,45 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
             }
           }
         };
+        // the first two steps' copies go out at once (the staging buffers are
+        // free: the previous item's last dequantisation is done)
         issue(0, stg, block_of(0));
         cp_async_commit();
         if (nsteps > 1) issue(1, stg + G::STG, block_of(1));
         cp_async_commit();
         int blk_next = block_of(2);
+        // Q' rows of the item, once every S of the previous item is complete;
+        // consecutive threads on consecutive 16-byte chunks (the rows of one
+        // token's group are contiguous; INT4 q' is stored in the tiles'
+        // nibble order).  They land with step 0's copies, before kfull.
+        wait_kfree_tail(prev_steps);
+        {
+          constexpr int CPR = D / 8;  // 16-byte chunks of a row
+#pragma unroll 4
+          for (int u = dt; u < ROWS * CPR; u += 32 * G::DQ_WARPS) {
+            const int rr = u / CPR, ch = u - rr * CPR;
+            uint8_t* d = sQ + sw128(ROWS, rr, ch);
+            if (rr < nrows) {
+              const int tj = (int)c.gdiv.div((uint32_t)rr), tjj = rr - tj * c.group;
+              cp_async16(d, reinterpret_cast<const uint8_t*>(
+                                pv.qrot + ((long long)(q0 + tok0 + tj) * c.hq + h * c.group + tjj) * D) + ch * 16);
+            } else {
+              *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          cp_async_commit();
+        }
+        // V tiles and the first ring entries: every PV of the previous item
+        // is complete
+        wait_vfree_tail(prev_steps);
 #pragma unroll 1
         for (int j = 0; j < nsteps; j++) {
           const int b = j & 1;
           uint8_t* const sb = stg + b * G::STG;
-          cp_async_wait<1>();
+          if (j == 0)
+            cp_async_wait<0>();  // with the item's Q' rows
+          else
+            cp_async_wait<1>();
           dq_sync();  // every thread's copies of step j have landed
           // the K tile of step j is free once S of step j - KBUF is complete;
           // the ring entry of step j once the softmax of step j - 3 is (S of
@@ -626,24 +737,28 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
           cp_async_commit();
           blk_next = block_of(j + 3);
         }
-        cp_async_wait<0>();
-        // the completions not waited for above: kfree of the last step, vfree of the last use of each V tile
-        for (int st = nsteps - G::KBUF < 0 ? 0 : nsteps - G::KBUF; st < nsteps; st++) {
-          ws_wait(bar(KFREE + (st & 1)), (ph_kfree >> (st & 1)) & 1, abort_flag, c.status);
-          ph_kfree ^= 1u << (st & 1);
-        }
-        for (int b = 0; b < 2 && b < nsteps; b++) {
-          ws_wait(bar(VFREE + b), (ph_vfree >> b) & 1, abort_flag, c.status);
-          ph_vfree ^= 1u << b;
-        }
-      } else {
-        // ================= MMA warp (lane 0 issues, the warp waits together) =================
-        const bool leader = lane == 0;
-        // operand descriptors: the start address is the low 14-bit field of
-        // (address >> 4), so an offset below 256 KB adds to the descriptor
-        const uint64_t dq = umma_desc(smem_addr(sQ), 16, 1024);
-        const uint64_t dk = umma_desc(smem_addr(sK), 16, 1024);
-        const uint64_t dv = umma_desc(smem_addr(sV), NK * 128, 1024);
+        if (nsteps == 0) cp_async_wait<0>();  // no step waited for this item's Q' copies
+        prev_steps = nsteps;
+      }
+      cp_async_wait<0>();
+    } else {
+      // ================= MMA warp (lane 0 issues, the warp waits together) =================
+      const bool leader = lane == 0;
+      uint32_t ph_ifull = 0;
+      // operand descriptors: the start address is the low 14-bit field of
+      // (address >> 4), so an offset below 256 KB adds to the descriptor
+      const uint64_t dq = umma_desc(smem_addr(sQ), 16, 1024);
+      const uint64_t dk = umma_desc(smem_addr(sK), 16, 1024);
+      const uint64_t dv = umma_desc(smem_addr(sV), NK * 128, 1024);
+#pragma unroll 1
+      for (int itc = 0;; itc++) {
+        int4 item;
+        if (!take_item(itc & 1, ph_ifull, item)) break;
+        const int seq = item.x, tile = item.z, nkb = item.w;
+        const int ql = c.qsl[seq + 1] - c.qsl[seq];
+        const int ctx = c.seq_lens[seq] - ql;
+        const int kb0 = window_lo(c, ctx + tile * c.tile_tokens) >> 4;  // blocks before the earliest row's window are skipped
+        const int nsteps = (nkb - kb0 + 3) / 4;
         // S_h = Q_h K^T over the head dimension into TMEM columns [64h, 64h + 64)
         auto issue_s = [&](int hh, int st) {
           if (leader) {
@@ -668,7 +783,7 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
           if (leader) umma_commit(bar(i));
           __syncwarp();
         };
-        q_sync();  // the softmax warps have written Q'
+        // kfull of step 0 also covers the item's Q' rows
         if (nsteps > 0) {
           ws_wait(bar(KFULL), ph_kfull & 1, abort_flag, c.status);
           ph_kfull ^= 1;
@@ -713,10 +828,6 @@ __global__ void __launch_bounds__(16 * 32, 1) prefill_ws_kernel(PreParams prm) {
         }
         commit(ODONE);
       }
-      // item end: every role is done with TMEM, the tiles and the ring
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
     }
   }
   if (warp == 15) {
