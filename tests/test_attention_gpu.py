@@ -297,3 +297,36 @@ def test_attention_is_deterministic(case, fmt):
         else:
             assert torch.equal(out, first), name
     assert pk.status.item() == 0
+
+
+@pytest.mark.parametrize("fmt", ["int4", "int8"])
+@pytest.mark.parametrize("d", [64, 96, 128, 192, 256])
+def test_strided_offset_q_and_out_match_contiguous(d, fmt):
+    """q and out as views with a token stride of Hq*d + 24 elements and a
+    start 16 bytes past a 256-byte boundary (legal: 16-byte aligned, stride a
+    multiple of 8; neither is 32-byte aligned) give the bit-identical output
+    of contiguous tensors, through prefill, decode and reduce, and write
+    nothing between the rows."""
+    seqs = [(150, 150), (1, 700), (37, 300), (1, 1500), (64, 64), (2, 90)]
+    w = synthetic.custom_workload(16, 4, d, seqs, seed=31)
+    pk = PagedKV(w, fmt=fmt)
+    pk.populate_history()
+    q, k_new, v_new, slots = pk.step_inputs()
+    pk.write(k_new, v_new, slots)
+    T, hq = w.num_q_tokens, w.num_q_heads
+    ref = torch.empty((T, hq, d), dtype=torch.bfloat16, device="cuda")
+    pk.attend(q, ref)
+    row, off = hq * d + 24, 8
+    qbuf = torch.zeros(off + T * row, dtype=torch.bfloat16, device="cuda")
+    qv = torch.as_strided(qbuf, (T, hq, d), (row, d, 1), storage_offset=off)
+    qv.copy_(q)
+    sentinel = torch.tensor(-12345.0, dtype=torch.bfloat16)
+    obuf = torch.full((off + T * row,), float(sentinel), dtype=torch.bfloat16, device="cuda")
+    ov = torch.as_strided(obuf, (T, hq, d), (row, d, 1), storage_offset=off)
+    pk.attend(qv, ov)
+    torch.cuda.synchronize()
+    assert int(pk.status.item()) == 0
+    assert torch.equal(ov.contiguous().view(torch.int16), ref.view(torch.int16))
+    written = torch.zeros(off + T * row, dtype=torch.bool, device="cuda")
+    torch.as_strided(written, (T, hq, d), (row, d, 1), storage_offset=off).fill_(True)
+    assert torch.all(obuf[~written] == sentinel)
