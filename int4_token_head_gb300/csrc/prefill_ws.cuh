@@ -30,7 +30,9 @@
 //     else tau = 0 (the exact running max); P' = p * v_scale is written back
 //     as f16 pairs over the row's S columns.  The epilogue normalises O,
 //     applies D (I_n (x) H_b) (.) / b in registers (packed f32x2 butterflies)
-//     and writes each thread's bf16 row straight from registers, leaving
+//     and writes the bf16 rows straight from registers (where the transform
+//     comes in 64-column groups, each lane quad first transposes its 32-byte
+//     units so that one store writes a 128-byte run per quad), leaving
 //     shared memory to the next item.
 // INT4 tiles keep each 8-element group in nibble order (elements 0,4,1,5,
 // 2,6,3,7: the two nibble lanes of a 32-bit word per f16x2, no byte
@@ -45,8 +47,9 @@
 // Hand-offs are mbarriers (every wait bounded; a wait that runs out sets
 // KV_INT4_DEV_TIMEOUT and a CTA-wide abort flag that ends every later
 // wait at once, so a fault in the pipeline costs one time-out, not one
-// per step).  Each comes in a pair, per K/V tile or per half, so that no
-// barrier can complete twice before its waiter has seen the first:
+// per step).  Each comes in a pair, per K/V tile, per half or per item ring
+// entry, so that no barrier can complete twice before its waiter has seen
+// the first:
 //   ifull[e] (dequant -> MMA, softmax)  item ring entry e written
 //   ifree[e] (MMA, softmax -> dequant)  item ring entry e read
 //   kfull[b] (dequant -> MMA)  K tile b and the step's ring entry written
